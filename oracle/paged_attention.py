@@ -1,0 +1,201 @@
+"""CPU oracle for batch-invariant paged-KV attention over one flat ragged step.
+
+TEST INFRASTRUCTURE, NOT PART OF THE PRODUCT. Only the tests, the smoke check
+and the benchmark's CPU-baseline leg may import or call this module. It shares
+no code with the CUDA library and imports nothing from it.
+
+It is the plain definition, written for a reader to check by eye:
+
+* write  -- byte copy of every new K/V row into ``cache[slot // bs, slot % bs]``
+  ("P3: native paged-KV continuous-batching sampler", section Design, paged.py:
+  PagedKVCache copy-free append that scatters into (block, offset));
+* gather -- contiguous ``[L, Hkv, D]`` keys of one sequence, read block by
+  block through its block-table row (same section: ``gather()`` returns the
+  sequence's keys in one contiguous layout whatever else is in the batch);
+* attend -- for every query row, softmax attention over exactly its own keys
+  (same section: TorchPagedAttention 'row' mode, one attention per query row;
+  the step first writes the new K/V, then returns ``[T, H, D]``), causal by
+  absolute position inside a prefill chunk, query head h reading kv head
+  ``h // (H / Hkv)`` (blocked GQA map, "Tensor parallelism" Design, GQA).
+
+Everything is widened exactly to float64 before any arithmetic. bf16 data is
+carried as raw uint16 bit patterns (bfloat16 is the upper half of an IEEE
+binary32, so widening is a 16-bit shift); fp32 data as float32.
+
+Readings where the pages leave a step open (listed with their reasons in the
+design notes of this repository):
+  * ``ctx_lens`` counts the keys after this step's write, so a lane with
+    ``q_len`` rows has its row j at position ``ctx - q_len + j``;
+  * a negative slot means "no write" (padding);
+  * ``scale`` is the caller's float32 value, widened.
+"""
+from __future__ import annotations
+
+import math
+
+import numpy as np
+
+
+# ---------------------------------------------------------------------------
+# element widening
+# ---------------------------------------------------------------------------
+
+def widen(x, dtype: str) -> np.ndarray:
+    """Exact float64 values of stored elements ('f32': float32, 'bf16': uint16 bits)."""
+    x = np.asarray(x)
+    if dtype == "f32":
+        if x.dtype != np.float32:
+            raise TypeError("f32 data must be float32")
+        return x.astype(np.float64)
+    if dtype == "bf16":
+        if x.dtype != np.uint16:
+            raise TypeError("bf16 data must be carried as uint16 bit patterns")
+        return (x.astype(np.uint32) << np.uint32(16)).view(np.float32).astype(np.float64)
+    raise ValueError(f"unknown dtype {dtype!r}")
+
+
+# ---------------------------------------------------------------------------
+# memory accounting
+# ---------------------------------------------------------------------------
+
+def kv_bytes_per_token(layers: int, kv_heads: int, head_dim: int, elem_bytes: int,
+                       tp_degree: int = 1) -> int:
+    """K and V bytes one token occupies across all layers on one rank.
+
+    "P3: native paged-KV continuous-batching sampler", section Memory
+    accounting: layers x 2 (K and V) x kv heads x head dim x element bytes;
+    kv heads are split evenly over tensor-parallel ranks ("Tensor
+    parallelism", Design: the cache is sharded by kv head).
+    """
+    if kv_heads % tp_degree:
+        raise ValueError("tp degree must divide the kv heads")
+    return layers * 2 * (kv_heads // tp_degree) * head_dim * elem_bytes
+
+
+# ---------------------------------------------------------------------------
+# write
+# ---------------------------------------------------------------------------
+
+def slot_location(slot: int, block_size: int):
+    """(block, offset) that a flat slot number names."""
+    return slot // block_size, slot % block_size
+
+
+def write_kv(k_cache, v_cache, k_new, v_new, slot_mapping, block_size: int):
+    """Return copies of the caches with every new row stored at its slot.
+
+    Bytes move unchanged; rows whose slot is negative are skipped.
+    Caches are ``[NB, bs, Hkv, D]``, new rows ``[T, Hkv, D]``.
+    """
+    k_out = np.array(k_cache, copy=True)
+    v_out = np.array(v_cache, copy=True)
+    for t, slot in enumerate(np.asarray(slot_mapping, dtype=np.int64)):
+        if slot < 0:
+            continue
+        blk, off = slot_location(int(slot), block_size)
+        k_out[blk, off] = k_new[t]
+        v_out[blk, off] = v_new[t]
+    return k_out, v_out
+
+
+# ---------------------------------------------------------------------------
+# gather
+# ---------------------------------------------------------------------------
+
+def gather(cache, table_row, ctx_len: int, block_size: int) -> np.ndarray:
+    """Contiguous ``[ctx_len, Hkv, D]`` keys (or values) of one sequence."""
+    rows = []
+    for p in range(ctx_len):
+        blk = int(table_row[p // block_size])
+        rows.append(cache[blk, p % block_size])
+    if not rows:
+        return np.zeros((0,) + tuple(cache.shape[2:]), dtype=cache.dtype)
+    return np.stack(rows)
+
+
+# ---------------------------------------------------------------------------
+# attend
+# ---------------------------------------------------------------------------
+
+def kv_head_of(h: int, H: int, Hkv: int) -> int:
+    """Blocked GQA map: query heads [g*k, g*k + g) read kv head k, g = H / Hkv."""
+    return h // (H // Hkv)
+
+
+def visible_keys(position: int) -> int:
+    """A row at absolute position p attends keys 0..p (causal)."""
+    return position + 1
+
+
+def softmax_weights(scores: np.ndarray) -> np.ndarray:
+    """exp(s - max s) / sum exp(s - max s), in float64."""
+    m = np.max(scores)
+    e = np.exp(scores - m)
+    return e / np.sum(e)
+
+
+def attend_row(q_row, K, V, position: int, scale: float):
+    """Output ``[H, D]`` (float64) of one query row.
+
+    q_row ``[H, D]``, K and V ``[L, Hkv, D]``, all float64.
+    """
+    H, D = q_row.shape
+    Hkv = K.shape[1]
+    n = visible_keys(position)
+    out = np.empty((H, D), dtype=np.float64)
+    for h in range(H):
+        kv = kv_head_of(h, H, Hkv)
+        s = scale * (K[:n, kv, :] @ q_row[h])
+        w = softmax_weights(s)
+        out[h] = w @ V[:n, kv, :]
+    return out
+
+
+def row_weights(q_row, K, position: int, scale: float, h: int) -> np.ndarray:
+    """Softmax weights of head h of one row (for invariant checks)."""
+    H = q_row.shape[0]
+    kv = kv_head_of(h, H, K.shape[1])
+    n = visible_keys(position)
+    return softmax_weights(scale * (K[:n, kv, :] @ q_row[h]))
+
+
+def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens,
+              scale: float, dtype: str, block_size: int,
+              slot_mapping=None, k_new=None, v_new=None, rows=None):
+    """Reference output of one flat ragged step, float64 ``[T, H, D]``.
+
+    When new rows are given they are written first (the step writes, then
+    attends). ``rows`` optionally restricts the work to a subset of flat
+    rows (others are left NaN), for sampled checks of large steps.
+    Returns (out, k_cache_after, v_cache_after).
+    """
+    if k_new is not None:
+        k_cache, v_cache = write_kv(k_cache, v_cache, k_new, v_new,
+                                    slot_mapping, block_size)
+    scale = float(np.float32(scale))
+    T, H, D = q.shape
+    cu = np.asarray(cu_seqlens_q, dtype=np.int64)
+    ctx = np.asarray(ctx_lens, dtype=np.int64)
+    B = ctx.shape[0]
+    want = None if rows is None else set(int(r) for r in rows)
+    out = np.full((T, H, D), np.nan, dtype=np.float64)
+    for b in range(B):
+        q_len = int(cu[b + 1] - cu[b])
+        if q_len == 0:
+            continue
+        lane_rows = [int(cu[b]) + j for j in range(q_len)]
+        if want is not None and not want.intersection(lane_rows):
+            continue
+        K = widen(gather(k_cache, block_tables[b], int(ctx[b]), block_size), dtype)
+        V = widen(gather(v_cache, block_tables[b], int(ctx[b]), block_size), dtype)
+        for j, r in enumerate(lane_rows):
+            if want is not None and r not in want:
+                continue
+            position = int(ctx[b]) - q_len + j
+            out[r] = attend_row(widen(q[r], dtype), K, V, position, scale)
+    return out, k_cache, v_cache
+
+
+def default_scale(D: int) -> float:
+    """1/sqrt(D) rounded to float32, the scale the workloads use."""
+    return float(np.float32(1.0 / math.sqrt(D)))
