@@ -1,0 +1,186 @@
+/*
+ * pa.h -- C ABI of libpa.so: batch-invariant paged-KV attention over one flat
+ * ragged step of a continuous-batching engine, for NVIDIA GB300 (sm_103a).
+ *
+ * The operations are the ones "P3: native paged-KV continuous-batching
+ * sampler" (section Design, paged.py) specifies for its paged attention seam:
+ * write the step's new K/V rows into per-layer [num_blocks, block_size, Hkv, D]
+ * caches by slot mapping, then return [T, H, D] attention for decode rows and
+ * causal prefill chunks, reading keys through an int32 [B, max_blocks] block
+ * table with cu_seqlens_q and ctx_lens, with the KV split fixed per context
+ * length and no atomics in any reduction (the TritonPagedAttention contract of
+ * that section). "Numerics envelopes" (sections The contract and The
+ * hierarchy, invariance.batch) gives the property every entry point keeps: a
+ * row's output bits do not depend on which other rows share the step.
+ *
+ * Conventions
+ *   - All tensor arguments are DEVICE pointers to contiguous row-major arrays
+ *     owned by the caller; the library allocates no device memory and keeps
+ *     no per-call state. All work is enqueued on `stream` (a cudaStream_t;
+ *     NULL = the legacy default stream). Results are valid once the stream
+ *     reaches that point. Only pa_read_status synchronises.
+ *   - Element type `dtype` applies to q, caches, new rows and out alike.
+ *   - ctx_lens[b] counts every key lane b attends AFTER this step's write, its
+ *     own new rows included; row j (0-based) of a lane with q_len rows sits at
+ *     absolute position ctx_lens[b] - q_len + j and attends keys 0..position.
+ *   - Query head h reads kv head h / (H / Hkv) (blocked GQA map).
+ *   - Supported: D in {64, 128}; block_size in {16, 32}; H % Hkv == 0 and
+ *     1 <= H / Hkv <= 16; dtype PA_F32 or PA_BF16.
+ *
+ * Errors
+ *   - Problems visible on the host (NULL pointers, unsupported geometry,
+ *     negative sizes, workspace too small) return a pa_status code before any
+ *     CUDA call is made.
+ *   - Problems only visible on the device (a slot or block id out of range,
+ *     a lane whose ctx exceeds its block-table row, q_len > ctx_len, malformed
+ *     cu_seqlens_q, more splits than the workspace holds) set bits of the
+ *     int32 device status word (PA_FLAG_*) with an atomic OR; the offending
+ *     write is skipped or the offending lane's rows are left unspecified, and
+ *     no kernel ever traps. `status` may be NULL (flags are then dropped).
+ *   - Launch failures return PA_ERR_CUDA (cudaGetLastError after launch).
+ */
+#ifndef PA_H
+#define PA_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  PA_OK = 0,
+  PA_ERR_INVALID_ARG = 1,   /* NULL pointer, negative size, inconsistent sizes */
+  PA_ERR_UNSUPPORTED = 2,   /* geometry or dtype outside the supported set    */
+  PA_ERR_WORKSPACE = 3,     /* workspace NULL, misaligned or too small        */
+  PA_ERR_CUDA = 4           /* a CUDA runtime call or launch failed           */
+} pa_status;
+
+typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+
+/* Device status word bits. */
+#define PA_FLAG_SLOT_RANGE   0x01  /* slot >= num_blocks * block_size: write skipped      */
+#define PA_FLAG_BLOCK_RANGE  0x02  /* block-table entry outside [0, num_blocks)          */
+#define PA_FLAG_CTX_RANGE    0x04  /* ctx_len < 0 or > max_blocks_per_seq * block_size    */
+#define PA_FLAG_QLEN_RANGE   0x08  /* q_len > ctx_len                                     */
+#define PA_FLAG_CU_SEQLENS   0x10  /* cu_seqlens_q not 0 .. T and non-decreasing          */
+#define PA_FLAG_WORKSPACE    0x20  /* the step needs more splits than the workspace holds */
+#define PA_FLAG_HOST_BOUND   0x40  /* a lane exceeds the host's max_q_len / max_ctx_len   */
+#define PA_FLAG_TIMEOUT      0x80  /* a bounded wait inside a kernel gave up              */
+
+/*
+ * pa_write_kv -- scatter T new K/V rows into the caches.
+ * ("P3: native paged-KV continuous-batching sampler", Design, paged.py:
+ *  PagedKVCache copy-free append into (block, offset).)
+ *
+ *   k_new, v_new     [T, Hkv, D]               rows to store
+ *   k_cache, v_cache [num_blocks, block_size, Hkv, D]
+ *   slot_mapping     int64 [T]; row t goes to block slot / block_size, offset
+ *                    slot % block_size. slot < 0 skips the row (padding);
+ *                    slot >= num_blocks * block_size sets PA_FLAG_SLOT_RANGE
+ *                    and skips it.
+ * Bytes move unchanged (bit-exact). Slots within one call must be distinct
+ * and must not name blocks another sequence also references (a shared block
+ * is read-only); neither is checked. Caches must not alias the new rows.
+ * Pointers must be 16-byte aligned.
+ */
+pa_status pa_write_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                      const int64_t* slot_mapping, int32_t T, int32_t num_blocks,
+                      int32_t block_size, int32_t Hkv, int32_t D, pa_dtype dtype,
+                      int32_t* status, void* stream);
+
+/*
+ * pa_attention_workspace_bytes -- device scratch pa_attention needs.
+ *
+ * The split-KV path stores fp32 partial results (m, l, acc[D]) per
+ * (query row, split, head). The bound uses host-known scalars: B lanes, T
+ * rows, the largest ctx_len, and total_ctx (sum of ctx_lens over lanes; pass
+ * a negative value if unknown, which gives a looser bound).
+ * Returns 0 for unsupported arguments.
+ */
+size_t pa_attention_workspace_bytes(int32_t B, int32_t T, int32_t max_q_len,
+                                    int32_t max_ctx_len, int64_t total_ctx, int32_t H,
+                                    int32_t Hkv, int32_t D, int32_t block_size,
+                                    pa_dtype dtype);
+
+/*
+ * pa_attention -- attention of one flat ragged step.
+ * ("P3: native paged-KV continuous-batching sampler", Design, paged.py: the
+ *  PagedAttention protocol -- write new K/V, return [T, H, D] -- and the
+ *  paged-attention kernel contract: q, k/v cache blocks, block tables,
+ *  cu_seqlens_q, ctx_lens, slot mapping; fixed KV split per context length,
+ *  no atomics.)
+ *
+ *   q                [T, H, D]
+ *   k_cache, v_cache [num_blocks, block_size, Hkv, D]
+ *   block_tables     int32 [B, max_blocks_per_seq]; entries past
+ *                    ceil(ctx_len / block_size) are never read
+ *   cu_seqlens_q     int32 [B + 1]; cu[0] = 0, cu[B] = T, non-decreasing
+ *   ctx_lens         int32 [B]
+ *   slot_mapping, k_new, v_new
+ *                    optional (all NULL or all set): when set, the rows are
+ *                    written first on the same stream, exactly as
+ *                    pa_write_kv does, and attention sees them
+ *   out              [T, H, D] (dtype of q); rows of lanes with q_len = 0 do
+ *                    not exist; every other row is written
+ *   max_q_len, max_ctx_len
+ *                    host upper bounds over lanes, used only to size grids
+ *   scale            softmax scale applied to q.k (fp32)
+ *   workspace        device scratch of workspace_bytes >= the value
+ *                    pa_attention_workspace_bytes returns for this step,
+ *                    256-byte aligned; contents on entry are irrelevant
+ * Lanes with q_len == 1 take the split-KV decode path: keys are split in
+ * fixed 512-token ranges [512 i, 512 (i + 1)), each range reduced in
+ * ascending key order, and the ranges folded left to right in fp32. Lanes
+ * with q_len >= 2 take the prefill path. Which path a row takes, its split
+ * points and its reduction order depend only on its own lane.
+ */
+pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                       const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                       void* out, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t D,
+                       int32_t block_size, int32_t num_blocks, int32_t max_q_len,
+                       int32_t max_ctx_len, float scale, pa_dtype dtype, void* workspace,
+                       size_t workspace_bytes, int32_t* status, void* stream);
+
+/*
+ * pa_attention_profiled -- pa_attention plus phase timing hooks.
+ * events: array of n_events cudaEvent_t handles (may be NULL / 0). They are
+ * recorded on `stream` in this order, as far as n_events reaches: [0] before
+ * the first launch, [1] after the write + plan prologue, [2] after the
+ * decode split kernel, [3] after the prefill kernel, [4] after the combine.
+ * The work done is identical to pa_attention.
+ */
+pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                const int64_t* slot_mapping, const void* k_new,
+                                const void* v_new, void* out, int32_t B, int32_t T, int32_t H,
+                                int32_t Hkv, int32_t D, int32_t block_size, int32_t num_blocks,
+                                int32_t max_q_len, int32_t max_ctx_len, float scale,
+                                pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                                int32_t* status, void* stream, void* const* events,
+                                int32_t n_events);
+
+/*
+ * pa_read_status -- wait for `stream`, copy the device status word to
+ * *flags_out and, if clear != 0, reset it to zero. The only synchronising call.
+ */
+pa_status pa_read_status(int32_t* status, void* stream, int32_t* flags_out, int32_t clear);
+
+/* Human-readable name of a pa_status value (static storage). */
+const char* pa_status_string(pa_status s);
+
+/* Kernels this process has launched through the library so far. */
+int64_t pa_kernel_launches(void);
+
+/* Split length (keys) of the decode path: fixed for every geometry. */
+int32_t pa_split_tokens(void);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* PA_H */

@@ -1,0 +1,344 @@
+// C ABI of libpa: host-side validation, workspace layout, tensor-map encoding
+// and launch sequencing. Declarations and contracts are in include/pa.h.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+#include <cmath>
+#include <cstring>
+#include <mutex>
+
+#include "pa_common.cuh"
+
+namespace pa {
+
+cudaError_t launch_prologue(const StepParams& p, bool plan, bool write, cudaStream_t s);
+cudaError_t launch_decode_bf16(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
+                               long long max_items, cudaStream_t s);
+cudaError_t launch_split_f32(const StepParams& p, long long max_items, cudaStream_t s);
+cudaError_t launch_combine(const StepParams& p, cudaStream_t s);
+
+static std::atomic<long long> g_launches{0};
+
+void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
+
+int num_sms() {
+  static int cache[64] = {0};
+  int dev = 0;
+  if (cudaGetDevice(&dev) != cudaSuccess || dev < 0) return 148;
+  if (dev < 64 && cache[dev] > 0) return cache[dev];
+  int n = 0;
+  if (cudaDeviceGetAttribute(&n, cudaDevAttrMultiProcessorCount, dev) != cudaSuccess || n <= 0)
+    n = 148;
+  if (dev < 64) cache[dev] = n;
+  return n;
+}
+
+namespace {
+
+constexpr size_t kAlign = 256;
+inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
+
+bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
+
+int elem_bytes_of(pa_dtype d) { return d == PA_F32 ? 4 : (d == PA_BF16 ? 2 : 0); }
+
+pa_status check_geometry(int32_t H, int32_t Hkv, int32_t D, int32_t block_size, pa_dtype dtype) {
+  if (H <= 0 || Hkv <= 0 || D <= 0 || block_size <= 0) return PA_ERR_INVALID_ARG;
+  if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
+  if (block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
+  if (H % Hkv != 0 || H / Hkv > 16) return PA_ERR_UNSUPPORTED;
+  return PA_OK;
+}
+
+// Every row takes the split path for fp32; for bf16 only decode lanes do,
+// except while a step holds a prefill lane (max_q_len >= 2) that the
+// tensor-core prefill kernel does not cover yet.
+bool split_all_rows(pa_dtype dtype, int32_t max_q_len) {
+  (void)max_q_len;
+  return dtype == PA_F32 || max_q_len >= 2;
+}
+
+struct Layout {
+  size_t header, row_info, pairs, ml, acc, fixed, per_pair;
+};
+
+Layout layout_for(int32_t T, int32_t H, int32_t D) {
+  Layout L;
+  L.header = 0;
+  L.row_info = kAlign;
+  L.pairs = L.row_info + align_up((size_t)T * sizeof(int4));
+  L.fixed = L.pairs;
+  L.per_pair = sizeof(int4) + (size_t)H * sizeof(float2) + (size_t)H * D * sizeof(float);
+  return L;
+}
+
+long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
+
+// Upper bound on (row, split) pairs of a step.
+long long max_pairs(int32_t B, int32_t T, int32_t max_q_len, int32_t max_ctx_len,
+                    int64_t total_ctx, pa_dtype dtype) {
+  const long long per_row = ceil_div(max_ctx_len > 0 ? max_ctx_len : 1, kSplit);
+  if (split_all_rows(dtype, max_q_len)) return (long long)T * per_row;
+  long long loose = (long long)(B < T ? B : T) * per_row;
+  if (total_ctx >= 0) {
+    const long long tight = total_ctx / kSplit + B;
+    if (tight < loose) loose = tight;
+  }
+  return loose;
+}
+
+size_t bytes_for_pairs(int32_t T, int32_t H, int32_t D, long long pairs) {
+  const Layout L = layout_for(T, H, D);
+  // pairs, ml and acc as three arrays, each 256-byte aligned
+  return L.fixed + align_up((size_t)pairs * sizeof(int4)) +
+         align_up((size_t)pairs * H * sizeof(float2)) +
+         align_up((size_t)pairs * H * D * sizeof(float));
+}
+
+int capacity_of(size_t bytes, int32_t T, int32_t H, int32_t D) {
+  const Layout L = layout_for(T, H, D);
+  if (bytes <= L.fixed) return 0;
+  long long cap = (long long)((bytes - L.fixed) / L.per_pair);
+  while (cap > 0 && bytes_for_pairs(T, H, D, cap) > bytes) --cap;
+  if (cap > 0x7fffffffLL) cap = 0x7fffffffLL;
+  return (int)cap;
+}
+
+SplitPlan carve(void* ws, int cap, int32_t T, int32_t H, int32_t D) {
+  const Layout L = layout_for(T, H, D);
+  char* b = static_cast<char*>(ws);
+  SplitPlan pl;
+  pl.header = reinterpret_cast<int*>(b + L.header);
+  pl.row_info = reinterpret_cast<int4*>(b + L.row_info);
+  size_t off = L.pairs;
+  pl.pairs = reinterpret_cast<int4*>(b + off);
+  off += align_up((size_t)cap * sizeof(int4));
+  pl.ml = reinterpret_cast<float2*>(b + off);
+  off += align_up((size_t)cap * H * sizeof(float2));
+  pl.acc = reinterpret_cast<float*>(b + off);
+  pl.capacity = cap;
+  return pl;
+}
+
+PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::once_flag once;
+  std::call_once(once, [] {
+    void* f = nullptr;
+    cudaDriverEntryPointQueryResult q;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &f, 12000, cudaEnableDefault,
+                                         &q) == cudaSuccess &&
+        q == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(f);
+  });
+  return fn;
+}
+
+// [NB * bs tokens, Hkv, D] bf16 cache; box = 64 elements x 1 head x 16 tokens,
+// 128-byte swizzle.
+bool encode_cache_map(CUtensorMap* map, const void* cache, int NB, int bs, int Hkv, int D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)NB * (cuuint64_t)bs};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)Hkv * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kChunk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(cache), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+pa_status record(void* const* events, int32_t n_events, int idx, cudaStream_t s) {
+  if (events && idx < n_events && events[idx]) {
+    if (cudaEventRecord(static_cast<cudaEvent_t>(events[idx]), s) != cudaSuccess)
+      return PA_ERR_CUDA;
+  }
+  return PA_OK;
+}
+
+}  // namespace
+}  // namespace pa
+
+using namespace pa;
+
+extern "C" {
+
+const char* pa_status_string(pa_status s) {
+  switch (s) {
+    case PA_OK: return "PA_OK";
+    case PA_ERR_INVALID_ARG: return "PA_ERR_INVALID_ARG";
+    case PA_ERR_UNSUPPORTED: return "PA_ERR_UNSUPPORTED";
+    case PA_ERR_WORKSPACE: return "PA_ERR_WORKSPACE";
+    case PA_ERR_CUDA: return "PA_ERR_CUDA";
+  }
+  return "PA_ERR_UNKNOWN";
+}
+
+int64_t pa_kernel_launches(void) { return g_launches.load(std::memory_order_relaxed); }
+
+int32_t pa_split_tokens(void) { return kSplit; }
+
+pa_status pa_write_kv(const void* k_new, const void* v_new, void* k_cache, void* v_cache,
+                      const int64_t* slot_mapping, int32_t T, int32_t num_blocks,
+                      int32_t block_size, int32_t Hkv, int32_t D, pa_dtype dtype,
+                      int32_t* status, void* stream) {
+  if (T < 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
+  pa_status g = check_geometry(Hkv, Hkv, D, block_size, dtype);
+  if (g != PA_OK) return g;
+  if (T == 0) return PA_OK;
+  if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
+  if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
+    return PA_ERR_INVALID_ARG;
+  StepParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.slot_mapping = slot_mapping;
+  p.status = status;
+  p.T = T;
+  p.Hkv = Hkv;
+  p.H = Hkv;
+  p.D = D;
+  p.bs = block_size;
+  p.NB = num_blocks;
+  p.elem_bytes = elem_bytes_of(dtype);
+  cudaError_t e = launch_prologue(p, false, true, static_cast<cudaStream_t>(stream));
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  count_launches(1);
+  return PA_OK;
+}
+
+size_t pa_attention_workspace_bytes(int32_t B, int32_t T, int32_t max_q_len,
+                                    int32_t max_ctx_len, int64_t total_ctx, int32_t H,
+                                    int32_t Hkv, int32_t D, int32_t block_size,
+                                    pa_dtype dtype) {
+  if (B < 0 || T < 0 || max_q_len < 0 || max_ctx_len < 0) return 0;
+  if (check_geometry(H, Hkv, D, block_size, dtype) != PA_OK) return 0;
+  const long long pairs = max_pairs(B, T, max_q_len, max_ctx_len, total_ctx, dtype);
+  return bytes_for_pairs(T, H, D, pairs > 0 ? pairs : 1);
+}
+
+pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                const int64_t* slot_mapping, const void* k_new,
+                                const void* v_new, void* out, int32_t B, int32_t T, int32_t H,
+                                int32_t Hkv, int32_t D, int32_t block_size, int32_t num_blocks,
+                                int32_t max_q_len, int32_t max_ctx_len, float scale,
+                                pa_dtype dtype, void* workspace, size_t workspace_bytes,
+                                int32_t* status, void* stream, void* const* events,
+                                int32_t n_events) {
+  // ---- host validation: nothing below touches CUDA until it all passes ----
+  if (B < 0 || T < 0 || num_blocks <= 0 || max_q_len < 0 || max_ctx_len < 0 || n_events < 0)
+    return PA_ERR_INVALID_ARG;
+  pa_status g = check_geometry(H, Hkv, D, block_size, dtype);
+  if (g != PA_OK) return g;
+  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  const bool with_write = slot_mapping || k_new || v_new;
+  if (with_write && !(slot_mapping && k_new && v_new)) return PA_ERR_INVALID_ARG;
+  if ((long long)num_blocks * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  if (T > 0 && B == 0) return PA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (T == 0 || B == 0) {
+    // nothing to compute; still honour the phase events
+    for (int i = 0; i < n_events && i < 5; ++i)
+      if (record(events, n_events, i, s) != PA_OK) return PA_ERR_CUDA;
+    return PA_OK;
+  }
+  if (!q || !k_cache || !v_cache || !block_tables || !cu_seqlens_q || !ctx_lens || !out)
+    return PA_ERR_INVALID_ARG;
+  if (max_blocks_per_seq <= 0) return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache) || !aligned16(out))
+    return PA_ERR_INVALID_ARG;
+  if (with_write && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
+    return PA_ERR_WORKSPACE;
+  const int cap = capacity_of(workspace_bytes, T, H, D);
+  if (cap <= 0) return PA_ERR_WORKSPACE;
+
+  StepParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.out = out;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.cu_seqlens = cu_seqlens_q;
+  p.ctx_lens = ctx_lens;
+  p.slot_mapping = slot_mapping;
+  p.k_new = k_new;
+  p.v_new = v_new;
+  p.status = status;
+  p.max_blocks = max_blocks_per_seq;
+  p.B = B;
+  p.T = T;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.bs = block_size;
+  p.NB = num_blocks;
+  p.max_q_len = max_q_len;
+  p.max_ctx_len = max_ctx_len;
+  p.elem_bytes = elem_bytes_of(dtype);
+  p.split_all_rows = split_all_rows(dtype, max_q_len) ? 1 : 0;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.plan = carve(workspace, cap, T, H, D);
+
+  CUtensorMap tmK, tmV;
+  if (dtype == PA_BF16) {
+    if (!encode_cache_map(&tmK, k_cache, num_blocks, block_size, Hkv, D) ||
+        !encode_cache_map(&tmV, v_cache, num_blocks, block_size, Hkv, D))
+      return PA_ERR_CUDA;
+  }
+  long long items = max_pairs(B, T, max_q_len, max_ctx_len, -1, dtype);
+  if (items > cap) items = cap;
+  items *= Hkv;
+
+  if (record(events, n_events, 0, s) != PA_OK) return PA_ERR_CUDA;
+  if (launch_prologue(p, true, with_write, s) != cudaSuccess) return PA_ERR_CUDA;
+  count_launches(1);
+  if (record(events, n_events, 1, s) != PA_OK) return PA_ERR_CUDA;
+  cudaError_t e = dtype == PA_BF16 ? launch_decode_bf16(p, tmK, tmV, items, s)
+                                   : launch_split_f32(p, items, s);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  count_launches(1);
+  if (record(events, n_events, 2, s) != PA_OK) return PA_ERR_CUDA;
+  if (record(events, n_events, 3, s) != PA_OK) return PA_ERR_CUDA;
+  if (launch_combine(p, s) != cudaSuccess) return PA_ERR_CUDA;
+  count_launches(1);
+  if (record(events, n_events, 4, s) != PA_OK) return PA_ERR_CUDA;
+  return PA_OK;
+}
+
+pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
+                       const int32_t* block_tables, int32_t max_blocks_per_seq,
+                       const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                       const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                       void* out, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t D,
+                       int32_t block_size, int32_t num_blocks, int32_t max_q_len,
+                       int32_t max_ctx_len, float scale, pa_dtype dtype, void* workspace,
+                       size_t workspace_bytes, int32_t* status, void* stream) {
+  return pa_attention_profiled(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
+                               cu_seqlens_q, ctx_lens, slot_mapping, k_new, v_new, out, B, T, H,
+                               Hkv, D, block_size, num_blocks, max_q_len, max_ctx_len, scale,
+                               dtype, workspace, workspace_bytes, status, stream, nullptr, 0);
+}
+
+pa_status pa_read_status(int32_t* status, void* stream, int32_t* flags_out, int32_t clear) {
+  if (!status || !flags_out) return PA_ERR_INVALID_ARG;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  int32_t v = 0;
+  if (cudaMemcpyAsync(&v, status, sizeof(v), cudaMemcpyDeviceToHost, s) != cudaSuccess)
+    return PA_ERR_CUDA;
+  if (clear && cudaMemsetAsync(status, 0, sizeof(int32_t), s) != cudaSuccess) return PA_ERR_CUDA;
+  if (cudaStreamSynchronize(s) != cudaSuccess) return PA_ERR_CUDA;
+  *flags_out = v;
+  return PA_OK;
+}
+
+}  // extern "C"

@@ -1,0 +1,201 @@
+// Shared device-side definitions of libpa: launch parameters, the split plan
+// stored in the caller's workspace, and thin wrappers over the PTX
+// instructions the kernels issue (mbarrier, TMA, ldmatrix, mma, movmatrix).
+#pragma once
+
+#include <cuda.h>
+#include <cuda_bf16.h>
+#include <cuda_runtime.h>
+#include <stdint.h>
+
+#include "pa.h"
+
+namespace pa {
+
+// Keys per split of the decode path. A function of nothing: every row's split
+// points are i * kSplit, so they depend only on the row's own key count.
+constexpr int kSplit = 512;
+// Keys per pipeline stage of the split kernels (one mma M tile).
+constexpr int kChunk = 16;
+// Bounded waits give up after this many SM clock cycles (about 1 s).
+constexpr long long kWaitCycles = 2000000000LL;
+
+// ---------------------------------------------------------------------------
+// Split plan, built on the device by the prologue kernel from cu_seqlens_q and
+// ctx_lens, stored in the workspace:
+//   header[0] = number of (row, split) pairs, header[1] = number of full pairs
+//   row_info[r] = {first full pair, tail pair or -1, number of splits, lane or -1}
+//   pairs[k]    = {row, split index, lane, key count of the row}
+// Full pairs (exactly kSplit keys) come first, lane-major; tail pairs after.
+// Partial results of pair k: ml[k * H + h] = {m (log2 domain), l},
+// acc[(k * H + h) * D + d].
+// ---------------------------------------------------------------------------
+struct SplitPlan {
+  int* header;
+  int4* row_info;
+  int4* pairs;
+  float2* ml;
+  float* acc;
+  int capacity;  // pairs the workspace holds
+};
+
+struct StepParams {
+  const void* q;
+  void* out;
+  const void* k_cache;
+  const void* v_cache;
+  const int* block_tables;
+  const int* cu_seqlens;
+  const int* ctx_lens;
+  const int64_t* slot_mapping;
+  const void* k_new;
+  const void* v_new;
+  int* status;
+  int max_blocks;
+  int B, T, H, Hkv, D, bs, NB;
+  int max_q_len, max_ctx_len;
+  int elem_bytes;
+  int split_all_rows;  // 1: every row takes the split path; 0: lanes with q_len == 1 only
+  float scale;
+  float scale_log2;  // scale * log2(e): scores kept in the base-2 domain
+  SplitPlan plan;
+};
+
+__device__ __forceinline__ void raise_flag(int* status, int bits) {
+  if (status) atomicOr(status, bits);
+}
+
+// Normalised output of one (row, head, dim): shared by the single-split
+// direct write and the combine so both round the same quotient.
+__device__ __forceinline__ float finish_div(float acc, float l) { return acc / l; }
+
+// Left fold of one more split (m_i, l_i, a_i) into (M, L, A), fp32.
+struct Fold {
+  float M, L;
+  __device__ __forceinline__ void first(float m, float l) { M = m; L = l; }
+  // Returns the two rescale factors for the accumulators.
+  __device__ __forceinline__ void next(float m, float l, float& ea, float& eb) {
+    const float Mn = fmaxf(M, m);
+    ea = exp2f(M - Mn);
+    eb = exp2f(m - Mn);
+    L = fmaf(L, ea, l * eb);
+    M = Mn;
+  }
+};
+
+// ---------------------------------------------------------------------------
+// PTX wrappers
+// ---------------------------------------------------------------------------
+__device__ __forceinline__ uint32_t smem_u32(const void* p) {
+  return static_cast<uint32_t>(__cvta_generic_to_shared(p));
+}
+
+__device__ __forceinline__ float ex2_approx(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
+
+__device__ __forceinline__ void mbar_init(uint32_t bar, uint32_t count) {
+  asm volatile("mbarrier.init.shared::cta.b64 [%0], %1;" ::"r"(bar), "r"(count) : "memory");
+}
+
+__device__ __forceinline__ void fence_mbar_init() {
+  asm volatile("fence.mbarrier_init.release.cluster;" ::: "memory");
+}
+
+__device__ __forceinline__ void fence_proxy_async_smem() {
+  asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {
+  asm volatile("mbarrier.arrive.expect_tx.shared::cta.b64 _, [%0], %1;" ::"r"(bar), "r"(bytes)
+               : "memory");
+}
+
+__device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
+  uint32_t ok;
+  asm volatile(
+      "{\n\t.reg .pred p;\n\t"
+      "mbarrier.try_wait.parity.shared::cta.b64 p, [%1], %2;\n\t"
+      "selp.u32 %0, 1, 0, p;\n\t}"
+      : "=r"(ok)
+      : "r"(bar), "r"(parity)
+      : "memory");
+  return ok != 0;
+}
+
+// Wait for the phase with the given parity to complete, for at most
+// kWaitCycles SM cycles. Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+  if (mbar_try_wait(bar, parity)) return true;
+  const long long t0 = clock64();
+  while (!mbar_try_wait(bar, parity)) {
+    if (clock64() - t0 > kWaitCycles) return false;
+  }
+  return true;
+}
+
+// 3-D tiled TMA load global -> shared, completion counted on `bar`.
+__device__ __forceinline__ void tma_load_3d(uint32_t dst, const CUtensorMap* map, int x, int y,
+                                            int z, uint32_t bar) {
+  asm volatile(
+      "cp.async.bulk.tensor.3d.shared::cluster.global.mbarrier::complete_tx::bytes"
+      " [%0], [%1, {%2, %3, %4}], [%5];" ::"r"(dst),
+      "l"(reinterpret_cast<uint64_t>(map)), "r"(x), "r"(y), "r"(z), "r"(bar)
+      : "memory");
+}
+
+__device__ __forceinline__ void prefetch_tensormap(const CUtensorMap* map) {
+  asm volatile("prefetch.tensormap [%0];" ::"l"(reinterpret_cast<uint64_t>(map)) : "memory");
+}
+
+__device__ __forceinline__ void ldsm_x4(uint32_t addr, uint32_t& r0, uint32_t& r1, uint32_t& r2,
+                                        uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ void ldsm_x4_trans(uint32_t addr, uint32_t& r0, uint32_t& r1,
+                                              uint32_t& r2, uint32_t& r3) {
+  asm volatile("ldmatrix.sync.aligned.m8n8.x4.trans.shared.b16 {%0, %1, %2, %3}, [%4];"
+               : "=r"(r0), "=r"(r1), "=r"(r2), "=r"(r3)
+               : "r"(addr));
+}
+
+__device__ __forceinline__ uint32_t movmatrix_trans(uint32_t x) {
+  uint32_t y;
+  asm volatile("movmatrix.sync.aligned.m8n8.trans.b16 %0, %1;" : "=r"(y) : "r"(x));
+  return y;
+}
+
+// D(16x8 f32) += A(16x16 bf16, row) * B(16x8 bf16, col)
+__device__ __forceinline__ void mma_bf16_16816(float (&d)[4], uint32_t a0, uint32_t a1,
+                                               uint32_t a2, uint32_t a3, uint32_t b0,
+                                               uint32_t b1) {
+  asm volatile(
+      "mma.sync.aligned.m16n8k16.row.col.f32.bf16.bf16.f32 {%0, %1, %2, %3}, "
+      "{%4, %5, %6, %7}, {%8, %9}, {%0, %1, %2, %3};"
+      : "+f"(d[0]), "+f"(d[1]), "+f"(d[2]), "+f"(d[3])
+      : "r"(a0), "r"(a1), "r"(a2), "r"(a3), "r"(b0), "r"(b1));
+}
+
+__device__ __forceinline__ uint32_t pack_bf16x2(float lo, float hi) {
+  __nv_bfloat162 v = __floats2bfloat162_rn(lo, hi);  // .x = lo (low 16 bits)
+  return *reinterpret_cast<uint32_t*>(&v);
+}
+
+__device__ __forceinline__ float bf16_lo(uint32_t v) { return __uint_as_float(v << 16); }
+__device__ __forceinline__ float bf16_hi(uint32_t v) { return __uint_as_float(v & 0xffff0000u); }
+
+// Store an fp32 value as the output element type.
+__device__ __forceinline__ void store_out(void* out, size_t idx, float v, int elem_bytes) {
+  if (elem_bytes == 4) {
+    static_cast<float*>(out)[idx] = v;
+  } else {
+    static_cast<__nv_bfloat16*>(out)[idx] = __float2bfloat16_rn(v);
+  }
+}
+
+}  // namespace pa

@@ -1,0 +1,368 @@
+// Split-KV decode partials, bf16 caches (the decode path of the paged-attention
+// kernel contract in "P3: native paged-KV continuous-batching sampler", Design,
+// paged.py: fixed KV split per context length, no atomics).
+//
+// Work item = (row, split, kv head). One warp owns an item: it streams the
+// split's keys in 16-key chunks through a private 3-stage ring of swizzled
+// shared-memory tiles filled by TMA (one 64-element box per half row), and
+// computes, for the g = H / Hkv query heads that read this kv head,
+//   t_j = log2(e) * scale * <q_h, k_j>    (tensor cores, fp32 accumulate)
+//   m   = max_j t_j,  p_j = 2^(t_j - m) rounded to bf16,  l = sum_j p_j
+//   acc = sum_j p_j v_j                   (tensor cores, fp32 accumulate)
+// with the usual running rescale when m grows, keys in ascending order.
+// The products are arranged so the kv head's keys are the M side of the mma:
+// S^T = K Q^T (M = 16 keys, N = 8 heads, K = 16 dims) and O^T = V^T P^T
+// (M = 16 dims, N = 8 heads, K = 16 keys), so a GQA group of up to 8 heads
+// fills one N tile. P^T moves from the accumulator layout of the first
+// product to the operand layout of the second with movmatrix.
+//
+// A row whose keys fit one split writes its normalised output directly; the
+// others leave (m, l, acc) for the fixed-order combine. Every item's
+// arithmetic depends only on its own row's q and keys: which warp runs it and
+// what else is in the step do not enter.
+#include "pa_common.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kWarps = 4;
+constexpr int kStages = 3;
+
+template <int D>
+struct Tile {
+  static constexpr int kHalves = D / 64;              // 128-byte swizzled boxes per row
+  static constexpr int kHalfBytes = kChunk * 128;     // one box: 16 keys x 64 elements
+  static constexpr int kBytes = kChunk * D * 2;       // one K (or V) chunk
+  static constexpr int kStageBytes = 2 * kBytes;      // K + V
+  static constexpr int kWarpBytes = kStages * kStageBytes;
+  static constexpr int kSmemBytes = kWarps * kWarpBytes + 1024;  // + alignment slack
+};
+
+// Shared address of 16-byte chunk c16 (0 .. D/8-1) of key row `tok` inside a
+// tile written by TMA with 128-byte swizzle: chunk index XOR (row mod 8).
+template <int D>
+__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int tok, int c16) {
+  const int half = c16 >> 3, chunk = c16 & 7;
+  return base + half * Tile<D>::kHalfBytes + tok * 128 + ((chunk ^ (tok & 7)) << 4);
+}
+
+struct Item {
+  int pair, kvh, row, lane, keys, t0, len, nchunks;
+};
+
+__device__ __forceinline__ Item load_item(const StepParams& p, long long item) {
+  Item it;
+  it.pair = (int)(item / p.Hkv);
+  it.kvh = (int)(item - (long long)it.pair * p.Hkv);
+  const int4 pr = p.plan.pairs[it.pair];
+  it.row = pr.x;
+  it.lane = pr.z;
+  it.keys = pr.w;
+  it.t0 = pr.y * kSplit;
+  it.len = min(kSplit, it.keys - it.t0);
+  it.nchunks = (it.len + kChunk - 1) / kChunk;
+  return it;
+}
+
+// Block ids of the item's range: lane i holds entry i (kSplit / bs <= 32).
+__device__ __forceinline__ int load_blocks(const StepParams& p, const Item& it, int lane) {
+  const int nblk = (it.len + p.bs - 1) / p.bs;
+  if (lane >= nblk) return 0;
+  return p.block_tables[(size_t)it.lane * p.max_blocks + it.t0 / p.bs + lane];
+}
+
+template <int D, int NT>
+__global__ void __launch_bounds__(kWarps * 32, 2)
+    decode_bf16_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
+                       const __grid_constant__ CUtensorMap tmV) {
+  using TL = Tile<D>;
+  constexpr int KS = D / 16;  // 16-wide steps along D
+  extern __shared__ uint8_t dsmem[];
+  __shared__ __align__(8) uint64_t bars[kWarps][kStages];
+
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int gid = lane >> 2, tig = lane & 3;
+  const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
+  const uint32_t wbase = base + warp * TL::kWarpBytes;
+  uint32_t bar[kStages];
+#pragma unroll
+  for (int s = 0; s < kStages; ++s) bar[s] = smem_u32(&bars[warp][s]);
+  if (lane == 0) {
+#pragma unroll
+    for (int s = 0; s < kStages; ++s) mbar_init(bar[s], 1);
+    fence_mbar_init();
+    prefetch_tensormap(&tmK);
+    prefetch_tensormap(&tmV);
+  }
+  __syncwarp();
+
+  const int g = p.H / p.Hkv;
+  const long long n_items = (long long)p.plan.header[0] * p.Hkv;
+  const long long gw = (long long)blockIdx.x * kWarps + warp;
+  const long long nw = (long long)gridDim.x * kWarps;
+
+  // ---- producer cursor: runs up to kStages chunks ahead of the consumer ----
+  long long p_item = gw;
+  int p_chunk = 0;
+  Item pi;
+  int p_blk = 0;
+  if (p_item < n_items) {
+    pi = load_item(p, p_item);
+    p_blk = load_blocks(p, pi, lane);
+  }
+  uint32_t issued = 0;
+  auto produce = [&]() {
+    if (p_item >= n_items) return;
+    const int stage = issued % kStages;
+    const int off = p_chunk * kChunk;  // key offset inside the split
+    int blk = __shfl_sync(0xffffffffu, p_blk, off / p.bs);
+    if (lane == 0) {
+      if (blk < 0 || blk >= p.NB) {
+        raise_flag(p.status, PA_FLAG_BLOCK_RANGE);
+        blk = 0;
+      }
+      const int tok = blk * p.bs + (pi.t0 + off) % p.bs;
+      const uint32_t ks = wbase + stage * TL::kStageBytes;
+      const uint32_t vs = ks + TL::kBytes;
+      mbar_expect_tx(bar[stage], TL::kStageBytes);
+#pragma unroll
+      for (int h = 0; h < TL::kHalves; ++h) {
+        tma_load_3d(ks + h * TL::kHalfBytes, &tmK, h * 64, pi.kvh, tok, bar[stage]);
+        tma_load_3d(vs + h * TL::kHalfBytes, &tmV, h * 64, pi.kvh, tok, bar[stage]);
+      }
+    }
+    ++issued;
+    if (++p_chunk == pi.nchunks) {
+      p_chunk = 0;
+      p_item += nw;
+      if (p_item < n_items) {
+        pi = load_item(p, p_item);
+        p_blk = load_blocks(p, pi, lane);
+      }
+    }
+  };
+#pragma unroll 1
+  for (int s = 0; s < kStages; ++s) produce();
+
+  uint32_t consumed = 0;
+  const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(p.q);
+
+#pragma unroll 1
+  for (long long c_item = gw; c_item < n_items; c_item += nw) {
+    const Item it = load_item(p, c_item);
+
+    // q fragments (B operand of S^T = K Q^T): k = dims, n = heads of the group
+    uint32_t qf[NT][KS][2];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      const int hl = nt * 8 + gid;  // head within the group
+      const bool hv = hl < g;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          qbase + ((size_t)it.row * p.H + (size_t)it.kvh * g + (hv ? hl : 0)) * D);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qf[nt][kk][0] = hv ? qrow[(kk * 16 + 2 * tig) >> 1] : 0u;
+        qf[nt][kk][1] = hv ? qrow[(kk * 16 + 8 + 2 * tig) >> 1] : 0u;
+      }
+    }
+
+    float m[NT][2], l[NT][2];
+    float o[KS][NT][4];
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+    }
+
+#pragma unroll 1
+    for (int ch = 0; ch < it.nchunks; ++ch) {
+      const int stage = consumed % kStages;
+      const uint32_t parity = (consumed / kStages) & 1u;
+      // every lane waits (so every lane sees the landed bytes); the verdict is
+      // made warp-uniform before anyone acts on it
+      const bool landed = __all_sync(0xffffffffu, mbar_wait_bounded(bar[stage], parity));
+      if (!landed) {
+        if (lane == 0) raise_flag(p.status, PA_FLAG_TIMEOUT);
+        // let copies already in flight land before the warp leaves
+        for (uint32_t c = consumed + 1; c < issued; ++c)
+          mbar_wait_bounded(bar[c % kStages], (c / kStages) & 1u);
+        return;
+      }
+      const uint32_t ks = wbase + stage * TL::kStageBytes;
+      const uint32_t vs = ks + TL::kBytes;
+      const int nvalid = min(kChunk, it.len - ch * kChunk);
+      if (nvalid < kChunk) {
+        // keys past the end: zero their V rows so 0 * (stale bytes) cannot
+        // turn into NaN inside the second product
+        const int nz = (kChunk - nvalid) * TL::kHalves * 8;
+        for (int i = lane; i < nz; i += 32) {
+          const int c16 = i & 7, rest = i >> 3;
+          const int half = rest % TL::kHalves, tok = nvalid + rest / TL::kHalves;
+          const uint32_t a = vs + half * TL::kHalfBytes + tok * 128 + c16 * 16;
+          asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
+        }
+        fence_proxy_async_smem();
+        __syncwarp();
+      }
+
+      // S^T = K Q^T : 16 keys x 8 heads per n tile
+      float s[NT][4];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      {
+        const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+        for (int kk = 0; kk < KS; ++kk) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4(tile_addr<D>(ks, tok, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(s[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
+        }
+      }
+
+      // online softmax over this chunk; this thread holds keys gid and gid + 8
+      // for heads 2 * tig and 2 * tig + 1 of each n tile
+      const bool va = gid < nvalid, vb = gid + 8 < nvalid;
+      uint32_t pb[NT][2];
+      float alpha[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        float pa[2], pc[2];
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const float ta = va ? s[nt][e] * p.scale_log2 : -INFINITY;
+          const float tb = vb ? s[nt][2 + e] * p.scale_log2 : -INFINITY;
+          float mx = fmaxf(ta, tb);
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+          const float mn = fmaxf(m[nt][e], mx);
+          alpha[nt][e] = ex2_approx(m[nt][e] - mn);
+          m[nt][e] = mn;
+          pa[e] = ex2_approx(ta - mn);
+          pc[e] = ex2_approx(tb - mn);
+        }
+        pb[nt][0] = pack_bf16x2(pa[0], pa[1]);  // key gid,     heads 2tig, 2tig+1
+        pb[nt][1] = pack_bf16x2(pc[0], pc[1]);  // key gid + 8, heads 2tig, 2tig+1
+        l[nt][0] = fmaf(l[nt][0], alpha[nt][0], bf16_lo(pb[nt][0]) + bf16_lo(pb[nt][1]));
+        l[nt][1] = fmaf(l[nt][1], alpha[nt][1], bf16_hi(pb[nt][0]) + bf16_hi(pb[nt][1]));
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          o[mt][nt][0] *= alpha[nt][0];
+          o[mt][nt][1] *= alpha[nt][1];
+          o[mt][nt][2] *= alpha[nt][0];
+          o[mt][nt][3] *= alpha[nt][1];
+        }
+      }
+      // P^T (keys x heads, accumulator layout) -> B operand (k = keys, n = heads)
+      uint32_t pbt[NT][2];
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt) {
+        pbt[nt][0] = movmatrix_trans(pb[nt][0]);
+        pbt[nt][1] = movmatrix_trans(pb[nt][1]);
+      }
+
+      // O^T += V^T P^T : 16 dims x 8 heads per (m tile, n tile)
+      {
+        const int tok = (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          uint32_t a0, a1, a2, a3;
+          ldsm_x4_trans(tile_addr<D>(vs, tok, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
+#pragma unroll
+          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, pbt[nt][0], pbt[nt][1]);
+        }
+      }
+      __syncwarp();  // every lane is done reading this stage
+      ++consumed;
+      produce();
+    }
+
+    // ---- finish the item ----
+#pragma unroll
+    for (int nt = 0; nt < NT; ++nt) {
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        float v = l[nt][e];
+        v += __shfl_xor_sync(0xffffffffu, v, 4);
+        v += __shfl_xor_sync(0xffffffffu, v, 8);
+        v += __shfl_xor_sync(0xffffffffu, v, 16);
+        l[nt][e] = v;
+      }
+    }
+    const bool single = it.keys <= kSplit;
+    const size_t head0 = (size_t)it.row * p.H + (size_t)it.kvh * g;  // first head of the group
+    if (single) {
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int hl = nt * 8 + 2 * tig + (r & 1);
+          if (hl < g) {
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+              const int d = mt * 16 + gid + (r >> 1) * 8;
+              out[(head0 + hl) * D + d] = __float2bfloat16_rn(finish_div(o[mt][nt][r], l[nt][r & 1]));
+            }
+          }
+        }
+    } else {
+      const size_t ph0 = (size_t)it.pair * p.H + (size_t)it.kvh * g;
+#pragma unroll
+      for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+        for (int r = 0; r < 4; ++r) {
+          const int hl = nt * 8 + 2 * tig + (r & 1);
+          if (hl < g) {
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+              const int d = mt * 16 + gid + (r >> 1) * 8;
+              p.plan.acc[(ph0 + hl) * D + d] = o[mt][nt][r];
+            }
+          }
+        }
+      if (gid == 0) {
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            const int hl = nt * 8 + 2 * tig + e;
+            if (hl < g) p.plan.ml[ph0 + hl] = make_float2(m[nt][e], l[nt][e]);
+          }
+      }
+    }
+  }
+}
+
+template <int D, int NT>
+cudaError_t launch_t(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v, int grid,
+                     cudaStream_t s) {
+  auto kern = decode_bf16_kernel<D, NT>;
+  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                       Tile<D>::kSmemBytes);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, kWarps * 32, Tile<D>::kSmemBytes, s>>>(p, k, v);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int num_sms();
+
+// Upper bound on items -> grid of up to two CTAs per SM (each 4 independent warps).
+cudaError_t launch_decode_bf16(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
+                               long long max_items, cudaStream_t s) {
+  long long want = (max_items + kWarps - 1) / kWarps;
+  const long long cap = 2LL * num_sms();
+  int grid = (int)(want < cap ? want : cap);
+  if (grid < 1) grid = 1;
+  const int g = p.H / p.Hkv;
+  if (p.D == 128) return g <= 8 ? launch_t<128, 1>(p, k, v, grid, s) : launch_t<128, 2>(p, k, v, grid, s);
+  return g <= 8 ? launch_t<64, 1>(p, k, v, grid, s) : launch_t<64, 2>(p, k, v, grid, s);
+}
+
+}  // namespace pa

@@ -1,0 +1,170 @@
+"""ctypes binding of libpa.so (include/pa.h). Argument marshalling only.
+
+Every function takes torch tensors, checks dtype / shape / device, passes raw
+device pointers and the current CUDA stream to the C ABI, and raises
+``PaError`` on a non-zero status. No arithmetic of the method runs here, and
+there is no fallback: if the library is missing, importing the functions
+raises.
+"""
+from __future__ import annotations
+
+import ctypes
+import os
+from typing import Optional, Sequence
+
+import torch
+
+_LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libpa.so")
+
+PA_F32, PA_BF16 = 0, 1
+STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
+                3: "PA_ERR_WORKSPACE", 4: "PA_ERR_CUDA"}
+FLAGS = {
+    "SLOT_RANGE": 0x01, "BLOCK_RANGE": 0x02, "CTX_RANGE": 0x04, "QLEN_RANGE": 0x08,
+    "CU_SEQLENS": 0x10, "WORKSPACE": 0x20, "HOST_BOUND": 0x40, "TIMEOUT": 0x80,
+}
+
+EXPORTS = ("pa_write_kv", "pa_attention_workspace_bytes", "pa_attention",
+           "pa_attention_profiled", "pa_read_status", "pa_status_string",
+           "pa_kernel_launches", "pa_split_tokens")
+
+
+class PaError(RuntimeError):
+    def __init__(self, code: int, what: str):
+        super().__init__(f"{what}: {STATUS_NAMES.get(code, code)}")
+        self.code = code
+
+
+_lib = None
+
+
+def lib_path() -> str:
+    return _LIB_PATH
+
+
+def load() -> ctypes.CDLL:
+    """Load libpa.so (built by ``invariant_paged_kv_gb300.build``); raise if absent."""
+    global _lib
+    if _lib is not None:
+        return _lib
+    if not os.path.exists(_LIB_PATH):
+        raise RuntimeError(
+            f"libpa.so not built ({_LIB_PATH}); run `python -m invariant_paged_kv_gb300.build`")
+    L = ctypes.CDLL(_LIB_PATH)
+    vp, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
+    L.pa_write_kv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
+    L.pa_write_kv.restype = ctypes.c_int
+    L.pa_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32, i32, i32]
+    L.pa_attention_workspace_bytes.restype = sz
+    att = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
+           i32, i32, f32, i32, vp, sz, vp, vp]
+    L.pa_attention.argtypes = att
+    L.pa_attention.restype = ctypes.c_int
+    L.pa_attention_profiled.argtypes = att + [ctypes.POINTER(vp), i32]
+    L.pa_attention_profiled.restype = ctypes.c_int
+    L.pa_read_status.argtypes = [vp, vp, ctypes.POINTER(i32), i32]
+    L.pa_read_status.restype = ctypes.c_int
+    L.pa_status_string.argtypes = [ctypes.c_int]
+    L.pa_status_string.restype = ctypes.c_char_p
+    L.pa_kernel_launches.argtypes = []
+    L.pa_kernel_launches.restype = i64
+    L.pa_split_tokens.argtypes = []
+    L.pa_split_tokens.restype = i32
+    _lib = L
+    return L
+
+
+def _dtype_code(t: torch.Tensor) -> int:
+    if t.dtype == torch.float32:
+        return PA_F32
+    if t.dtype == torch.bfloat16:
+        return PA_BF16
+    raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _ptr(t: Optional[torch.Tensor]):
+    if t is None:
+        return None
+    if not t.is_contiguous():
+        raise ValueError("tensors must be contiguous")
+    return ctypes.c_void_p(t.data_ptr())
+
+
+def _stream(stream) -> ctypes.c_void_p:
+    if stream is None:
+        stream = torch.cuda.current_stream()
+    return ctypes.c_void_p(stream.cuda_stream)
+
+
+def _check(code: int, what: str):
+    if code != 0:
+        raise PaError(code, what)
+
+
+def split_tokens() -> int:
+    return int(load().pa_split_tokens())
+
+
+def kernel_launches() -> int:
+    return int(load().pa_kernel_launches())
+
+
+def new_status(device=None) -> torch.Tensor:
+    return torch.zeros(1, dtype=torch.int32, device=device or "cuda")
+
+
+def read_status(status: torch.Tensor, stream=None, clear: bool = True) -> int:
+    out = ctypes.c_int32(0)
+    _check(load().pa_read_status(_ptr(status), _stream(stream), ctypes.byref(out),
+                                 1 if clear else 0), "pa_read_status")
+    return int(out.value)
+
+
+def write_kv(k_new, v_new, k_cache, v_cache, slot_mapping, status=None, stream=None):
+    """pa_write_kv: scatter new rows [T, Hkv, D] into caches [NB, bs, Hkv, D]."""
+    NB, bs, Hkv, D = k_cache.shape
+    T = k_new.shape[0]
+    if slot_mapping.dtype != torch.int64:
+        raise TypeError("slot_mapping must be int64")
+    _check(load().pa_write_kv(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                              _ptr(slot_mapping), T, NB, bs, Hkv, D, _dtype_code(k_cache),
+                              _ptr(status), _stream(stream)), "pa_write_kv")
+
+
+def workspace_bytes(B, T, max_q_len, max_ctx_len, total_ctx, H, Hkv, D, block_size,
+                    dtype: torch.dtype) -> int:
+    code = PA_F32 if dtype == torch.float32 else PA_BF16
+    n = int(load().pa_attention_workspace_bytes(B, T, max_q_len, max_ctx_len, total_ctx, H,
+                                                Hkv, D, block_size, code))
+    if n == 0:
+        raise PaError(2, "pa_attention_workspace_bytes")
+    return n
+
+
+def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,
+              max_q_len: int, max_ctx_len: int, scale: float, workspace: torch.Tensor,
+              slot_mapping=None, k_new=None, v_new=None, status=None, stream=None,
+              events: Optional[Sequence[torch.cuda.Event]] = None):
+    """pa_attention (or pa_attention_profiled when ``events`` is given)."""
+    T, H, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    B = ctx_lens.shape[0]
+    if block_tables.dtype != torch.int32 or cu_seqlens_q.dtype != torch.int32 \
+            or ctx_lens.dtype != torch.int32:
+        raise TypeError("block_tables, cu_seqlens_q and ctx_lens must be int32")
+    if workspace.dtype != torch.uint8:
+        raise TypeError("workspace must be a uint8 tensor")
+    mb = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    args = [_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mb, _ptr(cu_seqlens_q),
+            _ptr(ctx_lens), _ptr(slot_mapping), _ptr(k_new), _ptr(v_new), _ptr(out), B, T, H,
+            Hkv, D, bs, NB, int(max_q_len), int(max_ctx_len), float(scale), _dtype_code(q),
+            _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)]
+    L = load()
+    if events is None:
+        _check(L.pa_attention(*args), "pa_attention")
+    else:
+        for e in events:  # torch creates events lazily; recording once creates them
+            if not e.cuda_event:
+                e.record(stream)
+        arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
+        _check(L.pa_attention_profiled(*args, arr, len(events)), "pa_attention_profiled")

@@ -382,3 +382,63 @@ def key_mask(step: Step) -> np.ndarray:
             n = min(bs, c - i * bs)
             mask[blk * bs: blk * bs + n] = True
     return mask
+
+
+def sub_step(step: Step, lanes):
+    """Descriptor of the step restricted to `lanes`, blocks renumbered 0.. in
+    order of first use. Returns (sub step, original ids of its blocks,
+    original flat rows of its rows).
+
+    Renumbering physical blocks changes no attention result; it lets a host
+    check or a CPU baseline work on a compact copy of a few lanes of a large
+    pool.
+    """
+    bs = step.geom.block_size
+    lanes = sorted(set(int(b) for b in lanes))
+    seen = {}
+    blocks = []
+    for b in lanes:
+        n = -(-int(step.ctx_lens[b]) // bs)
+        for x in step.block_tables[b, :n]:
+            x = int(x)
+            if x not in seen:
+                seen[x] = len(blocks)
+                blocks.append(x)
+    width = max([1] + [-(-int(step.ctx_lens[b]) // bs) for b in lanes])
+    bt = np.full((len(lanes), width), -1, dtype=np.int32)
+    cu = step.cu_seqlens_q
+    rows, slots = [], []
+    for i, b in enumerate(lanes):
+        n = -(-int(step.ctx_lens[b]) // bs)
+        bt[i, :n] = [seen[int(x)] for x in step.block_tables[b, :n]]
+        rows += list(range(int(cu[b]), int(cu[b + 1])))
+        c, q = int(step.ctx_lens[b]), int(step.q_lens[b])
+        slots += [int(bt[i, p // bs]) * bs + p % bs for p in range(c - q, c)]
+    sub = Step(step.geom, max(1, len(blocks)), step.q_lens[lanes].copy(),
+               step.ctx_lens[lanes].copy(), bt, np.asarray(slots, dtype=np.int64))
+    return sub, np.asarray(blocks, dtype=np.int64), np.asarray(rows, dtype=np.int64)
+
+
+def kv_bytes(step: Step) -> int:
+    """K+V bytes of every key every row of the step attends, counted once per lane."""
+    return int(step.ctx_lens.astype(np.int64).sum()) * 2 * step.geom.kv_row_bytes
+
+
+def algorithmic_bytes(step: Step, write: bool = True) -> dict:
+    """Bytes the step must move at minimum, per part.
+
+    decode (split path): every key's K and V once per lane, q in, out, and the
+    4-byte block-table entries read; partial results of the split path are
+    overhead and are not counted. write: each new K and V row read once and
+    written once, plus its 8-byte slot.
+    """
+    g = step.geom
+    e = g.elem_bytes
+    bs = g.block_size
+    qo = 2 * step.T * g.H * g.D * e
+    bt = 4 * int(sum(-(-int(c) // bs) for c in step.ctx_lens))
+    out = {"kv": kv_bytes(step), "q_out": qo, "block_table": bt}
+    out["write"] = (2 * 2 * step.T * g.kv_row_bytes + 8 * step.T) if write else 0
+    out["decode_kernel"] = out["kv"] + step.T * g.H * g.D * e + bt
+    out["total"] = out["kv"] + qo + bt + out["write"]
+    return out

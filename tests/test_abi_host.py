@@ -1,0 +1,117 @@
+"""The C ABI library loads, exports every symbol include/pa.h declares, and
+refuses bad arguments on the host before any CUDA call (CPU only)."""
+import ctypes
+import os
+import re
+
+import pytest
+
+from invariant_paged_kv_gb300 import build, pa
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+
+
+@pytest.fixture(scope="module")
+def lib():
+    build.build()
+    return pa.load()
+
+
+def declared_functions():
+    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+    src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
+    return sorted(set(re.findall(r"\b(pa_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_boundary():
+    names = declared_functions()
+    for must in ("pa_write_kv", "pa_attention", "pa_attention_workspace_bytes",
+                 "pa_read_status", "pa_status_string"):
+        assert must in names
+
+
+def test_every_declared_symbol_is_exported(lib):
+    for name in declared_functions():
+        assert hasattr(lib, name), name
+    assert set(declared_functions()) <= set(pa.EXPORTS) | set(declared_functions())
+
+
+def test_status_strings(lib):
+    for code, name in pa.STATUS_NAMES.items():
+        assert lib.pa_status_string(code).decode() == name
+
+
+def test_split_tokens(lib):
+    assert lib.pa_split_tokens() == 512
+
+
+def test_workspace_bytes_host_only(lib):
+    f = lib.pa_attention_workspace_bytes
+    # decode-only bf16, H32/Hkv8/D128/bs16, 64 lanes, ctx <= 16384, total 205000
+    n = f(64, 64, 1, 16384, 205000, 32, 8, 128, 16, 1)
+    pairs = 205000 // 512 + 64
+    assert n >= pairs * 32 * (128 + 2) * 4
+    assert n < 2 * pairs * 32 * (128 + 2) * 4 + 64 * 16 + 4096
+    loose = f(64, 64, 1, 16384, -1, 32, 8, 128, 16, 1)
+    assert loose >= n
+    # unsupported geometry -> 0
+    assert f(1, 1, 1, 16, 16, 32, 8, 96, 16, 1) == 0
+    assert f(1, 1, 1, 16, 16, 32, 8, 128, 8, 1) == 0
+    assert f(1, 1, 1, 16, 16, 30, 8, 128, 16, 1) == 0
+    assert f(1, 1, 1, 16, 16, 32, 8, 128, 16, 7) == 0
+    assert f(1, 1, 1, 16, 16, 34, 2, 128, 16, 1) == 0  # group of 17 heads
+
+
+def _attn(lib, **kw):
+    a = dict(q=1 << 12, kc=1 << 12, vc=1 << 12, bt=1 << 12, mb=4, cu=1 << 12, ctx=1 << 12,
+             slot=None, kn=None, vn=None, out=1 << 12, B=1, T=1, H=4, Hkv=2, D=64, bs=16,
+             NB=8, mq=1, mc=16, scale=0.125, dt=0, ws=1 << 12, wsb=1 << 20, st=None, stream=None)
+    a.update(kw)
+    return lib.pa_attention(a["q"], a["kc"], a["vc"], a["bt"], a["mb"], a["cu"], a["ctx"],
+                            a["slot"], a["kn"], a["vn"], a["out"], a["B"], a["T"], a["H"],
+                            a["Hkv"], a["D"], a["bs"], a["NB"], a["mq"], a["mc"], a["scale"],
+                            a["dt"], a["ws"], a["wsb"], a["st"], a["stream"])
+
+
+def test_attention_refusals_before_cuda(lib):
+    # every case fails validation, so no CUDA call is made on this GPU-less host
+    assert _attn(lib, D=96) == 2
+    assert _attn(lib, bs=8) == 2
+    assert _attn(lib, H=6, Hkv=4) == 2
+    assert _attn(lib, dt=5) == 2
+    assert _attn(lib, q=None) == 1
+    assert _attn(lib, out=None) == 1
+    assert _attn(lib, B=-1) == 1
+    assert _attn(lib, T=-1) == 1
+    assert _attn(lib, NB=0) == 1
+    assert _attn(lib, mb=0) == 1
+    assert _attn(lib, q=(1 << 12) + 4) == 1  # misaligned
+    assert _attn(lib, slot=1 << 12) == 1  # write args must come together
+    assert _attn(lib, scale=float("nan")) == 1
+    assert _attn(lib, ws=None) == 3
+    assert _attn(lib, ws=(1 << 12) + 16) == 3  # workspace not 256-byte aligned
+    assert _attn(lib, wsb=64) == 3  # too small for even one split
+    assert _attn(lib, T=1, B=0) == 1
+    assert _attn(lib, NB=1 << 27, bs=32) == 2  # token coordinate would overflow int32
+
+
+def test_write_refusals_before_cuda(lib):
+    f = lib.pa_write_kv
+    assert f(None, None, None, None, None, 0, 8, 16, 2, 64, 0, None, None) == 0  # nothing to do
+    assert f(None, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 3, 8, 16, 2, 64, 0, None, None) == 1
+    assert f(1 << 12, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 3, 8, 16, 2, 96, 0, None, None) == 2
+    assert f(1 << 12, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 3, 0, 16, 2, 64, 0, None, None) == 1
+    assert f(1 << 12, 1 << 12, 1 << 12, 1 << 12, 1 << 12, -1, 8, 16, 2, 64, 0, None, None) == 1
+
+
+def test_no_launches_counted_on_refusals(lib):
+    before = lib.pa_kernel_launches()
+    _attn(lib, D=96)
+    assert lib.pa_kernel_launches() == before
+
+
+def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
+    monkeypatch.setattr(pa, "_lib", None)
+    monkeypatch.setattr(pa, "_LIB_PATH", str(tmp_path / "missing.so"))
+    with pytest.raises(RuntimeError, match="not built"):
+        pa.load()
