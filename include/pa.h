@@ -165,6 +165,46 @@ pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* 
                                 int32_t n_events);
 
 /*
+ * pa_attention_static_scratch -- pa_attention for callers that cannot
+ * allocate device memory. (No counterpart in the paper: this entry point
+ * exists for integration, not for the method.)
+ *
+ * Some callers cannot call cudaMalloc where they run a step: a plugin whose
+ * host framework offers it no device allocator, a process whose memory pool
+ * has claimed all free device memory up front, or a latency-critical loop
+ * that cannot take the device-wide synchronisation cudaMalloc / cudaFree may
+ * cause. This entry point takes the same inputs and outputs as pa_attention
+ * but no workspace: its split-KV scratch is one array of
+ * PA_STATIC_SCRATCH_BYTES compiled into the library, which every GPU that
+ * loads the library holds until the process exits. It calls no cudaMalloc,
+ * cudaFree or other allocating routine.
+ *
+ *   total_ctx  sum of ctx_lens over the lanes (negative if unknown), used
+ *              with B, T, max_q_len and max_ctx_len to bound the scratch the
+ *              step needs, exactly as pa_attention_workspace_bytes does.
+ * Returns PA_ERR_WORKSPACE, before any CUDA call, when that bound exceeds
+ * PA_STATIC_SCRATCH_BYTES; PA_ERR_UNSUPPORTED for unsupported geometry.
+ * Set-up: the first call on each device looks up the array's device address
+ * (cudaGetSymbolAddress, with that device current) and keeps it; make that
+ * first call before any stream capture. Every call on a device shares the
+ * one array and it keeps the last call's contents (nothing in it needs to
+ * start at zero); calls whose work overlaps on the GPU -- on different
+ * streams, or from different threads -- race on it and must be serialised by
+ * the caller.
+ */
+#define PA_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
+
+pa_status pa_attention_static_scratch(const void* q, const void* k_cache, const void* v_cache,
+                                      const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                      const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                      const int64_t* slot_mapping, const void* k_new,
+                                      const void* v_new, void* out, int32_t B, int32_t T,
+                                      int32_t H, int32_t Hkv, int32_t D, int32_t block_size,
+                                      int32_t num_blocks, int32_t max_q_len, int32_t max_ctx_len,
+                                      int64_t total_ctx, float scale, pa_dtype dtype,
+                                      int32_t* status, void* stream);
+
+/*
  * pa_read_status -- wait for `stream`, copy the device status word to
  * *flags_out and, if clear != 0, reset it to zero. The only synchronising call.
  */

@@ -26,7 +26,7 @@ FLAGS = {
 
 EXPORTS = ("pa_write_kv", "pa_attention_workspace_bytes", "pa_attention",
            "pa_attention_profiled", "pa_read_status", "pa_status_string",
-           "pa_kernel_launches", "pa_split_tokens")
+           "pa_kernel_launches", "pa_split_tokens", "pa_attention_static_scratch")
 
 
 class PaError(RuntimeError):
@@ -70,6 +70,10 @@ def load() -> ctypes.CDLL:
     L.pa_kernel_launches.restype = i64
     L.pa_split_tokens.argtypes = []
     L.pa_split_tokens.restype = i32
+    L.pa_attention_static_scratch.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, i32,
+                                              i32, i32, i32, i32, i32, i32, i32, i32, i64, f32,
+                                              i32, vp, vp]
+    L.pa_attention_static_scratch.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -168,3 +172,28 @@ def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,
                 e.record(stream)
         arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
         _check(L.pa_attention_profiled(*args, arr, len(events)), "pa_attention_profiled")
+
+
+def attention_static_scratch(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,
+                             max_q_len: int, max_ctx_len: int, total_ctx: int, scale: float,
+                             slot_mapping=None, k_new=None, v_new=None, status=None,
+                             stream=None):
+    """pa_attention_static_scratch: like ``attention`` but without a workspace.
+
+    For callers that cannot allocate device memory: the split scratch is an
+    array built into the library (``PA_STATIC_SCRATCH_BYTES`` per GPU). Steps
+    that need more raise PaError(PA_ERR_WORKSPACE). Calls overlapping on the
+    GPU share that array and must be serialised by the caller.
+    """
+    T, H, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    B = ctx_lens.shape[0]
+    if block_tables.dtype != torch.int32 or cu_seqlens_q.dtype != torch.int32 \
+            or ctx_lens.dtype != torch.int32:
+        raise TypeError("block_tables, cu_seqlens_q and ctx_lens must be int32")
+    mb = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    _check(load().pa_attention_static_scratch(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mb, _ptr(cu_seqlens_q),
+        _ptr(ctx_lens), _ptr(slot_mapping), _ptr(k_new), _ptr(v_new), _ptr(out), B, T, H, Hkv,
+        D, bs, NB, int(max_q_len), int(max_ctx_len), int(total_ctx), float(scale),
+        _dtype_code(q), _ptr(status), _stream(stream)), "pa_attention_static_scratch")
