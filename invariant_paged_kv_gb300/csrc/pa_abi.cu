@@ -16,6 +16,8 @@ cudaError_t launch_decode_bf16(const StepParams& p, const CUtensorMap& k, const 
                                long long max_items, cudaStream_t s);
 cudaError_t launch_split_f32(const StepParams& p, long long max_items, cudaStream_t s);
 cudaError_t launch_combine(const StepParams& p, cudaStream_t s);
+cudaError_t launch_prefill_tc(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                              const CUtensorMap& v, long long max_items, cudaStream_t s);
 
 static std::atomic<long long> g_launches{0};
 
@@ -51,23 +53,30 @@ pa_status check_geometry(int32_t H, int32_t Hkv, int32_t D, int32_t block_size, 
   return PA_OK;
 }
 
-// Every row takes the split path for fp32; for bf16 only decode lanes do,
-// except while a step holds a prefill lane (max_q_len >= 2) that the
-// tensor-core prefill kernel does not cover yet.
+// Every row takes the split path for fp32 (CUDA-core FMA, no TF32). For
+// bf16 only decode lanes (q_len == 1) do; lanes with q_len >= 2 go to the
+// tensor-core prefill kernel.
 bool split_all_rows(pa_dtype dtype, int32_t max_q_len) {
   (void)max_q_len;
-  return dtype == PA_F32 || max_q_len >= 2;
+  return dtype == PA_F32;
 }
 
+// Prefill tiles a step can hold: sum over lanes of ceil(q_len / 128).
+long long max_prefill_tiles(int32_t B, int32_t T) { return (long long)T / kPrefillRows + B + 1; }
+
 struct Layout {
-  size_t header, row_info, pairs, ml, acc, fixed, per_pair;
+  size_t header, row_info, ptiles, ptiles_tmp, pairs, fixed, per_pair;
+  int ptile_capacity;
 };
 
-Layout layout_for(int32_t T, int32_t H, int32_t D) {
+Layout layout_for(int32_t B, int32_t T, int32_t H, int32_t D) {
   Layout L;
+  L.ptile_capacity = (int)max_prefill_tiles(B, T);
   L.header = 0;
   L.row_info = kAlign;
-  L.pairs = L.row_info + align_up((size_t)T * sizeof(int4));
+  L.ptiles = L.row_info + align_up((size_t)T * sizeof(int4));
+  L.ptiles_tmp = L.ptiles + align_up((size_t)L.ptile_capacity * sizeof(int4));
+  L.pairs = L.ptiles_tmp + align_up((size_t)L.ptile_capacity * sizeof(int4));
   L.fixed = L.pairs;
   L.per_pair = sizeof(int4) + (size_t)H * sizeof(float2) + (size_t)H * D * sizeof(float);
   return L;
@@ -88,29 +97,32 @@ long long max_pairs(int32_t B, int32_t T, int32_t max_q_len, int32_t max_ctx_len
   return loose;
 }
 
-size_t bytes_for_pairs(int32_t T, int32_t H, int32_t D, long long pairs) {
-  const Layout L = layout_for(T, H, D);
+size_t bytes_for_pairs(int32_t B, int32_t T, int32_t H, int32_t D, long long pairs) {
+  const Layout L = layout_for(B, T, H, D);
   // pairs, ml and acc as three arrays, each 256-byte aligned
   return L.fixed + align_up((size_t)pairs * sizeof(int4)) +
          align_up((size_t)pairs * H * sizeof(float2)) +
          align_up((size_t)pairs * H * D * sizeof(float));
 }
 
-int capacity_of(size_t bytes, int32_t T, int32_t H, int32_t D) {
-  const Layout L = layout_for(T, H, D);
+int capacity_of(size_t bytes, int32_t B, int32_t T, int32_t H, int32_t D) {
+  const Layout L = layout_for(B, T, H, D);
   if (bytes <= L.fixed) return 0;
   long long cap = (long long)((bytes - L.fixed) / L.per_pair);
-  while (cap > 0 && bytes_for_pairs(T, H, D, cap) > bytes) --cap;
+  while (cap > 0 && bytes_for_pairs(B, T, H, D, cap) > bytes) --cap;
   if (cap > 0x7fffffffLL) cap = 0x7fffffffLL;
   return (int)cap;
 }
 
-SplitPlan carve(void* ws, int cap, int32_t T, int32_t H, int32_t D) {
-  const Layout L = layout_for(T, H, D);
+SplitPlan carve(void* ws, int cap, int32_t B, int32_t T, int32_t H, int32_t D) {
+  const Layout L = layout_for(B, T, H, D);
   char* b = static_cast<char*>(ws);
   SplitPlan pl;
   pl.header = reinterpret_cast<int*>(b + L.header);
   pl.row_info = reinterpret_cast<int4*>(b + L.row_info);
+  pl.ptiles = reinterpret_cast<int4*>(b + L.ptiles);
+  pl.ptiles_tmp = reinterpret_cast<int4*>(b + L.ptiles_tmp);
+  pl.ptile_capacity = L.ptile_capacity;
   size_t off = L.pairs;
   pl.pairs = reinterpret_cast<int4*>(b + off);
   off += align_up((size_t)cap * sizeof(int4));
@@ -145,6 +157,20 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, int NB, int bs, int H
   cuuint32_t box[3] = {64, 1, (cuuint32_t)kChunk};
   cuuint32_t estr[3] = {1, 1, 1};
   CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(cache), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+// q [T, H, D] bf16; box = 64 elements x 1 head x 128 rows, 128-byte swizzle.
+bool encode_q_map(CUtensorMap* map, const void* q, int T, int H, int D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)H, (cuuint64_t)T};
+  cuuint64_t strides[2] = {(cuuint64_t)D * 2, (cuuint64_t)H * D * 2};
+  cuuint32_t box[3] = {64, 1, (cuuint32_t)kPrefillRows};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 3, const_cast<void*>(q), dims, strides,
                   box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
@@ -219,7 +245,7 @@ size_t pa_attention_workspace_bytes(int32_t B, int32_t T, int32_t max_q_len,
   if (B < 0 || T < 0 || max_q_len < 0 || max_ctx_len < 0) return 0;
   if (check_geometry(H, Hkv, D, block_size, dtype) != PA_OK) return 0;
   const long long pairs = max_pairs(B, T, max_q_len, max_ctx_len, total_ctx, dtype);
-  return bytes_for_pairs(T, H, D, pairs > 0 ? pairs : 1);
+  return bytes_for_pairs(B, T, H, D, pairs > 0 ? pairs : 1);
 }
 
 pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* v_cache,
@@ -257,7 +283,7 @@ pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* 
   if (with_write && (!aligned16(k_new) || !aligned16(v_new))) return PA_ERR_INVALID_ARG;
   if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)))
     return PA_ERR_WORKSPACE;
-  const int cap = capacity_of(workspace_bytes, T, H, D);
+  const int cap = capacity_of(workspace_bytes, B, T, H, D);
   if (cap <= 0) return PA_ERR_WORKSPACE;
 
   StepParams p;
@@ -287,13 +313,15 @@ pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* 
   p.split_all_rows = split_all_rows(dtype, max_q_len) ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
-  p.plan = carve(workspace, cap, T, H, D);
+  p.plan = carve(workspace, cap, B, T, H, D);
+  const bool prefill_tc = dtype == PA_BF16 && max_q_len >= 2;
 
-  CUtensorMap tmK, tmV;
+  CUtensorMap tmK, tmV, tmQ;
   if (dtype == PA_BF16) {
     if (!encode_cache_map(&tmK, k_cache, num_blocks, block_size, Hkv, D) ||
         !encode_cache_map(&tmV, v_cache, num_blocks, block_size, Hkv, D))
       return PA_ERR_CUDA;
+    if (prefill_tc && !encode_q_map(&tmQ, q, T, H, D)) return PA_ERR_CUDA;
   }
   long long items = max_pairs(B, T, max_q_len, max_ctx_len, -1, dtype);
   if (items > cap) items = cap;
@@ -308,6 +336,11 @@ pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* 
   if (e != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
   if (record(events, n_events, 2, s) != PA_OK) return PA_ERR_CUDA;
+  if (prefill_tc) {
+    const long long pitems = max_prefill_tiles(B, T) * H;
+    if (launch_prefill_tc(p, tmQ, tmK, tmV, pitems, s) != cudaSuccess) return PA_ERR_CUDA;
+    count_launches(1);
+  }
   if (record(events, n_events, 3, s) != PA_OK) return PA_ERR_CUDA;
   if (launch_combine(p, s) != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);

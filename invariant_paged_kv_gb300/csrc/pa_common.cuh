@@ -23,9 +23,12 @@ constexpr long long kWaitCycles = 2000000000LL;
 // ---------------------------------------------------------------------------
 // Split plan, built on the device by the prologue kernel from cu_seqlens_q and
 // ctx_lens, stored in the workspace:
-//   header[0] = number of (row, split) pairs, header[1] = number of full pairs
+//   header[0] = number of (row, split) pairs, header[1] = number of full pairs,
+//   header[2] = number of prefill q tiles
 //   row_info[r] = {first full pair, tail pair or -1, number of splits, lane or -1}
 //   pairs[k]    = {row, split index, lane, key count of the row}
+//   ptiles[i]   = {lane, 128-row tile index, position of its last row, 0},
+//                 heaviest first (tensor-core prefill path)
 // Full pairs (exactly kSplit keys) come first, lane-major; tail pairs after.
 // Partial results of pair k: ml[k * H + h] = {m (log2 domain), l},
 // acc[(k * H + h) * D + d].
@@ -33,11 +36,17 @@ constexpr long long kWaitCycles = 2000000000LL;
 struct SplitPlan {
   int* header;
   int4* row_info;
+  int4* ptiles;
+  int4* ptiles_tmp;  // unsorted list, scratch of the plan
   int4* pairs;
   float2* ml;
   float* acc;
-  int capacity;  // pairs the workspace holds
+  int capacity;        // pairs the workspace holds
+  int ptile_capacity;  // prefill tiles the workspace holds
 };
+
+// Query rows per tile of the tensor-core prefill path.
+constexpr int kPrefillRows = 128;
 
 struct StepParams {
   const void* q;

@@ -27,11 +27,9 @@ __device__ __forceinline__ long long floor_sum(long long n) {
   return kSplit * t * (t - 1) / 2 + t * (r + 1);
 }
 
-// Validates lane b and returns its contribution to the plan: the number of
-// full and tail split ranges over its rows. `report` raises status flags.
-__device__ bool lane_plan(const StepParams& p, int b, bool report, int& q, int& c, int& cu0,
-                          long long& nfull, long long& ntail) {
-  nfull = ntail = 0;
+// Validates lane b (raising status flags when `report`) and returns whether
+// it is well formed; q, c, cu0 are its q_len, ctx_len and first row.
+__device__ bool lane_valid(const StepParams& p, int b, bool report, int& q, int& c, int& cu0) {
   cu0 = p.cu_seqlens[b];
   const int cu1 = p.cu_seqlens[b + 1];
   c = p.ctx_lens[b];
@@ -45,10 +43,16 @@ __device__ bool lane_plan(const StepParams& p, int b, bool report, int& q, int& 
     bad = PA_FLAG_QLEN_RANGE;
   else if (q > p.max_q_len || c > p.max_ctx_len)
     bad = PA_FLAG_HOST_BOUND;
-  if (bad) {
-    if (report) raise_flag(p.status, bad);
-    return false;
-  }
+  if (bad && report) raise_flag(p.status, bad);
+  return bad == 0;
+}
+
+// Lane b's contribution to the split plan: the number of full and tail split
+// ranges over its rows (zero when the lane is not on the split path).
+__device__ bool lane_plan(const StepParams& p, int b, bool report, int& q, int& c, int& cu0,
+                          long long& nfull, long long& ntail) {
+  nfull = ntail = 0;
+  if (!lane_valid(p, b, report, q, c, cu0)) return false;
   const bool on_split = q >= 1 && (p.split_all_rows || q == 1);
   if (!on_split) return false;
   // rows attend k = c - q + 1 .. c keys
@@ -102,6 +106,57 @@ __device__ void block_scan2(long long a, long long b, long long& ea, long long& 
   __syncthreads();
 }
 
+// Tensor-core prefill tiles: 128-row tiles of every lane with q_len >= 2
+// (when those lanes do not take the split path), ordered heaviest first (by
+// the position of the tile's last row; ties by list order) when there are at
+// most 1024 of them. The order only decides which CTA runs a tile first.
+__device__ void build_prefill_tiles(const StepParams& p) {
+  __shared__ int s_work[1024];
+  const int tid = threadIdx.x, nth = blockDim.x;
+  const SplitPlan& pl = p.plan;
+  long long total = 0;
+  if (!p.split_all_rows) {
+    for (int base = 0; base < p.B; base += nth) {
+      const int b = base + tid;
+      int q = 0, c = 0, cu0 = 0;
+      long long nt = 0;
+      if (b < p.B && lane_valid(p, b, false, q, c, cu0) && q >= 2)
+        nt = (q + kPrefillRows - 1) / kPrefillRows;
+      long long e0, e1, t0, t1;
+      block_scan2(nt, 0, e0, e1, t0, t1);
+      if (nt > 0 && total + e0 + nt <= pl.ptile_capacity) {
+        for (int t = 0; t < nt; ++t) {
+          const int last = min(q, (t + 1) * kPrefillRows) - 1;
+          pl.ptiles_tmp[total + e0 + t] = make_int4(b, t, c - q + last, 0);
+        }
+      }
+      total += t0;
+    }
+  }
+  if (total > pl.ptile_capacity) {
+    if (tid == 0) raise_flag(p.status, PA_FLAG_WORKSPACE);
+    total = 0;
+  }
+  __syncthreads();
+  const int n = (int)total;
+  if (n <= nth) {
+    if (tid < n) s_work[tid] = pl.ptiles_tmp[tid].z;
+    __syncthreads();
+    if (tid < n) {
+      const int w = s_work[tid];
+      int rank = 0;
+      for (int j = 0; j < n; ++j) {
+        const int x = s_work[j];
+        rank += (x > w) || (x == w && j < tid);
+      }
+      pl.ptiles[rank] = pl.ptiles_tmp[tid];
+    }
+  } else {
+    for (int i = tid; i < n; i += nth) pl.ptiles[i] = pl.ptiles_tmp[i];
+  }
+  if (tid == 0) pl.header[2] = n;
+}
+
 __device__ void build_plan(const StepParams& p) {
   const int tid = threadIdx.x, nth = blockDim.x;
   const SplitPlan& pl = p.plan;
@@ -125,6 +180,7 @@ __device__ void build_plan(const StepParams& p) {
       pl.header[0] = 0;
       pl.header[1] = 0;
     }
+    build_prefill_tiles(p);
     return;
   }
   long long carry_full = 0, carry_tail = 0;
@@ -160,6 +216,7 @@ __device__ void build_plan(const StepParams& p) {
     pl.header[0] = (int)(tot_full + tot_tail);
     pl.header[1] = (int)tot_full;
   }
+  build_prefill_tiles(p);
 }
 
 __device__ void write_rows(const StepParams& p, int cta, int ncta) {

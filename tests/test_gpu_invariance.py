@@ -119,3 +119,43 @@ def test_poisoned_tails_do_not_leak():
     b, _ = run_attention(step, dirty)
     assert not torch.isnan(b.float()).any()
     assert torch.equal(a.view(torch.int16), b.view(torch.int16))
+
+
+def test_prefill_rows_bitwise_across_compositions():
+    """A fixed 200-row prefill chunk (positions 800..999) keeps its output bits
+    whatever lanes surround it and wherever its blocks sit."""
+    geom = wl.Geometry(32, 8, 128, 16, "bf16")
+    g = torch.Generator(device="cuda").manual_seed(99)
+    C, Q = 1000, 200
+    mk = lambda *s: torch.randn(*s, generator=g, device="cuda", dtype=torch.bfloat16)
+    K, V, q = mk(C, 8, 128), mk(C, 8, 128), mk(Q, 32, 128)
+    ref = None
+    for t in (1, 2, 5, 17):
+        rng = np.random.default_rng(500 + t)
+        lanes = [(1, int(rng.integers(1, 5000))) if rng.random() < 0.6 else
+                 (int(rng.integers(2, 300)), int(rng.integers(300, 3000))) for _ in range(t - 1)]
+        pos = int(rng.integers(0, t))
+        lanes.insert(pos, (Q, C))
+        ql = [x[0] for x in lanes]
+        cl = [x[1] for x in lanes]
+        used = sum(-(-c // 16) for c in cl)
+        step = wl.build_step(geom, ql, cl, int(used * 1.2) + 4, rng)
+        tens = wl.make_tensors(step, 900 + t, "cuda")
+        bs = 16
+        p_ = np.arange(C)
+        flat = torch.from_numpy(step.block_tables[pos, p_ // bs].astype(np.int64) * bs + p_ % bs).cuda()
+        r0 = int(step.cu_seqlens_q[pos])
+        tens["k_cache"][0].view(-1, 8, 128)[flat[:C - Q]] = K[:C - Q]
+        tens["v_cache"][0].view(-1, 8, 128)[flat[:C - Q]] = V[:C - Q]
+        tens["k_new"][0][r0:r0 + Q] = K[C - Q:]
+        tens["v_new"][0][r0:r0 + Q] = V[C - Q:]
+        tens["q"][0][r0:r0 + Q] = q
+        out, flags = run_attention(step, tens)
+        assert flags == 0
+        bits = out[r0:r0 + Q].view(torch.int16).cpu()
+        if ref is None:
+            ref = bits
+            oref, _, _ = oracle_attention(step, to_cpu(tens), rows=list(range(r0, r0 + Q)))
+            assert max_abs(out, oref, list(range(r0, r0 + Q))) <= 2e-2
+        else:
+            assert torch.equal(bits, ref), f"prefill rows changed in the {t}-lane step"

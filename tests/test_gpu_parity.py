@@ -126,6 +126,17 @@ def test_gqa_groups_bf16(H, Hkv):
     _check_step(step, 91)
 
 
+@pytest.mark.parametrize("D,bs", [(128, 16), (64, 32), (128, 32)])
+def test_prefill_chunk_edges_bf16(D, bs):
+    """Tensor-core prefill: chunks on and off 128-row / 128-key tile edges,
+    chunks starting at key 0, a 2-row chunk, next to decode rows."""
+    geom = wl.Geometry(16, 2, D, bs, "bf16")
+    q = [128, 129, 300, 2, 257, 1, 64, 1]
+    ctx = [128, 300, 1000, 2, 384, 700, 64 + 191, 5]
+    step = _ragged(geom, q, ctx, 21)
+    _check_step(step, 211)
+
+
 def test_mixed_small_full():
     """Mixed bf16 step, small enough for the oracle on every row."""
     geom = wl.Geometry(40, 8, 128, 16, "bf16")
