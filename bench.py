@@ -233,6 +233,16 @@ def measured_hbm_peak():
         return FALLBACK_HBM_GBS, "fallback"
 
 
+def measured_bf16_peak(sustained):
+    path = os.path.join(ROOT, "MEASURED_PEAKS.json")
+    key = "bf16_tflops_sustained" if sustained else "bf16_tflops"
+    try:
+        with open(path) as f:
+            return float(json.load(f)[key]), "measured " + ("sustained" if sustained else "burst")
+    except (OSError, KeyError, ValueError):
+        return (1700.0 if sustained else 1900.0), "fallback"
+
+
 def committed_traffic():
     """Per-launch DRAM bytes of the decode kernel from the committed ncu
     summary, if the kernel sources still match the ones it was taken on."""
@@ -326,9 +336,11 @@ def run_ours(args, rank, world, local_rank):
     if flags:
         raise RuntimeError(f"device status flags {flags:#x}")
     decode_ms = [e[1].elapsed_time(e[2]) for st in ev for e in st]
+    prefill_ms = [e[2].elapsed_time(e[3]) for st in ev for e in st]
     phase_ms = {
         "prologue": statistics.mean(e[0].elapsed_time(e[1]) for st in ev for e in st),
         "decode": statistics.mean(decode_ms),
+        "prefill": statistics.mean(prefill_ms),
         "combine": statistics.mean(e[3].elapsed_time(e[4]) for st in ev for e in st),
     }
     ms_t = torch.tensor([ms], dtype=torch.float64, device=dev)
@@ -389,6 +401,9 @@ def run_ours(args, rank, world, local_rank):
 
     peak, peak_kind = measured_hbm_peak()
     dec_ms = statistics.mean(decode_ms)
+    dec_bytes = wl.decode_rows_kv_bytes(step) + (step.q_lens == 1).sum() * g.H * g.D * g.elem_bytes \
+        + 4 * int(sum(-(-int(c) // g.block_size) for c, q in zip(step.ctx_lens, step.q_lens) if q == 1))
+    nbytes["decode_kernel"] = int(dec_bytes)
     achieved = nbytes["decode_kernel"] / (dec_ms * 1e-3) / 1e9
     traffic, sha = committed_traffic()
     roofline = {"bound": "hbm", "kernel": "decode_bf16_kernel (split-KV decode partials)",
@@ -396,6 +411,17 @@ def run_ours(args, rank, world, local_rank):
                 "peak_kind": peak_kind, "frac": round(achieved / peak, 4),
                 "traffic": traffic, "algorithmic_bytes_per_launch": nbytes["decode_kernel"],
                 "avg_launch_ms": round(dec_ms, 4), "source_sha256_16": sha}
+
+    prefill = None
+    pf = wl.prefill_flops(step)
+    if pf:
+        pf_ms = statistics.mean(prefill_ms)
+        tpeak, tkind = measured_bf16_peak(sustained=True)
+        ach = pf / (pf_ms * 1e-3) / 1e12
+        prefill = {"bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05, bf16 -> fp32)",
+                   "achieved": round(ach, 1), "peak": tpeak, "unit": "TFLOP/s",
+                   "peak_kind": tkind, "frac": round(ach / tpeak, 4),
+                   "flops_per_launch": pf, "avg_launch_ms": round(pf_ms, 4)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
@@ -413,7 +439,7 @@ def run_ours(args, rank, world, local_rank):
         "frac_of_hbm_peak": round(value / peak, 4),
         "bytes_per_step": step_bytes,
         "phase_ms_per_layer": {k: round(v, 4) for k, v in phase_ms.items()},
-        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+        "roofline": roofline, "prefill_roofline": prefill, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
         "clocks": clk,
     }
     return line

@@ -126,7 +126,7 @@ size_t pa_attention_workspace_bytes(int32_t B, int32_t T, int32_t max_q_len,
  *                    not exist; every other row is written
  *   max_q_len, max_ctx_len
  *                    host upper bounds over lanes, used only to size grids
- *   scale            softmax scale applied to q.k (fp32)
+ *   scale            softmax scale applied to q.k (fp32, finite and > 0)
  *   workspace        device scratch of workspace_bytes >= the value
  *                    pa_attention_workspace_bytes returns for this step,
  *                    256-byte aligned; contents on entry are irrelevant

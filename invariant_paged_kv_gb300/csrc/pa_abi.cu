@@ -263,7 +263,7 @@ pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* 
     return PA_ERR_INVALID_ARG;
   pa_status g = check_geometry(H, Hkv, D, block_size, dtype);
   if (g != PA_OK) return g;
-  if (!std::isfinite(scale)) return PA_ERR_INVALID_ARG;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
   const bool with_write = slot_mapping || k_new || v_new;
   if (with_write && !(slot_mapping && k_new && v_new)) return PA_ERR_INVALID_ARG;
   if ((long long)num_blocks * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
@@ -337,7 +337,7 @@ pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* 
   count_launches(1);
   if (record(events, n_events, 2, s) != PA_OK) return PA_ERR_CUDA;
   if (prefill_tc) {
-    const long long pitems = max_prefill_tiles(B, T) * H;
+    const long long pitems = max_prefill_tiles(B, T) * Hkv * ((H / Hkv + 1) / 2);
     if (launch_prefill_tc(p, tmQ, tmK, tmV, pitems, s) != cudaSuccess) return PA_ERR_CUDA;
     count_launches(1);
   }

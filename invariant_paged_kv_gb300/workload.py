@@ -442,3 +442,22 @@ def algorithmic_bytes(step: Step, write: bool = True) -> dict:
     out["decode_kernel"] = out["kv"] + step.T * g.H * g.D * e + bt
     out["total"] = out["kv"] + qo + bt + out["write"]
     return out
+
+
+def prefill_flops(step: Step) -> int:
+    """Dense-contraction flops of the prefill lanes (q_len >= 2): per row and
+    head, 2 D flops for q.k and 2 D for p.v over each attended key; a lane of q
+    rows after `off` earlier keys attends q * off + q (q + 1) / 2 keys per head."""
+    g = step.geom
+    tot = 0
+    for q, c in zip(step.q_lens.tolist(), step.ctx_lens.tolist()):
+        if q >= 2:
+            off = c - q
+            tot += g.H * 4 * g.D * (q * off + q * (q + 1) // 2)
+    return int(tot)
+
+
+def decode_rows_kv_bytes(step: Step) -> int:
+    """K+V bytes the decode lanes (q_len == 1) attend."""
+    m = step.q_lens == 1
+    return int(step.ctx_lens[m].astype(np.int64).sum()) * 2 * step.geom.kv_row_bytes

@@ -88,6 +88,8 @@ def test_attention_refusals_before_cuda(lib):
     assert _attn(lib, q=(1 << 12) + 4) == 1  # misaligned
     assert _attn(lib, slot=1 << 12) == 1  # write args must come together
     assert _attn(lib, scale=float("nan")) == 1
+    assert _attn(lib, scale=0.0) == 1
+    assert _attn(lib, scale=-0.125) == 1
     assert _attn(lib, ws=None) == 3
     assert _attn(lib, ws=(1 << 12) + 16) == 3  # workspace not 256-byte aligned
     assert _attn(lib, wsb=64) == 3  # too small for even one split
