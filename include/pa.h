@@ -130,11 +130,13 @@ size_t pa_attention_workspace_bytes(int32_t B, int32_t T, int32_t max_q_len,
  *   workspace        device scratch of workspace_bytes >= the value
  *                    pa_attention_workspace_bytes returns for this step,
  *                    256-byte aligned; contents on entry are irrelevant
- * Lanes with q_len == 1 take the split-KV decode path: keys are split in
- * fixed 512-token ranges [512 i, 512 (i + 1)), each range reduced in
- * ascending key order, and the ranges folded left to right in fp32. Lanes
- * with q_len >= 2 take the prefill path. Which path a row takes, its split
- * points and its reduction order depend only on its own lane.
+ * Lanes with q_len == 1 take the split-KV decode path: a row with K keys is
+ * split into ranges [S i, S (i + 1)) with S = 512 * 2^j for the smallest j
+ * that gives at most 128 ranges (512-key ranges up to K = 65536), each range
+ * reduced in ascending key order, and the ranges folded left to right in
+ * fp32. Lanes with q_len >= 2 take the prefill path. Which path a row
+ * takes, its split points and its reduction order depend only on its own
+ * lane.
  */
 pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
                        const int32_t* block_tables, int32_t max_blocks_per_seq,
@@ -216,7 +218,8 @@ const char* pa_status_string(pa_status s);
 /* Kernels this process has launched through the library so far. */
 int64_t pa_kernel_launches(void);
 
-/* Split length (keys) of the decode path: fixed for every geometry. */
+/* Shortest split length (keys) of the decode path; longer rows use the
+ * power-of-two multiple of it that keeps them at most 128 splits. */
 int32_t pa_split_tokens(void);
 
 #ifdef __cplusplus

@@ -84,7 +84,8 @@ Layout layout_for(int32_t B, int32_t T, int32_t H, int32_t D) {
 
 long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
-// Upper bound on (row, split) pairs of a step.
+// Upper bound on (row, split) pairs of a step (split_len(K) >= kSplit, so a
+// row of K keys has at most ceil(K / kSplit) splits).
 long long max_pairs(int32_t B, int32_t T, int32_t max_q_len, int32_t max_ctx_len,
                     int64_t total_ctx, pa_dtype dtype) {
   const long long per_row = ceil_div(max_ctx_len > 0 ? max_ctx_len : 1, kSplit);

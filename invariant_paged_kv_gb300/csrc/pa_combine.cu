@@ -10,54 +10,81 @@
 // combine_attention_partials with the ordered fold), applied to splits
 // instead of ranks. n depends only on the row's own key count, so the fold is
 // the same whatever else is in the step.
+#include <type_traits>
+
 #include "pa_common.cuh"
 
 namespace pa {
 
 namespace {
 
-__global__ void __launch_bounds__(128) combine_kernel(const StepParams p) {
+constexpr int kWarps = 8;   // heads per CTA (one warp per (row, head))
+constexpr int kAhead = 8;   // splits loaded ahead of the fold
+
+// One warp folds the splits of one (row, head); lane l owns dims 4l .. 4l+3
+// (D = 128) or 2l .. 2l+1 (D = 64). The loads of kAhead splits are issued
+// before their fold so the memory system sees many requests at once; the fold
+// itself runs strictly in split order.
+template <int D>
+__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p) {
+  constexpr int VPL = D / 32;  // values per lane
+  using Vec = typename std::conditional<VPL == 4, float4, float2>::type;
   const int row = blockIdx.x;
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  const int h = blockIdx.y * kWarps + warp;
+  if (h >= p.H) return;
   const int4 info = p.plan.row_info[row];
   if (info.w < 0 || info.z <= 1) return;  // not on the split path, or written directly
   const int n = info.z;
   const int nfull = info.y >= 0 ? n - 1 : n;
-  const int D4 = p.D / 4;
-  const int hpc = blockDim.x / D4;  // heads per CTA
-  const int h = blockIdx.y * hpc + threadIdx.x / D4;
-  if (h >= p.H) return;
-  const int d4 = threadIdx.x - (threadIdx.x / D4) * D4;
-  const float4* acc = reinterpret_cast<const float4*>(p.plan.acc);
+  const Vec* acc = reinterpret_cast<const Vec*>(p.plan.acc);
 
   Fold f;
-  float4 A = make_float4(0.f, 0.f, 0.f, 0.f);
-#pragma unroll 4
-  for (int i = 0; i < n; ++i) {
-    const int pair = i < nfull ? info.x + i : info.y;
-    const float2 ml = p.plan.ml[(size_t)pair * p.H + h];
-    const float4 a = acc[((size_t)pair * p.H + h) * D4 + d4];
-    if (i == 0) {
-      f.first(ml.x, ml.y);
-      A = a;
-    } else {
-      float ea, eb;
-      f.next(ml.x, ml.y, ea, eb);
-      A.x = fmaf(A.x, ea, a.x * eb);
-      A.y = fmaf(A.y, ea, a.y * eb);
-      A.z = fmaf(A.z, ea, a.z * eb);
-      A.w = fmaf(A.w, ea, a.w * eb);
+  float A[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) A[j] = 0.f;
+  for (int i0 = 0; i0 < n; i0 += kAhead) {
+    float2 ml[kAhead];
+    Vec a[kAhead];
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const int i = i0 + u;
+      if (i < n) {
+        const int pair = i < nfull ? info.x + i : info.y;
+        ml[u] = p.plan.ml[(size_t)pair * p.H + h];
+        a[u] = acc[((size_t)pair * p.H + h) * 32 + lane];
+      }
+    }
+#pragma unroll
+    for (int u = 0; u < kAhead; ++u) {
+      const int i = i0 + u;
+      if (i < n) {
+        const float* av = reinterpret_cast<const float*>(&a[u]);
+        if (i == 0) {
+          f.first(ml[u].x, ml[u].y);
+#pragma unroll
+          for (int j = 0; j < VPL; ++j) A[j] = av[j];
+        } else {
+          float ea, eb;
+          f.next(ml[u].x, ml[u].y, ea, eb);
+#pragma unroll
+          for (int j = 0; j < VPL; ++j) A[j] = fmaf(A[j], ea, av[j] * eb);
+        }
+      }
     }
   }
-  const size_t o = ((size_t)row * p.H + h) * p.D + 4 * d4;
-  const float r0 = finish_div(A.x, f.L), r1 = finish_div(A.y, f.L);
-  const float r2 = finish_div(A.z, f.L), r3 = finish_div(A.w, f.L);
+  const size_t o = ((size_t)row * p.H + h) * D + VPL * lane;
+  float r[VPL];
+#pragma unroll
+  for (int j = 0; j < VPL; ++j) r[j] = finish_div(A[j], f.L);
   if (p.elem_bytes == 4) {
-    *reinterpret_cast<float4*>(static_cast<float*>(p.out) + o) = make_float4(r0, r1, r2, r3);
+    float* out = static_cast<float*>(p.out) + o;
+#pragma unroll
+    for (int j = 0; j < VPL; ++j) out[j] = r[j];
   } else {
-    uint2 v;
-    v.x = pack_bf16x2(r0, r1);
-    v.y = pack_bf16x2(r2, r3);
-    *reinterpret_cast<uint2*>(static_cast<__nv_bfloat16*>(p.out) + o) = v;
+    uint32_t* out = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + o);
+#pragma unroll
+    for (int j = 0; j < VPL; j += 2) out[j / 2] = pack_bf16x2(r[j], r[j + 1]);
   }
 }
 
@@ -65,10 +92,11 @@ __global__ void __launch_bounds__(128) combine_kernel(const StepParams p) {
 
 cudaError_t launch_combine(const StepParams& p, cudaStream_t s) {
   if (p.T <= 0) return cudaSuccess;
-  const int D4 = p.D / 4;
-  const int hpc = 128 / D4;
-  dim3 grid(p.T, (p.H + hpc - 1) / hpc);
-  combine_kernel<<<grid, 128, 0, s>>>(p);
+  dim3 grid(p.T, (p.H + kWarps - 1) / kWarps);
+  if (p.D == 128)
+    combine_kernel<128><<<grid, kWarps * 32, 0, s>>>(p);
+  else
+    combine_kernel<64><<<grid, kWarps * 32, 0, s>>>(p);
   return cudaGetLastError();
 }
 

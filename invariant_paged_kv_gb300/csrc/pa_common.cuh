@@ -12,9 +12,18 @@
 
 namespace pa {
 
-// Keys per split of the decode path. A function of nothing: every row's split
-// points are i * kSplit, so they depend only on the row's own key count.
+// Split-KV partition of a row with K keys: ranges of split_len(K) keys,
+// split_len(K) = kSplit * 2^j for the smallest j giving at most kMaxSplits
+// ranges. A function of K alone, so a row's split points never depend on
+// what else is in the step (rows up to 65536 keys use 512-key splits).
 constexpr int kSplit = 512;
+constexpr int kMaxSplits = 128;
+
+__host__ __device__ __forceinline__ int split_len(int keys) {
+  int s = kSplit;
+  while ((keys + s - 1) / s > kMaxSplits) s <<= 1;
+  return s;
+}
 // Keys per pipeline stage of the split kernels (one mma M tile).
 constexpr int kChunk = 16;
 // Bounded waits give up after this many SM clock cycles (about 1 s).
@@ -25,11 +34,16 @@ constexpr long long kWaitCycles = 2000000000LL;
 // ctx_lens, stored in the workspace:
 //   header[0] = number of (row, split) pairs, header[1] = number of full pairs,
 //   header[2] = number of prefill q tiles
+//   (full pairs of rows with longer splits come first, then full 512-key
+//   pairs, then tails: roughly largest first, for the snake-order schedule)
+//   (pair k < header[1] sits at pairs[k]; tail pair k >= header[1] at
+//   pairs[capacity - 1 - (k - header[1])], see pair_slot)
 //   row_info[r] = {first full pair, tail pair or -1, number of splits, lane or -1}
 //   pairs[k]    = {row, split index, lane, key count of the row}
 //   ptiles[i]   = {lane, 128-row tile index, position of its last row, 0},
 //                 heaviest first (tensor-core prefill path)
 // Full pairs (exactly kSplit keys) come first, lane-major; tail pairs after.
+// row_info.y holds the tail pair's slot itself.
 // Partial results of pair k: ml[k * H + h] = {m (log2 domain), l},
 // acc[(k * H + h) * D + d].
 // ---------------------------------------------------------------------------
@@ -44,6 +58,12 @@ struct SplitPlan {
   int capacity;        // pairs the workspace holds
   int ptile_capacity;  // prefill tiles the workspace holds
 };
+
+// Slot of the k-th pair in work order: full pairs from the front of the
+// list, tail pairs from its back.
+__device__ __forceinline__ int pair_slot(const SplitPlan& pl, int k, int nfull) {
+  return k < nfull ? k : pl.capacity - 1 - (k - nfull);
+}
 
 // Query rows per tile of the tensor-core prefill path.
 constexpr int kPrefillRows = 128;

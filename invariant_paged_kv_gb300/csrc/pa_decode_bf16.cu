@@ -2,7 +2,8 @@
 // kernel contract in "P3: native paged-KV continuous-batching sampler", Design,
 // paged.py: fixed KV split per context length, no atomics).
 //
-// Work item = (row, split, kv head). One warp owns an item: it streams the
+// Work item = (row, split, kv head); splits follow split_len (512 keys for
+// rows up to 8192 keys, longer for longer rows). One warp owns an item: it streams the
 // split's keys in 16-key chunks through a private 3-stage ring of swizzled
 // shared-memory tiles filled by TMA (one 64-element box per half row), and
 // computes, for the g = H / Hkv query heads that read this kv head,
@@ -48,28 +49,40 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int tok, int c16) {
 }
 
 struct Item {
-  int pair, kvh, row, lane, keys, t0, len, nchunks;
+  int pair, kvh, row, lane, keys, t0, len, nchunks, single;
 };
 
-__device__ __forceinline__ Item load_item(const StepParams& p, long long item) {
+// k-th item of warp gw among nw warps: passes over the item list alternate
+// direction (snake order), so with items sorted by size every warp gets a
+// near-equal share of the work. Which warp runs an item never changes its
+// arithmetic.
+__device__ __forceinline__ long long item_at(long long k, long long gw, long long nw) {
+  return k * nw + ((k & 1) ? (nw - 1 - gw) : gw);
+}
+
+__device__ __forceinline__ Item load_item(const StepParams& p, long long item, int nfull) {
   Item it;
-  it.pair = (int)(item / p.Hkv);
-  it.kvh = (int)(item - (long long)it.pair * p.Hkv);
+  const int k = (int)(item / p.Hkv);
+  it.kvh = (int)(item - (long long)k * p.Hkv);
+  it.pair = pair_slot(p.plan, k, nfull);
   const int4 pr = p.plan.pairs[it.pair];
   it.row = pr.x;
   it.lane = pr.z;
   it.keys = pr.w;
-  it.t0 = pr.y * kSplit;
-  it.len = min(kSplit, it.keys - it.t0);
+  const int sl = split_len(it.keys);
+  it.t0 = pr.y * sl;
+  it.len = min(sl, it.keys - it.t0);
   it.nchunks = (it.len + kChunk - 1) / kChunk;
+  it.single = it.keys <= sl;
   return it;
 }
 
-// Block ids of the item's range: lane i holds entry i (kSplit / bs <= 32).
-__device__ __forceinline__ int load_blocks(const StepParams& p, const Item& it, int lane) {
+// Block ids w0 .. w0 + 31 of the item's range (relative to its first block):
+// lane i holds entry w0 + i.
+__device__ __forceinline__ int load_blocks(const StepParams& p, const Item& it, int w0, int lane) {
   const int nblk = (it.len + p.bs - 1) / p.bs;
-  if (lane >= nblk) return 0;
-  return p.block_tables[(size_t)it.lane * p.max_blocks + it.t0 / p.bs + lane];
+  if (w0 + lane >= nblk) return 0;
+  return p.block_tables[(size_t)it.lane * p.max_blocks + it.t0 / p.bs + w0 + lane];
 }
 
 template <int D, int NT>
@@ -99,24 +112,30 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 
   const int g = p.H / p.Hkv;
   const long long n_items = (long long)p.plan.header[0] * p.Hkv;
+  const int nfull = p.plan.header[1];
   const long long gw = (long long)blockIdx.x * kWarps + warp;
   const long long nw = (long long)gridDim.x * kWarps;
 
   // ---- producer cursor: runs up to kStages chunks ahead of the consumer ----
-  long long p_item = gw;
-  int p_chunk = 0;
+  long long p_k = 0;
+  long long p_item = item_at(0, gw, nw);
+  int p_chunk = 0, p_w0 = 0;
   Item pi;
   int p_blk = 0;
   if (p_item < n_items) {
-    pi = load_item(p, p_item);
-    p_blk = load_blocks(p, pi, lane);
+    pi = load_item(p, p_item, nfull);
+    p_blk = load_blocks(p, pi, 0, lane);
   }
   uint32_t issued = 0;
   auto produce = [&]() {
     if (p_item >= n_items) return;
     const int stage = issued % kStages;
     const int off = p_chunk * kChunk;  // key offset inside the split
-    int blk = __shfl_sync(0xffffffffu, p_blk, off / p.bs);
+    if (off / p.bs - p_w0 >= 32) {     // next window of block ids
+      p_w0 += 32;
+      p_blk = load_blocks(p, pi, p_w0, lane);
+    }
+    int blk = __shfl_sync(0xffffffffu, p_blk, off / p.bs - p_w0);
     if (lane == 0) {
       if (blk < 0 || blk >= p.NB) {
         raise_flag(p.status, PA_FLAG_BLOCK_RANGE);
@@ -135,10 +154,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     ++issued;
     if (++p_chunk == pi.nchunks) {
       p_chunk = 0;
-      p_item += nw;
+      p_w0 = 0;
+      p_item = item_at(++p_k, gw, nw);
       if (p_item < n_items) {
-        pi = load_item(p, p_item);
-        p_blk = load_blocks(p, pi, lane);
+        pi = load_item(p, p_item, nfull);
+        p_blk = load_blocks(p, pi, 0, lane);
       }
     }
   };
@@ -149,8 +169,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(p.q);
 
 #pragma unroll 1
-  for (long long c_item = gw; c_item < n_items; c_item += nw) {
-    const Item it = load_item(p, c_item);
+  for (long long c_k = 0;; ++c_k) {
+    const long long c_item = item_at(c_k, gw, nw);
+    if (c_item >= n_items) break;
+    const Item it = load_item(p, c_item, nfull);
 
     // q fragments (B operand of S^T = K Q^T): k = dims, n = heads of the group
     uint32_t qf[NT][KS][2];
@@ -293,7 +315,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         l[nt][e] = v;
       }
     }
-    const bool single = it.keys <= kSplit;
+    const bool single = it.single;
     const size_t head0 = (size_t)it.row * p.H + (size_t)it.kvh * g;  // first head of the group
     if (single) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);

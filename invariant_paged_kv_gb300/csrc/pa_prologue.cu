@@ -10,22 +10,16 @@
 // vectors and never converts.
 //
 // Split plan: every row on the split path attends keys 0..position and is cut
-// into ranges [kSplit * i, kSplit * (i + 1)) -- a function of its own key
-// count only ("Numerics envelopes", The hierarchy, invariance.batch: no split
-// count that scales with batch or occupancy). The plan lists one pair
-// (row, split) per range, full ranges first.
+// into ranges [S i, S (i + 1)) with S = split_len(its key count) -- a function
+// of its own key count only ("Numerics envelopes", The hierarchy,
+// invariance.batch: no split count that scales with batch or occupancy). The plan lists one pair
+// (row, split) per range: full ranges from the front of the list (longer
+// splits first), tail ranges from its back.
 #include "pa_common.cuh"
 
 namespace pa {
 
 namespace {
-
-// Sum over k = 0..n of floor(k / kSplit), for n >= -1.
-__device__ __forceinline__ long long floor_sum(long long n) {
-  if (n < 0) return 0;
-  const long long t = n / kSplit, r = n % kSplit;
-  return kSplit * t * (t - 1) / 2 + t * (r + 1);
-}
 
 // Validates lane b (raising status flags when `report`) and returns whether
 // it is well formed; q, c, cu0 are its q_len, ctx_len and first row.
@@ -47,98 +41,143 @@ __device__ bool lane_valid(const StepParams& p, int b, bool report, int& q, int&
   return bad == 0;
 }
 
-// Lane b's contribution to the split plan: the number of full and tail split
-// ranges over its rows (zero when the lane is not on the split path).
-__device__ bool lane_plan(const StepParams& p, int b, bool report, int& q, int& c, int& cu0,
-                          long long& nfull, long long& ntail) {
-  nfull = ntail = 0;
-  if (!lane_valid(p, b, report, q, c, cu0)) return false;
-  const bool on_split = q >= 1 && (p.split_all_rows || q == 1);
-  if (!on_split) return false;
-  // rows attend k = c - q + 1 .. c keys
-  nfull = floor_sum(c) - floor_sum((long long)c - q);
-  ntail = q - ((long long)c / kSplit - ((long long)c - q) / kSplit);
-  return true;
-}
-
-// Exclusive block-wide scan of two counters; returns the block totals.
-__device__ void block_scan2(long long a, long long b, long long& ea, long long& eb,
-                            long long& ta, long long& tb) {
-  __shared__ long long sa[32], sb[32];
+// Exclusive block-wide scan of four counters; returns the block totals.
+__device__ void block_scan4(const long long (&v)[4], long long (&ex)[4], long long (&tot)[4]) {
+  __shared__ long long sm[4][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  long long ia = a, ib = b;  // inclusive within the warp
+  long long inc[4] = {v[0], v[1], v[2], v[3]};  // inclusive within the warp
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
-    const long long xa = __shfl_up_sync(0xffffffffu, ia, o);
-    const long long xb = __shfl_up_sync(0xffffffffu, ib, o);
-    if (lane >= o) {
-      ia += xa;
-      ib += xb;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) {
+      const long long x = __shfl_up_sync(0xffffffffu, inc[k], o);
+      if (lane >= o) inc[k] += x;
     }
   }
   if (lane == 31) {
-    sa[warp] = ia;
-    sb[warp] = ib;
+#pragma unroll
+    for (int k = 0; k < 4; ++k) sm[k][warp] = inc[k];
   }
   __syncthreads();
   if (warp == 0) {
-    long long va = lane < nw ? sa[lane] : 0, vb = lane < nw ? sb[lane] : 0;
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const long long xa = __shfl_up_sync(0xffffffffu, va, o);
-      const long long xb = __shfl_up_sync(0xffffffffu, vb, o);
-      if (lane >= o) {
-        va += xa;
-        vb += xb;
+    for (int k = 0; k < 4; ++k) {
+      long long x = lane < nw ? sm[k][lane] : 0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const long long y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
       }
-    }
-    if (lane < nw) {
-      sa[lane] = va;  // inclusive over warps
-      sb[lane] = vb;
+      if (lane < nw) sm[k][lane] = x;  // inclusive over warps
     }
   }
   __syncthreads();
-  const long long wa = warp ? sa[warp - 1] : 0, wb = warp ? sb[warp - 1] : 0;
-  ea = wa + ia - a;
-  eb = wb + ib - b;
-  ta = sa[nw - 1];
-  tb = sb[nw - 1];
+#pragma unroll
+  for (int k = 0; k < 4; ++k) {
+    ex[k] = (warp ? sm[k][warp - 1] : 0) + inc[k] - v[k];
+    tot[k] = sm[k][nw - 1];
+  }
   __syncthreads();
 }
 
-// Tensor-core prefill tiles: 128-row tiles of every lane with q_len >= 2
-// (when those lanes do not take the split path), ordered heaviest first (by
-// the position of the tile's last row; ties by list order) when there are at
-// most 1024 of them. The order only decides which CTA runs a tile first.
-__device__ void build_prefill_tiles(const StepParams& p) {
+// Two passes over the lanes (blockDim at a time); each lane's data is read
+// once per pass. Pass 1 counts full split pairs of rows with splits longer
+// than kSplit ("long"), full kSplit pairs ("short"), tail pairs and prefill
+// tiles. Pass 2 scans the same counts and writes: long full pairs from the
+// front of the list, short full pairs after all long ones, tail pairs from
+// the back of the list, prefill tiles to a scratch list. Totals are checked
+// against the workspace; on overflow nothing runs.
+__device__ bool lane_counts(const StepParams& p, int b, bool report, int& q, int& c, int& cu0,
+                            long long (&cnt)[4], bool& split, bool& tiles) {
+  cnt[0] = cnt[1] = cnt[2] = cnt[3] = 0;
+  split = tiles = false;
+  if (!lane_valid(p, b, report, q, c, cu0)) return false;
+  split = q >= 1 && (p.split_all_rows || q == 1);
+  tiles = !p.split_all_rows && q >= 2;
+  if (split) {  // row j attends c - q + j + 1 keys
+    for (int j = 0; j < q; ++j) {
+      const int keys = c - q + j + 1;
+      const int sl = split_len(keys);
+      cnt[sl > kSplit ? 0 : 1] += keys / sl;
+      cnt[2] += (keys % sl) != 0;
+    }
+  }
+  if (tiles) cnt[3] = (q + kPrefillRows - 1) / kPrefillRows;
+  return true;
+}
+
+__device__ void build_plan(const StepParams& p) {
   __shared__ int s_work[1024];
   const int tid = threadIdx.x, nth = blockDim.x;
   const SplitPlan& pl = p.plan;
-  long long total = 0;
-  if (!p.split_all_rows) {
+  for (int r = tid; r < p.T; r += nth) pl.row_info[r] = make_int4(0, -1, 0, -1);
+
+  long long total[4] = {0, 0, 0, 0};
+  for (int base = 0; base < p.B; base += nth) {
+    const int b = base + tid;
+    int q, c, cu0;
+    long long cnt[4] = {0, 0, 0, 0};
+    bool split, tiles;
+    if (b < p.B) lane_counts(p, b, true, q, c, cu0, cnt, split, tiles);
+    long long ex[4], tot[4];
+    block_scan4(cnt, ex, tot);
+#pragma unroll
+    for (int k = 0; k < 4; ++k) total[k] += tot[k];
+  }
+  const int cap = pl.capacity;
+  const long long nfull = total[0] + total[1];
+  const bool overflow = nfull + total[2] > cap || total[3] > pl.ptile_capacity;
+  if (overflow && tid == 0) raise_flag(p.status, PA_FLAG_WORKSPACE);
+  __syncthreads();
+
+  if (!overflow) {
+    long long carry[4] = {0, 0, 0, 0};
     for (int base = 0; base < p.B; base += nth) {
       const int b = base + tid;
       int q = 0, c = 0, cu0 = 0;
-      long long nt = 0;
-      if (b < p.B && lane_valid(p, b, false, q, c, cu0) && q >= 2)
-        nt = (q + kPrefillRows - 1) / kPrefillRows;
-      long long e0, e1, t0, t1;
-      block_scan2(nt, 0, e0, e1, t0, t1);
-      if (nt > 0 && total + e0 + nt <= pl.ptile_capacity) {
-        for (int t = 0; t < nt; ++t) {
-          const int last = min(q, (t + 1) * kPrefillRows) - 1;
-          pl.ptiles_tmp[total + e0 + t] = make_int4(b, t, c - q + last, 0);
+      long long cnt[4] = {0, 0, 0, 0};
+      bool split = false, tiles = false;
+      if (b < p.B) lane_counts(p, b, false, q, c, cu0, cnt, split, tiles);
+      long long ex[4], tot[4];
+      block_scan4(cnt, ex, tot);
+      if (split) {
+        long long lb = carry[0] + ex[0];             // long full pairs
+        long long sb = total[0] + carry[1] + ex[1];  // short full pairs
+        long long tb = carry[2] + ex[2];             // tail pair k sits at cap - 1 - k
+        for (int j = 0; j < q; ++j) {
+          const int keys = c - q + j + 1;
+          const int sl = split_len(keys);
+          const int nf = keys / sl;
+          const bool has_tail = (keys % sl) != 0;
+          const int row = cu0 + j;
+          long long& fb = sl > kSplit ? lb : sb;
+          const long long tslot = cap - 1 - tb;
+          pl.row_info[row] =
+              make_int4((int)fb, has_tail ? (int)tslot : -1, nf + (has_tail ? 1 : 0), b);
+          for (int i = 0; i < nf; ++i) pl.pairs[fb + i] = make_int4(row, i, b, keys);
+          fb += nf;
+          if (has_tail) {
+            pl.pairs[tslot] = make_int4(row, nf, b, keys);
+            ++tb;
+          }
         }
       }
-      total += t0;
+      if (tiles) {
+        const long long t0 = carry[3] + ex[3];
+        for (int t = 0; t < cnt[3]; ++t) {
+          const int last = min(q, (t + 1) * kPrefillRows) - 1;
+          pl.ptiles_tmp[t0 + t] = make_int4(b, t, c - q + last, 0);
+        }
+      }
+#pragma unroll
+      for (int k = 0; k < 4; ++k) carry[k] += tot[k];
     }
   }
-  if (total > pl.ptile_capacity) {
-    if (tid == 0) raise_flag(p.status, PA_FLAG_WORKSPACE);
-    total = 0;
-  }
+  const int n = overflow ? 0 : (int)total[3];
   __syncthreads();
-  const int n = (int)total;
+  // prefill tiles heaviest first (position of the tile's last row; ties by
+  // list order) when there are at most blockDim of them: the order only
+  // decides which CTA takes a tile first
   if (n <= nth) {
     if (tid < n) s_work[tid] = pl.ptiles_tmp[tid].z;
     __syncthreads();
@@ -154,69 +193,11 @@ __device__ void build_prefill_tiles(const StepParams& p) {
   } else {
     for (int i = tid; i < n; i += nth) pl.ptiles[i] = pl.ptiles_tmp[i];
   }
-  if (tid == 0) pl.header[2] = n;
-}
-
-__device__ void build_plan(const StepParams& p) {
-  const int tid = threadIdx.x, nth = blockDim.x;
-  const SplitPlan& pl = p.plan;
-  for (int r = tid; r < p.T; r += nth) pl.row_info[r] = make_int4(0, -1, 0, -1);
-
-  long long tot_full = 0, tot_tail = 0;
-  for (int base = 0; base < p.B; base += nth) {
-    const int b = base + tid;
-    int q, c, cu0;
-    long long f = 0, t = 0;
-    if (b < p.B) lane_plan(p, b, true, q, c, cu0, f, t);
-    long long ef, et, tf, tt;
-    block_scan2(f, t, ef, et, tf, tt);
-    tot_full += tf;
-    tot_tail += tt;
-  }
-  __syncthreads();
-  if (tot_full + tot_tail > pl.capacity) {
-    if (tid == 0) {
-      raise_flag(p.status, PA_FLAG_WORKSPACE);
-      pl.header[0] = 0;
-      pl.header[1] = 0;
-    }
-    build_prefill_tiles(p);
-    return;
-  }
-  long long carry_full = 0, carry_tail = 0;
-  for (int base = 0; base < p.B; base += nth) {
-    const int b = base + tid;
-    int q = 0, c = 0, cu0 = 0;
-    long long f = 0, t = 0;
-    bool on = false;
-    if (b < p.B) on = lane_plan(p, b, false, q, c, cu0, f, t);
-    long long ef, et, tf, tt;
-    block_scan2(f, t, ef, et, tf, tt);
-    if (on) {
-      long long fb = carry_full + ef;
-      long long tb = tot_full + carry_tail + et;
-      for (int j = 0; j < q; ++j) {
-        const int keys = c - q + j + 1;
-        const int nf = keys / kSplit;
-        const bool has_tail = (keys % kSplit) != 0;
-        const int row = cu0 + j;
-        pl.row_info[row] = make_int4((int)fb, has_tail ? (int)tb : -1, nf + (has_tail ? 1 : 0), b);
-        for (int i = 0; i < nf; ++i) pl.pairs[fb + i] = make_int4(row, i, b, keys);
-        fb += nf;
-        if (has_tail) {
-          pl.pairs[tb] = make_int4(row, nf, b, keys);
-          ++tb;
-        }
-      }
-    }
-    carry_full += tf;
-    carry_tail += tt;
-  }
   if (tid == 0) {
-    pl.header[0] = (int)(tot_full + tot_tail);
-    pl.header[1] = (int)tot_full;
+    pl.header[0] = overflow ? 0 : (int)(nfull + total[2]);
+    pl.header[1] = overflow ? 0 : (int)nfull;
+    pl.header[2] = n;
   }
-  build_prefill_tiles(p);
 }
 
 __device__ void write_rows(const StepParams& p, int cta, int ncta) {

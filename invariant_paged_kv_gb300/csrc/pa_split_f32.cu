@@ -2,7 +2,7 @@
 // which "Numerics envelopes", The hierarchy, kernels.deterministic rules out).
 //
 // Same work decomposition as the bf16 decode kernel -- item = (row, split,
-// kv head), one warp per item, splits of kSplit keys -- but every row of the
+// kv head), one warp per item, the same split points -- but every row of the
 // step takes this path, prefill rows included. Lanes of the warp own D / 32
 // dims each; per key the g scores are full-warp butterfly sums (every lane
 // ends with the same bits), then the running max, the rescale and the
@@ -21,6 +21,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_f32_kernel(const StepParams
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.H / p.Hkv;
   const long long n_items = (long long)p.plan.header[0] * p.Hkv;
+  const int nfull = p.plan.header[1];
   const long long nw = (long long)gridDim.x * kWarps;
   const float* qg = static_cast<const float*>(p.q);
   const float* kc = static_cast<const float*>(p.k_cache);
@@ -28,12 +29,14 @@ __global__ void __launch_bounds__(kWarps * 32) split_f32_kernel(const StepParams
 
 #pragma unroll 1
   for (long long item = (long long)blockIdx.x * kWarps + warp; item < n_items; item += nw) {
-    const int pair = (int)(item / p.Hkv);
-    const int kvh = (int)(item - (long long)pair * p.Hkv);
+    const int k = (int)(item / p.Hkv);
+    const int kvh = (int)(item - (long long)k * p.Hkv);
+    const int pair = pair_slot(p.plan, k, nfull);
     const int4 pr = p.plan.pairs[pair];
     const int row = pr.x, lane_b = pr.z, keys = pr.w;
-    const int t0 = pr.y * kSplit;
-    const int t1 = min(t0 + kSplit, keys);
+    const int sl = split_len(keys);
+    const int t0 = pr.y * sl;
+    const int t1 = min(t0 + sl, keys);
     const size_t head0 = (size_t)row * p.H + (size_t)kvh * g;
 
     float qv[GMAX][DPL], acc[GMAX][DPL], m[GMAX], l[GMAX];
@@ -81,7 +84,7 @@ __global__ void __launch_bounds__(kWarps * 32) split_f32_kernel(const StepParams
       }
     }
     float* out = static_cast<float*>(p.out);
-    const bool single = keys <= kSplit;
+    const bool single = keys <= sl;
     const size_t ph0 = (size_t)pair * p.H + (size_t)kvh * g;
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) {

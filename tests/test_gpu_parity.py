@@ -112,8 +112,9 @@ def _ragged(geom, q_lens, ctx, seed, pool_extra=1.3):
 def test_ragged_edges(dtype, D, bs):
     """ctx = 1, ctx on and off split / chunk / block edges, empty lanes, prefill chunks."""
     geom = wl.Geometry(8, 2, D, bs, dtype)
-    ctx = [1, 15, 16, 17, 511, 512, 513, 1024, 1500, 2049, 7, 40, 600]
-    q = [1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 0, 9, 23]
+    # 65536 / 65537 keys: 512- and 1024-key splits
+    ctx = [1, 15, 16, 17, 511, 512, 513, 1024, 1500, 2049, 7, 40, 600, 12000, 65536, 65537]
+    q = [1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 0, 9, 23, 1, 1, 1]
     step = _ragged(geom, q, ctx, 7)
     _check_step(step, 77)
 
