@@ -153,6 +153,8 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
  * recorded on `stream` in this order, as far as n_events reaches: [0] before
  * the first launch, [1] after the write + plan prologue, [2] after the
  * decode split kernel, [3] after the prefill kernel, [4] after the combine.
+ * When `stream` is being captured into a CUDA graph the events become
+ * event-record nodes of the graph (recorded at each replay).
  * The work done is identical to pa_attention.
  */
 pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* v_cache,

@@ -177,10 +177,17 @@ bool encode_q_map(CUtensorMap* map, const void* q, int T, int H, int D) {
   return r == CUDA_SUCCESS;
 }
 
+// Record a phase event. Under stream capture it becomes an event-record node
+// of the graph (recorded at every replay) rather than a capture dependency.
 pa_status record(void* const* events, int32_t n_events, int idx, cudaStream_t s) {
   if (events && idx < n_events && events[idx]) {
-    if (cudaEventRecord(static_cast<cudaEvent_t>(events[idx]), s) != cudaSuccess)
-      return PA_ERR_CUDA;
+    cudaStreamCaptureStatus cs = cudaStreamCaptureStatusNone;
+    if (cudaStreamIsCapturing(s, &cs) != cudaSuccess) return PA_ERR_CUDA;
+    const cudaEvent_t ev = static_cast<cudaEvent_t>(events[idx]);
+    const cudaError_t e = cs == cudaStreamCaptureStatusActive
+                              ? cudaEventRecordWithFlags(ev, s, cudaEventRecordExternal)
+                              : cudaEventRecord(ev, s);
+    if (e != cudaSuccess) return PA_ERR_CUDA;
   }
   return PA_OK;
 }

@@ -90,6 +90,20 @@ struct StepParams {
   SplitPlan plan;
 };
 
+// Opt a kernel in to `bytes` of dynamic shared memory once per device (the
+// attribute is per device and sticky; later calls only read a flag).
+template <typename Kernel>
+inline cudaError_t smem_opt_in(Kernel kern, int bytes, unsigned long long* done_mask) {
+  int dev = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e != cudaSuccess) return e;
+  const unsigned long long bit = dev < 64 ? (1ull << dev) : 0ull;
+  if (bit && (__atomic_load_n(done_mask, __ATOMIC_ACQUIRE) & bit)) return cudaSuccess;
+  e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, bytes);
+  if (e == cudaSuccess && bit) __atomic_fetch_or(done_mask, bit, __ATOMIC_RELEASE);
+  return e;
+}
+
 __device__ __forceinline__ void raise_flag(int* status, int bits) {
   if (status) atomicOr(status, bits);
 }

@@ -364,8 +364,8 @@ template <int D, int NT>
 cudaError_t launch_t(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v, int grid,
                      cudaStream_t s) {
   auto kern = decode_bf16_kernel<D, NT>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       Tile<D>::kSmemBytes);
+  static unsigned long long done = 0;
+  cudaError_t e = smem_opt_in(kern, Tile<D>::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
   kern<<<grid, kWarps * 32, Tile<D>::kSmemBytes, s>>>(p, k, v);
   return cudaGetLastError();

@@ -443,8 +443,8 @@ template <int D>
 cudaError_t launch_d(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
                      const CUtensorMap& v, int grid, cudaStream_t s) {
   auto kern = prefill_tc_kernel<D>;
-  cudaError_t e = cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                       PfLayout<D>::kSmemBytes);
+  static unsigned long long done = 0;
+  cudaError_t e = smem_opt_in(kern, PfLayout<D>::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
   kern<<<grid, kThreads, PfLayout<D>::kSmemBytes, s>>>(p, q, k, v);
   return cudaGetLastError();
