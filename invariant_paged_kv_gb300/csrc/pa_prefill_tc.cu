@@ -26,9 +26,9 @@
 // computed while the softmax works on tile f and P V of tile f - 1 runs; the
 // tensor core also alternates between the two heads. TMEM (512 columns):
 // S/P buffers 0 and 1 and O of head A, then the same for head B. Every wait
-// is bounded (timeout -> PA_FLAG_TIMEOUT). Every waiter of an mbarrier waits
-// on each of its phases in order, so a parity wait never meets a barrier more
-// than one phase away from the awaited one (ahead or behind).
+// is bounded (timeout -> PA_FLAG_TIMEOUT). No parity wait ever meets a barrier
+// more than one phase away from the awaited one, ahead or behind (see the P V
+// barriers, which alternate by tile parity for that reason).
 #include "pa_tcgen05.cuh"
 
 namespace pa {
@@ -61,7 +61,7 @@ struct PfLayout {
 
 struct Bars {
   uint64_t q, kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
-  uint64_t s[2][2], p[2][2], o[2];  // s, p: [head][buffer]; o: [head]
+  uint64_t s[2][2], p[2][2], o[2][2];  // [head][buffer / tile parity]
 };
 
 struct ItemInfo {
@@ -151,7 +151,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         mbar_init(smem_u32(&bars.s[h][b]), 1);
         mbar_init(smem_u32(&bars.p[h][b]), kRows);
       }
-      mbar_init(smem_u32(&bars.o[h]), 1);
+      mbar_init(smem_u32(&bars.o[h][0]), 1);
+      mbar_init(smem_u32(&bars.o[h][1]), 1);
     }
     s_abort = 0;
     fence_mbar_init();
@@ -171,7 +172,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   auto tO = [&](int h) -> uint32_t { return tmem + 256 * h + 128; };
   auto bS = [&](int h, uint32_t b) -> uint32_t { return smem_u32(&bars.s[h][b]); };
   auto bP = [&](int h, uint32_t b) -> uint32_t { return smem_u32(&bars.p[h][b]); };
-  auto bO = [&](int h) -> uint32_t { return smem_u32(&bars.o[h]); };
+  // P V of tile t completes on o[head][t & 1]
+  auto bO = [&](int h, uint32_t t) -> uint32_t { return smem_u32(&bars.o[h][t & 1]); };
 
   const int g = p.H / p.Hkv;
   const int n_items = p.plan.header[2] * p.Hkv * ((g + 1) / 2);
@@ -264,7 +266,7 @@ __global__ void __launch_bounds__(kThreads, 1)
               umma_bf16_tmem_a(tO(hb), tS(hb, th & 1) + k * 8, bd, idPV,
                                (j > 0 || k > 0) ? 1u : 0u);
             }
-            umma_commit(bO(hb));
+            umma_commit(bO(hb, th));
           }
           __syncwarp();
         }
@@ -278,7 +280,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hb = 0; hb < nh; ++hb) {
           const uint32_t th = n_t[hb] + kt;
           // buffer th & 1 last held P of tile kt - 2: its P V must be done
-          if (kt >= 2 && !wait_or_abort(bO(hb), (th - 2) & 1, &s_abort, p.status)) {
+          if (kt >= 2 && !wait_or_abort(bO(hb, th - 2), ((th - 2) >> 1) & 1, &s_abort, p.status)) {
             ok = false;
             break;
           }
@@ -373,15 +375,18 @@ __global__ void __launch_bounds__(kThreads, 1)
         tmem_st16(tSr + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
         tmem_wait_st();
         l = fmaf(l, alpha, rs);
-        // P V of the previous tile must be done before O is rescaled. The wait
-        // is taken on every tile, not only when rescaling: a parity wait is
-        // only sound when the barrier's last completed phase is at most one
-        // behind the awaited one, so no phase of this barrier may be skipped.
-        if (kt > 0) {
-          if (!wait_or_abort(bO(hb), (th - 1) & 1, &s_abort, p.status)) { ok = false; break; }
-          tc_fence_after();
-        }
+        // P V of the previous tile must be done before O is rescaled. P V
+        // completions alternate between two barriers by tile parity, so a
+        // barrier is never more than one phase away from any wait on it even
+        // when tiles without a rescale skip the wait (S of this tile was
+        // issued after P V of tile th - 2 finished, and P V of tile th + 1
+        // needs this tile's P).
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
+          if (!wait_or_abort(bO(hb, th - 1), ((th - 1) >> 1) & 1, &s_abort, p.status)) {
+            ok = false;
+            break;
+          }
+          tc_fence_after();
 #pragma unroll 1
           for (int c = 0; c < D / 32; ++c) {
             uint32_t ov[32];
@@ -396,7 +401,8 @@ __global__ void __launch_bounds__(kThreads, 1)
         tc_fence_before();
         mbar_arrive(bP(hb, b));
       }
-      if (ok && wait_or_abort(bO(hb), (n_t[hb] + it.nkt - 1) & 1, &s_abort, p.status)) {
+      const uint32_t last = n_t[hb] + it.nkt - 1;
+      if (ok && wait_or_abort(bO(hb, last), (last >> 1) & 1, &s_abort, p.status)) {
         tc_fence_after();
         const bool valid = r < it.nrows;
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
