@@ -58,6 +58,8 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--mode", choices=["batch", "row"], default="batch",
+                    help="invariance mode: 'row' sends prefill rows down the split path too")
     return ap.parse_args()
 
 
@@ -99,6 +101,7 @@ def workload_config(step, layers, name, args):
         "l2": "no flush: each layer's keys exceed the 129 MB L2",
         "small": bool(args.small),
         "cuda_graph": not getattr(args, "no_graph", True),
+        "invariance_mode": getattr(args, "mode", "batch"),
     }
 
 
@@ -323,7 +326,7 @@ def run_ours(args, rank, world, local_rank):
     outs = [torch.empty_like(q) for q in tens["q"]]
     ws = torch.empty(pa.workspace_bytes(step.B, step.T, step.max_q_len, step.max_ctx_len,
                                         int(step.ctx_lens.sum()), g.H, g.Hkv, g.D,
-                                        g.block_size, tens["q"][0].dtype),
+                                        g.block_size, tens["q"][0].dtype, mode=args.mode),
                      dtype=torch.uint8, device=dev)
     status = pa.new_status(dev)
     scale = 1.0 / math.sqrt(g.D)
@@ -338,7 +341,8 @@ def run_ours(args, rank, world, local_rank):
                          max_q_len=step.max_q_len, max_ctx_len=step.max_ctx_len, scale=scale,
                          workspace=ws, slot_mapping=dslots if dslots is not None else slots,
                          k_new=(kn or tens["k_new"])[l], v_new=(vn or tens["v_new"])[l],
-                         status=status, events=None if events is None else events[l])
+                         status=status, events=None if events is None else events[l],
+                         mode=args.mode)
 
     def barrier():
         if world > 1:

@@ -59,6 +59,28 @@ typedef enum {
 
 typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
 
+/*
+ * Invariance modes of pa_attention_ex.
+ *   PA_MODE_BATCH_INVARIANT  a row's output bits depend only on its own lane
+ *                            (q, keys, ctx_len, q_len), never on the other
+ *                            lanes of the step. Decode rows (q_len == 1) take
+ *                            the split-KV path; bf16 lanes with q_len >= 2
+ *                            take the tensor-core prefill path.
+ *   PA_MODE_ROW_INVARIANT    additionally independent of the row's own
+ *                            lane's q_len: every row, decode or prefill, takes
+ *                            the split-KV path with the split partition of
+ *                            its own key count (position + 1), so a row has
+ *                            the same bits whether it arrives as a decode row,
+ *                            inside a prefill chunk of any length, or again
+ *                            on recompute after a prefix hit at any token
+ *                            ("Numerics envelopes", Prefix hits resume at any
+ *                            token; "P3: native paged-KV continuous-batching
+ *                            sampler", Evidence, batch invariance under
+ *                            chunk sizes 1, 2 and 64). fp32 steps always
+ *                            behave this way.
+ */
+typedef enum { PA_MODE_BATCH_INVARIANT = 0, PA_MODE_ROW_INVARIANT = 1 } pa_mode;
+
 /* Device status word bits. */
 #define PA_FLAG_SLOT_RANGE   0x01  /* slot >= num_blocks * block_size: write skipped      */
 #define PA_FLAG_BLOCK_RANGE  0x02  /* block-table entry outside [0, num_blocks)          */
@@ -105,6 +127,18 @@ size_t pa_attention_workspace_bytes(int32_t B, int32_t T, int32_t max_q_len,
                                     pa_dtype dtype);
 
 /*
+ * pa_attention_workspace_bytes_ex -- the same for an invariance mode
+ * (pa_attention_workspace_bytes is this with PA_MODE_BATCH_INVARIANT). In
+ * PA_MODE_ROW_INVARIANT every row holds split partials, so the bound is
+ * T * ceil(max_ctx_len / 512) (row, split) pairs. Returns 0 for unsupported
+ * arguments or an unknown mode.
+ */
+size_t pa_attention_workspace_bytes_ex(int32_t B, int32_t T, int32_t max_q_len,
+                                       int32_t max_ctx_len, int64_t total_ctx, int32_t H,
+                                       int32_t Hkv, int32_t D, int32_t block_size,
+                                       pa_dtype dtype, pa_mode mode);
+
+/*
  * pa_attention -- attention of one flat ragged step.
  * ("P3: native paged-KV continuous-batching sampler", Design, paged.py: the
  *  PagedAttention protocol -- write new K/V, return [T, H, D] -- and the
@@ -148,25 +182,29 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
                        size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
- * pa_attention_profiled -- pa_attention plus phase timing hooks.
- * events: array of n_events cudaEvent_t handles (may be NULL / 0). They are
- * recorded on `stream` in this order, as far as n_events reaches: [0] before
- * the first launch, [1] after the write + plan prologue, [2] after the
- * decode split kernel, [3] after the prefill kernel, [4] after the combine.
- * When `stream` is being captured into a CUDA graph the events become
- * event-record nodes of the graph (recorded at each replay).
- * The work done is identical to pa_attention.
+ * pa_attention_ex -- pa_attention with an invariance mode and phase timing
+ * hooks (pa_attention is this with PA_MODE_BATCH_INVARIANT and no events).
+ *   mode      see pa_mode; an unknown value returns PA_ERR_INVALID_ARG. The
+ *             workspace must hold what pa_attention_workspace_bytes_ex
+ *             returns for the same mode.
+ *   events    array of n_events cudaEvent_t handles (may be NULL / 0). They
+ *             are recorded on `stream` in this order, as far as n_events
+ *             reaches: [0] before the first launch, [1] after the write +
+ *             plan prologue, [2] after the split kernel, [3] after the
+ *             prefill kernel (no launch between [2] and [3] when no row
+ *             takes the prefill path), [4] after the combine. When `stream`
+ *             is being captured into a CUDA graph the events become
+ *             event-record nodes of the graph (recorded at each replay).
  */
-pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* v_cache,
-                                const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
-                                const int64_t* slot_mapping, const void* k_new,
-                                const void* v_new, void* out, int32_t B, int32_t T, int32_t H,
-                                int32_t Hkv, int32_t D, int32_t block_size, int32_t num_blocks,
-                                int32_t max_q_len, int32_t max_ctx_len, float scale,
-                                pa_dtype dtype, void* workspace, size_t workspace_bytes,
-                                int32_t* status, void* stream, void* const* events,
-                                int32_t n_events);
+pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                          const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                          void* out, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t D,
+                          int32_t block_size, int32_t num_blocks, int32_t max_q_len,
+                          int32_t max_ctx_len, float scale, pa_dtype dtype, void* workspace,
+                          size_t workspace_bytes, int32_t* status, void* stream, pa_mode mode,
+                          void* const* events, int32_t n_events);
 
 /*
  * pa_attention_static_scratch -- pa_attention for callers that cannot

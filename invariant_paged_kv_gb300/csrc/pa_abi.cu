@@ -53,12 +53,15 @@ pa_status check_geometry(int32_t H, int32_t Hkv, int32_t D, int32_t block_size, 
   return PA_OK;
 }
 
-// Every row takes the split path for fp32 (CUDA-core FMA, no TF32). For
-// bf16 only decode lanes (q_len == 1) do; lanes with q_len >= 2 go to the
-// tensor-core prefill kernel.
-bool split_all_rows(pa_dtype dtype, int32_t max_q_len) {
-  (void)max_q_len;
-  return dtype == PA_F32;
+// Every row takes the split path for fp32 (CUDA-core FMA, no TF32) and in
+// the row-invariant mode. Otherwise (bf16) only decode lanes (q_len == 1)
+// do; lanes with q_len >= 2 go to the tensor-core prefill kernel.
+bool split_all_rows(pa_dtype dtype, pa_mode mode) {
+  return dtype == PA_F32 || mode == PA_MODE_ROW_INVARIANT;
+}
+
+bool mode_known(pa_mode mode) {
+  return mode == PA_MODE_BATCH_INVARIANT || mode == PA_MODE_ROW_INVARIANT;
 }
 
 // Prefill tiles a step can hold: sum over lanes of ceil(q_len / 128).
@@ -86,10 +89,10 @@ long long ceil_div(long long a, long long b) { return (a + b - 1) / b; }
 
 // Upper bound on (row, split) pairs of a step (split_len(K) >= kSplit, so a
 // row of K keys has at most ceil(K / kSplit) splits).
-long long max_pairs(int32_t B, int32_t T, int32_t max_q_len, int32_t max_ctx_len,
-                    int64_t total_ctx, pa_dtype dtype) {
+long long max_pairs(int32_t B, int32_t T, int32_t max_ctx_len, int64_t total_ctx,
+                    pa_dtype dtype, pa_mode mode) {
   const long long per_row = ceil_div(max_ctx_len > 0 ? max_ctx_len : 1, kSplit);
-  if (split_all_rows(dtype, max_q_len)) return (long long)T * per_row;
+  if (split_all_rows(dtype, mode)) return (long long)T * per_row;
   long long loose = (long long)(B < T ? B : T) * per_row;
   if (total_ctx >= 0) {
     const long long tight = total_ctx / kSplit + B;
@@ -246,28 +249,36 @@ pa_status pa_write_kv(const void* k_new, const void* v_new, void* k_cache, void*
   return PA_OK;
 }
 
+size_t pa_attention_workspace_bytes_ex(int32_t B, int32_t T, int32_t max_q_len,
+                                       int32_t max_ctx_len, int64_t total_ctx, int32_t H,
+                                       int32_t Hkv, int32_t D, int32_t block_size,
+                                       pa_dtype dtype, pa_mode mode) {
+  if (B < 0 || T < 0 || max_q_len < 0 || max_ctx_len < 0 || !mode_known(mode)) return 0;
+  if (check_geometry(H, Hkv, D, block_size, dtype) != PA_OK) return 0;
+  const long long pairs = max_pairs(B, T, max_ctx_len, total_ctx, dtype, mode);
+  return bytes_for_pairs(B, T, H, D, pairs > 0 ? pairs : 1);
+}
+
 size_t pa_attention_workspace_bytes(int32_t B, int32_t T, int32_t max_q_len,
                                     int32_t max_ctx_len, int64_t total_ctx, int32_t H,
                                     int32_t Hkv, int32_t D, int32_t block_size,
                                     pa_dtype dtype) {
-  if (B < 0 || T < 0 || max_q_len < 0 || max_ctx_len < 0) return 0;
-  if (check_geometry(H, Hkv, D, block_size, dtype) != PA_OK) return 0;
-  const long long pairs = max_pairs(B, T, max_q_len, max_ctx_len, total_ctx, dtype);
-  return bytes_for_pairs(B, T, H, D, pairs > 0 ? pairs : 1);
+  return pa_attention_workspace_bytes_ex(B, T, max_q_len, max_ctx_len, total_ctx, H, Hkv, D,
+                                         block_size, dtype, PA_MODE_BATCH_INVARIANT);
 }
 
-pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* v_cache,
-                                const int32_t* block_tables, int32_t max_blocks_per_seq,
-                                const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
-                                const int64_t* slot_mapping, const void* k_new,
-                                const void* v_new, void* out, int32_t B, int32_t T, int32_t H,
-                                int32_t Hkv, int32_t D, int32_t block_size, int32_t num_blocks,
-                                int32_t max_q_len, int32_t max_ctx_len, float scale,
-                                pa_dtype dtype, void* workspace, size_t workspace_bytes,
-                                int32_t* status, void* stream, void* const* events,
-                                int32_t n_events) {
+pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cache,
+                          const int32_t* block_tables, int32_t max_blocks_per_seq,
+                          const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                          const int64_t* slot_mapping, const void* k_new, const void* v_new,
+                          void* out, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t D,
+                          int32_t block_size, int32_t num_blocks, int32_t max_q_len,
+                          int32_t max_ctx_len, float scale, pa_dtype dtype, void* workspace,
+                          size_t workspace_bytes, int32_t* status, void* stream, pa_mode mode,
+                          void* const* events, int32_t n_events) {
   // ---- host validation: nothing below touches CUDA until it all passes ----
-  if (B < 0 || T < 0 || num_blocks <= 0 || max_q_len < 0 || max_ctx_len < 0 || n_events < 0)
+  if (B < 0 || T < 0 || num_blocks <= 0 || max_q_len < 0 || max_ctx_len < 0 || n_events < 0 ||
+      !mode_known(mode))
     return PA_ERR_INVALID_ARG;
   pa_status g = check_geometry(H, Hkv, D, block_size, dtype);
   if (g != PA_OK) return g;
@@ -318,11 +329,11 @@ pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* 
   p.max_q_len = max_q_len;
   p.max_ctx_len = max_ctx_len;
   p.elem_bytes = elem_bytes_of(dtype);
-  p.split_all_rows = split_all_rows(dtype, max_q_len) ? 1 : 0;
+  p.split_all_rows = split_all_rows(dtype, mode) ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
   p.plan = carve(workspace, cap, B, T, H, D);
-  const bool prefill_tc = dtype == PA_BF16 && max_q_len >= 2;
+  const bool prefill_tc = !p.split_all_rows && max_q_len >= 2;
 
   CUtensorMap tmK, tmV, tmQ;
   if (dtype == PA_BF16) {
@@ -331,7 +342,7 @@ pa_status pa_attention_profiled(const void* q, const void* k_cache, const void* 
       return PA_ERR_CUDA;
     if (prefill_tc && !encode_q_map(&tmQ, q, T, H, D)) return PA_ERR_CUDA;
   }
-  long long items = max_pairs(B, T, max_q_len, max_ctx_len, -1, dtype);
+  long long items = max_pairs(B, T, max_ctx_len, -1, dtype, mode);
   if (items > cap) items = cap;
   items *= Hkv;
 
@@ -364,10 +375,10 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
                        int32_t block_size, int32_t num_blocks, int32_t max_q_len,
                        int32_t max_ctx_len, float scale, pa_dtype dtype, void* workspace,
                        size_t workspace_bytes, int32_t* status, void* stream) {
-  return pa_attention_profiled(q, k_cache, v_cache, block_tables, max_blocks_per_seq,
-                               cu_seqlens_q, ctx_lens, slot_mapping, k_new, v_new, out, B, T, H,
-                               Hkv, D, block_size, num_blocks, max_q_len, max_ctx_len, scale,
-                               dtype, workspace, workspace_bytes, status, stream, nullptr, 0);
+  return pa_attention_ex(q, k_cache, v_cache, block_tables, max_blocks_per_seq, cu_seqlens_q,
+                         ctx_lens, slot_mapping, k_new, v_new, out, B, T, H, Hkv, D, block_size,
+                         num_blocks, max_q_len, max_ctx_len, scale, dtype, workspace,
+                         workspace_bytes, status, stream, PA_MODE_BATCH_INVARIANT, nullptr, 0);
 }
 
 pa_status pa_read_status(int32_t* status, void* stream, int32_t* flags_out, int32_t clear) {

@@ -17,6 +17,7 @@ import torch
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libpa.so")
 
 PA_F32, PA_BF16 = 0, 1
+MODES = {"batch": 0, "row": 1}  # pa_mode: PA_MODE_BATCH_INVARIANT, PA_MODE_ROW_INVARIANT
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
                 3: "PA_ERR_WORKSPACE", 4: "PA_ERR_CUDA"}
 FLAGS = {
@@ -24,8 +25,8 @@ FLAGS = {
     "CU_SEQLENS": 0x10, "WORKSPACE": 0x20, "HOST_BOUND": 0x40, "TIMEOUT": 0x80,
 }
 
-EXPORTS = ("pa_write_kv", "pa_attention_workspace_bytes", "pa_attention",
-           "pa_attention_profiled", "pa_read_status", "pa_status_string",
+EXPORTS = ("pa_write_kv", "pa_attention_workspace_bytes", "pa_attention_workspace_bytes_ex",
+           "pa_attention", "pa_attention_ex", "pa_read_status", "pa_status_string",
            "pa_kernel_launches", "pa_split_tokens", "pa_attention_static_scratch")
 
 
@@ -56,12 +57,15 @@ def load() -> ctypes.CDLL:
     L.pa_write_kv.restype = ctypes.c_int
     L.pa_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32, i32, i32]
     L.pa_attention_workspace_bytes.restype = sz
+    L.pa_attention_workspace_bytes_ex.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32, i32,
+                                                  i32, i32]
+    L.pa_attention_workspace_bytes_ex.restype = sz
     att = [vp, vp, vp, vp, i32, vp, vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, i32,
            i32, i32, f32, i32, vp, sz, vp, vp]
     L.pa_attention.argtypes = att
     L.pa_attention.restype = ctypes.c_int
-    L.pa_attention_profiled.argtypes = att + [ctypes.POINTER(vp), i32]
-    L.pa_attention_profiled.restype = ctypes.c_int
+    L.pa_attention_ex.argtypes = att + [i32, ctypes.POINTER(vp), i32]
+    L.pa_attention_ex.restype = ctypes.c_int
     L.pa_read_status.argtypes = [vp, vp, ctypes.POINTER(i32), i32]
     L.pa_read_status.restype = ctypes.c_int
     L.pa_status_string.argtypes = [ctypes.c_int]
@@ -135,21 +139,33 @@ def write_kv(k_new, v_new, k_cache, v_cache, slot_mapping, status=None, stream=N
                               _ptr(status), _stream(stream)), "pa_write_kv")
 
 
+def _mode_code(mode: str) -> int:
+    if mode not in MODES:
+        raise ValueError(f"mode must be one of {sorted(MODES)}")
+    return MODES[mode]
+
+
 def workspace_bytes(B, T, max_q_len, max_ctx_len, total_ctx, H, Hkv, D, block_size,
-                    dtype: torch.dtype) -> int:
+                    dtype: torch.dtype, mode: str = "batch") -> int:
+    """pa_attention_workspace_bytes_ex for ``mode`` ("batch" or "row")."""
     code = PA_F32 if dtype == torch.float32 else PA_BF16
-    n = int(load().pa_attention_workspace_bytes(B, T, max_q_len, max_ctx_len, total_ctx, H,
-                                                Hkv, D, block_size, code))
+    n = int(load().pa_attention_workspace_bytes_ex(B, T, max_q_len, max_ctx_len, total_ctx, H,
+                                                   Hkv, D, block_size, code, _mode_code(mode)))
     if n == 0:
-        raise PaError(2, "pa_attention_workspace_bytes")
+        raise PaError(2, "pa_attention_workspace_bytes_ex")
     return n
 
 
 def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,
               max_q_len: int, max_ctx_len: int, scale: float, workspace: torch.Tensor,
               slot_mapping=None, k_new=None, v_new=None, status=None, stream=None,
-              events: Optional[Sequence[torch.cuda.Event]] = None):
-    """pa_attention (or pa_attention_profiled when ``events`` is given)."""
+              events: Optional[Sequence[torch.cuda.Event]] = None, mode: str = "batch"):
+    """pa_attention, or pa_attention_ex when ``events`` or mode="row" is given.
+
+    mode "batch": a row's bits depend only on its own lane. mode "row": also
+    not on its lane's q_len (every row takes the split-KV path); the
+    workspace must then be sized with ``workspace_bytes(..., mode="row")``.
+    """
     T, H, D = q.shape
     NB, bs, Hkv, _ = k_cache.shape
     B = ctx_lens.shape[0]
@@ -164,14 +180,18 @@ def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,
             Hkv, D, bs, NB, int(max_q_len), int(max_ctx_len), float(scale), _dtype_code(q),
             _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)]
     L = load()
-    if events is None:
+    code = _mode_code(mode)
+    if events is None and code == 0:
         _check(L.pa_attention(*args), "pa_attention")
-    else:
+        return
+    arr, n = None, 0
+    if events:
         for e in events:  # torch creates events lazily; recording once creates them
             if not e.cuda_event:
                 e.record(stream)
         arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
-        _check(L.pa_attention_profiled(*args, arr, len(events)), "pa_attention_profiled")
+        n = len(events)
+    _check(L.pa_attention_ex(*args, code, arr, n), "pa_attention_ex")
 
 
 def attention_static_scratch(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,

@@ -17,16 +17,17 @@ def device_step(step: wl.Step, device="cuda"):
     )
 
 
-def workspace_for(step: wl.Step):
+def workspace_for(step: wl.Step, mode="batch"):
     g = step.geom
     dt = torch.float32 if g.dtype == "f32" else torch.bfloat16
     n = pa.workspace_bytes(step.B, step.T, step.max_q_len, step.max_ctx_len,
-                           int(step.ctx_lens.sum()), g.H, g.Hkv, g.D, g.block_size, dt)
+                           int(step.ctx_lens.sum()), g.H, g.Hkv, g.D, g.block_size, dt,
+                           mode=mode)
     return torch.empty(n, dtype=torch.uint8, device="cuda")
 
 
 def run_attention(step: wl.Step, t: dict, layer=0, write=True, scale=None, status=None,
-                  out=None, dev=None, workspace=None):
+                  out=None, dev=None, workspace=None, mode="batch"):
     """One pa_attention call; returns out (device) and the status flags."""
     g = step.geom
     dev = dev or device_step(step)
@@ -34,7 +35,7 @@ def run_attention(step: wl.Step, t: dict, layer=0, write=True, scale=None, statu
     if out is None:
         out = torch.full_like(q, float("nan"))
     st = status if status is not None else pa.new_status()
-    ws = workspace if workspace is not None else workspace_for(step)
+    ws = workspace if workspace is not None else workspace_for(step, mode)
     kw = {}
     if write:
         kw = dict(slot_mapping=dev["slot_mapping"], k_new=t["k_new"][layer],
@@ -43,7 +44,7 @@ def run_attention(step: wl.Step, t: dict, layer=0, write=True, scale=None, statu
                  dev["cu_seqlens_q"], dev["ctx_lens"], out,
                  max_q_len=step.max_q_len, max_ctx_len=step.max_ctx_len,
                  scale=opa.default_scale(g.D) if scale is None else scale,
-                 workspace=ws, status=st, **kw)
+                 workspace=ws, status=st, mode=mode, **kw)
     flags = pa.read_status(st)
     return out, flags
 

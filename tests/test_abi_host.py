@@ -117,3 +117,29 @@ def test_binding_fails_loudly_without_library(monkeypatch, tmp_path):
     monkeypatch.setattr(pa, "_LIB_PATH", str(tmp_path / "missing.so"))
     with pytest.raises(RuntimeError, match="not built"):
         pa.load()
+
+
+def test_workspace_bytes_ex_modes(lib):
+    f = lib.pa_attention_workspace_bytes_ex
+    args = (128, 4216, 512, 16384, 120 * 3000 + 8 * 2560, 40, 8, 128, 16, 1)
+    batch = f(*args, 0)
+    row = f(*args, 1)
+    assert batch == lib.pa_attention_workspace_bytes(*args)
+    # row mode: every row holds up to ceil(max_ctx / 512) splits
+    pairs = 4216 * (16384 // 512)
+    assert row >= pairs * 40 * (128 + 2) * 4
+    assert row > batch
+    # fp32 steps split every row in both modes
+    f32 = args[:-1] + (0,)
+    assert f(*f32, 0) == f(*f32, 1)
+    assert f(*args, 2) == 0 and f(*args, -1) == 0  # unknown mode
+
+
+def test_attention_ex_refuses_unknown_mode(lib):
+    a = [1 << 12, 1 << 12, 1 << 12, 1 << 12, 4, 1 << 12, 1 << 12, None, None, None, 1 << 12,
+         1, 1, 4, 2, 64, 16, 8, 1, 16, 0.125, 0, 1 << 12, 1 << 20, None, None]
+    before = lib.pa_kernel_launches()
+    assert lib.pa_attention_ex(*a, 2, None, 0) == 1
+    assert lib.pa_attention_ex(*a, -1, None, 0) == 1
+    assert lib.pa_attention_ex(*(a[:15] + [96] + a[16:]), 1, None, 0) == 2
+    assert lib.pa_kernel_launches() == before

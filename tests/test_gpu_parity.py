@@ -64,8 +64,8 @@ def test_write_kv_flags_out_of_range_slot():
 # attention
 # ---------------------------------------------------------------------------
 
-def _check_step(step, seed, rows=None, poison=True, layers=1):
-    """Run the step through the C ABI and compare with the oracle.
+def _check_step(step, seed, rows=None, poison=True, layers=1, mode="batch"):
+    """Run the step through the C ABI (invariance ``mode``) and compare with the oracle.
 
     The oracle sees a compact copy of the lanes that own the checked rows
     (all rows when ``rows`` is None): their blocks, before the step's write.
@@ -76,7 +76,7 @@ def _check_step(step, seed, rows=None, poison=True, layers=1):
     worst = 0.0
     for layer in range(layers):
         sub, sub_t, sub_rows, blk = compact_lanes(step, t, lanes, layer)
-        out, flags = run_attention(step, t, layer=layer)
+        out, flags = run_attention(step, t, layer=layer, mode=mode)
         assert flags == 0, flags
         ref, kc, vc = oracle_attention(sub, sub_t)
         # the write inside the call is bit-exact on every block the lanes use
@@ -107,16 +107,17 @@ def _ragged(geom, q_lens, ctx, seed, pool_extra=1.3):
     return wl.build_step(geom, q_lens, ctx, int(used * pool_extra) + 2, rng)
 
 
+@pytest.mark.parametrize("mode", ["batch", "row"])
 @pytest.mark.parametrize("dtype", ["f32", "bf16"])
 @pytest.mark.parametrize("D,bs", [(64, 16), (128, 32)])
-def test_ragged_edges(dtype, D, bs):
+def test_ragged_edges(dtype, D, bs, mode):
     """ctx = 1, ctx on and off split / chunk / block edges, empty lanes, prefill chunks."""
     geom = wl.Geometry(8, 2, D, bs, dtype)
     # 65536 / 65537 keys: 512- and 1024-key splits
     ctx = [1, 15, 16, 17, 511, 512, 513, 1024, 1500, 2049, 7, 40, 600, 12000, 65536, 65537]
     q = [1, 1, 1, 1, 1, 1, 1, 1, 1, 1, 0, 9, 23, 1, 1, 1]
     step = _ragged(geom, q, ctx, 7)
-    _check_step(step, 77)
+    _check_step(step, 77, mode=mode)
 
 
 @pytest.mark.parametrize("H,Hkv", [(16, 1), (40, 8), (64, 4), (4, 4)])
@@ -127,15 +128,17 @@ def test_gqa_groups_bf16(H, Hkv):
     _check_step(step, 91)
 
 
+@pytest.mark.parametrize("mode", ["batch", "row"])
 @pytest.mark.parametrize("D,bs", [(128, 16), (64, 32), (128, 32)])
-def test_prefill_chunk_edges_bf16(D, bs):
-    """Tensor-core prefill: chunks on and off 128-row / 128-key tile edges,
-    chunks starting at key 0, a 2-row chunk, next to decode rows."""
+def test_prefill_chunk_edges_bf16(D, bs, mode):
+    """Prefill chunks on and off 128-row / 128-key tile edges, chunks starting
+    at key 0, a 2-row chunk, next to decode rows (tensor-core prefill in
+    batch mode, the split path in row mode)."""
     geom = wl.Geometry(16, 2, D, bs, "bf16")
     q = [128, 129, 300, 2, 257, 1, 64, 1]
     ctx = [128, 300, 1000, 2, 384, 700, 64 + 191, 5]
     step = _ragged(geom, q, ctx, 21)
-    _check_step(step, 211)
+    _check_step(step, 211, mode=mode)
 
 
 def test_mixed_small_full():
@@ -148,14 +151,15 @@ def test_mixed_small_full():
     _check_step(step, 3100)
 
 
-def test_mixed_step_sampled():
+@pytest.mark.parametrize("mode", ["batch", "row"])
+def test_mixed_step_sampled(mode):
     """Mixed bf16 step at full size (8 x 512 chunks + 120 decodes); sampled rows."""
     step = wl.mixed_step(0)
     cu = step.cu_seqlens_q
     rows = list(range(0, 120, 7))
     for b in range(120, step.B):
         rows += [int(cu[b]), int(cu[b]) + 255, int(cu[b + 1]) - 1]
-    _check_step(step, 3000, rows=rows)
+    _check_step(step, 3000, rows=rows, mode=mode)
 
 
 def test_long_tail_sampled():
