@@ -20,7 +20,10 @@ It is the plain definition, written for a reader to check by eye:
 
 Everything is widened exactly to float64 before any arithmetic. bf16 data is
 carried as raw uint16 bit patterns (bfloat16 is the upper half of an IEEE
-binary32, so widening is a 16-bit shift); fp32 data as float32.
+binary32, so widening is a 16-bit shift); fp32 data as float32. With the
+'fp8' dtype the queries and new rows are bf16 and the caches hold e4m3 codes
+under one scale per tensor: the write quantises the new rows and the gather
+reads codes back as decode(code) * scale (oracle/e4m3.py).
 
 Readings where the pages leave a step open (listed with their reasons in the
 design notes of this repository):
@@ -34,6 +37,8 @@ from __future__ import annotations
 import math
 
 import numpy as np
+
+from . import e4m3
 
 
 # ---------------------------------------------------------------------------
@@ -159,19 +164,33 @@ def row_weights(q_row, K, position: int, scale: float, h: int) -> np.ndarray:
     return softmax_weights(scale * (K[:n, kv, :] @ q_row[h]))
 
 
+def widen_kv(x, dtype: str, kv_scale: float) -> np.ndarray:
+    """Exact float64 values of cache elements: e4m3 codes times their
+    tensor's scale for 'fp8', ``widen`` otherwise."""
+    if dtype == "fp8":
+        return e4m3.dequantize(x, kv_scale)
+    return widen(x, dtype)
+
+
 def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens,
               scale: float, dtype: str, block_size: int,
-              slot_mapping=None, k_new=None, v_new=None, rows=None):
+              slot_mapping=None, k_new=None, v_new=None, rows=None,
+              k_scale: float = 1.0, v_scale: float = 1.0):
     """Reference output of one flat ragged step, float64 ``[T, H, D]``.
 
     When new rows are given they are written first (the step writes, then
-    attends). ``rows`` optionally restricts the work to a subset of flat
-    rows (others are left NaN), for sampled checks of large steps.
-    Returns (out, k_cache_after, v_cache_after).
+    attends); with dtype 'fp8' they are quantised under ``k_scale`` /
+    ``v_scale`` on the way in. ``rows`` optionally restricts the work to a
+    subset of flat rows (others are left NaN), for sampled checks of large
+    steps. Returns (out, k_cache_after, v_cache_after).
     """
     if k_new is not None:
+        if dtype == "fp8":
+            k_new = e4m3.quantize_bf16(k_new, k_scale)
+            v_new = e4m3.quantize_bf16(v_new, v_scale)
         k_cache, v_cache = write_kv(k_cache, v_cache, k_new, v_new,
                                     slot_mapping, block_size)
+    q_dtype = "bf16" if dtype == "fp8" else dtype
     scale = float(np.float32(scale))
     T, H, D = q.shape
     cu = np.asarray(cu_seqlens_q, dtype=np.int64)
@@ -186,13 +205,13 @@ def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens,
         lane_rows = [int(cu[b]) + j for j in range(q_len)]
         if want is not None and not want.intersection(lane_rows):
             continue
-        K = widen(gather(k_cache, block_tables[b], int(ctx[b]), block_size), dtype)
-        V = widen(gather(v_cache, block_tables[b], int(ctx[b]), block_size), dtype)
+        K = widen_kv(gather(k_cache, block_tables[b], int(ctx[b]), block_size), dtype, k_scale)
+        V = widen_kv(gather(v_cache, block_tables[b], int(ctx[b]), block_size), dtype, v_scale)
         for j, r in enumerate(lane_rows):
             if want is not None and r not in want:
                 continue
             position = int(ctx[b]) - q_len + j
-            out[r] = attend_row(widen(q[r], dtype), K, V, position, scale)
+            out[r] = attend_row(widen(q[r], q_dtype), K, V, position, scale)
     return out, k_cache, v_cache
 
 

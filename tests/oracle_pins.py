@@ -16,6 +16,14 @@ What pins what:
   * weights sum           -> softmax weights sum to 1 within 1e-15
   * write bytes           -> write == a flat-index scatter, other bytes untouched
   * kv bytes golden       -> the memory-accounting values the P3 page prints
+  * e4m3 values golden    -> the named values of the e4m3 format's table, and
+                             torch's float8_e4m3fn reading of all 256 codes
+  * e4m3 nearest          -> encode == a brute-force nearest-value search
+                             (ties to the even code, saturation at 448)
+  * e4m3 scaled quantise  -> codes == torch's float32 division then its
+                             float8_e4m3fn cast (inside the finite range)
+  * fp8 brute force       -> fp8 paged oracle == codes read by torch, scaled,
+                             scipy softmax on the unpaged sequence
 """
 import json
 import math
@@ -25,6 +33,7 @@ import numpy as np
 import scipy.special
 import torch
 
+import oracle.e4m3 as e4m3
 import oracle.paged_attention as pa
 from helpers import as_f64, to_store
 
@@ -279,10 +288,148 @@ def check_kv_bytes_golden():
     return None
 
 
+def check_e4m3_values_golden():
+    with open(os.path.join(GOLDEN, "e4m3_values.json")) as f:
+        data = json.load(f)
+    for c in data["cases"]:
+        got = float(e4m3.decode(np.array([c["code"]], np.uint8))[0])
+        want = c["value"]
+        if want == "nan":
+            if not math.isnan(got):
+                return f"e4m3 {c['what']} (code {c['code']}) reads {got}, not NaN"
+        elif got != want or math.copysign(1, got) != math.copysign(1, want):
+            return f"e4m3 {c['what']} (code {c['code']}) reads {got}, the format gives {want}"
+    codes = np.arange(256, dtype=np.uint8)
+    mine = e4m3.decode(codes)
+    lib = torch.from_numpy(codes.copy()).view(torch.float8_e4m3fn).to(torch.float64).numpy()
+    same = (np.isnan(mine) == np.isnan(lib)) & ((mine == lib) | np.isnan(mine))
+    if not np.all(same) or not np.array_equal(np.signbit(mine[mine == 0]), np.signbit(lib[lib == 0])):
+        return "e4m3 decode disagrees with torch.float8_e4m3fn on some code"
+    return None
+
+
+def _nearest_code(y):
+    """Brute force: the finite code nearest to float32 y, ties to the even code."""
+    codes = np.arange(127, dtype=np.int64)  # +0 .. +448
+    vals = np.array([float(torch.tensor([c], dtype=torch.uint8).view(torch.float8_e4m3fn)
+                           .to(torch.float64)) for c in codes])
+    out = []
+    for x in np.asarray(y, dtype=np.float32).astype(np.float64):
+        if math.isnan(x):
+            out.append(0x7F)
+            continue
+        a = min(abs(x), 448.0)
+        d = np.abs(vals - a)
+        best = np.nonzero(d == d.min())[0]
+        c = int(codes[best[0]]) if len(best) == 1 else int([codes[i] for i in best if codes[i] % 2 == 0][0])
+        out.append(c | (0x80 if math.copysign(1, x) < 0 else 0))
+    return np.array(out, dtype=np.uint8)
+
+
+def check_e4m3_nearest():
+    rng = np.random.default_rng(61)
+    vals = e4m3.decode(np.arange(127, dtype=np.uint8))
+    mids = (vals[:-1] + vals[1:]) / 2  # exact in float32: ties
+    ys = np.concatenate([
+        (rng.standard_normal(3000) * np.exp2(rng.integers(-12, 10, 3000))),
+        mids, -mids, np.nextafter(mids, 0), np.nextafter(mids, 1e9),
+        [0.0, -0.0, 448.0, 463.99, 464.0, 464.01, 500.0, 1e30, np.inf, -np.inf, np.nan,
+         2.0 ** -10, 2.0 ** -11, 3 * 2.0 ** -10, -(2.0 ** -6), 2.0 ** -6 * 0.999]])
+    ys = ys.astype(np.float32)
+    got = e4m3.encode(ys)
+    want = _nearest_code(ys)
+    bad = np.nonzero(got != want)[0]
+    if len(bad):
+        i = int(bad[0])
+        return f"e4m3 encode({ys[i]!r}) = {got[i]:#04x}, nearest search gives {want[i]:#04x}"
+    return None
+
+
+def check_e4m3_scaled_quantize():
+    g = torch.Generator().manual_seed(71)
+    x = torch.randn(4096, generator=g).to(torch.bfloat16)
+    for s in (4.5 / 448, 0.013, 1.0, 3.0):
+        codes = e4m3.quantize_bf16(to_store(x), s)
+        y = x.float() / torch.tensor(s, dtype=torch.float32)
+        if float(y.abs().max()) > 448:
+            return "scaled-quantise pin chose a scale that saturates"
+        lib = y.to(torch.float8_e4m3fn).view(torch.uint8).numpy()
+        if not np.array_equal(codes, lib):
+            return f"quantize_bf16(scale {s}) differs from torch's float32 division and cast"
+    return None
+
+
+def check_fp8_brute_force():
+    rng = np.random.default_rng(81)
+    H, Hkv, D, bs = 6, 2, 16, 4
+    lens = [1, 5, 9, 14, 4]
+    q_lens = [1, 1, 6, 3, 0]
+    ks, vs = 0.021, 0.0075
+    Kc = [rng.integers(0, 256, size=(L, Hkv, D)).astype(np.uint8) for L in lens]
+    Vc = [rng.integers(0, 256, size=(L, Hkv, D)).astype(np.uint8) for L in lens]
+    for a in Kc + Vc:  # no NaN codes among the keys
+        a[(a & 0x7F) == 0x7F] = 0x7E
+    g = torch.Generator().manual_seed(82)
+    qt = torch.randn(sum(q_lens), H, D, generator=g).to(torch.bfloat16)
+    # pool of codes (unreferenced entries hold the NaN code)
+    NB = 16
+    kc = np.full((NB * bs, Hkv, D), 0x7F, np.uint8)
+    vc = np.full_like(kc, 0x7F)
+    perm = list(rng.permutation(NB))
+    tables = []
+    for K, V in zip(Kc, Vc):
+        blocks = [int(perm.pop()) for _ in range(-(-K.shape[0] // bs))]
+        tables.append(blocks)
+        for p in range(K.shape[0]):
+            kc[blocks[p // bs] * bs + p % bs] = K[p]
+            vc[blocks[p // bs] * bs + p % bs] = V[p]
+    bt = np.full((len(tables), max(len(t) for t in tables)), -1, np.int64)
+    for i, t in enumerate(tables):
+        bt[i, :len(t)] = t
+    cu = np.concatenate([[0], np.cumsum(q_lens)]).astype(np.int64)
+    scale = 0.37
+    out, _, _ = pa.attention(to_store(qt), kc.reshape(NB, bs, Hkv, D),
+                             vc.reshape(NB, bs, Hkv, D), bt, cu, lens, scale, "fp8", bs,
+                             k_scale=ks, v_scale=vs)
+    read = lambda a, s: torch.from_numpy(a.copy()).view(torch.float8_e4m3fn).to(
+        torch.float64).numpy() * float(np.float32(s))
+    qf = as_f64(qt)
+    s32 = float(np.float32(scale))
+    r, worst = 0, 0.0
+    for b, (L, ql) in enumerate(zip(lens, q_lens)):
+        Kf, Vf = read(Kc[b], ks), read(Vc[b], vs)
+        for j in range(ql):
+            p = L - ql + j
+            for h in range(H):
+                kv = h * Hkv // H
+                w = scipy.special.softmax(s32 * np.einsum("ld,d->l", Kf[:p + 1, kv], qf[r, h]))
+                want = np.einsum("l,ld->d", w, Vf[:p + 1, kv])
+                worst = max(worst, float(np.max(np.abs(out[r, h] - want))))
+            r += 1
+    if not worst <= 1e-12:
+        return f"fp8 brute force: max |diff| {worst}"
+    # the write quantises new rows exactly as torch's division + cast does
+    kn = torch.randn(3, Hkv, D, generator=g).to(torch.bfloat16)
+    vn = torch.randn(3, Hkv, D, generator=g).to(torch.bfloat16)
+    slots = np.array([2, -1, 9], np.int64)
+    _, k2, v2 = pa.attention(to_store(qt[:1]), kc.reshape(NB, bs, Hkv, D),
+                             vc.reshape(NB, bs, Hkv, D), bt[:1], np.array([0, 1]), [1],
+                             scale, "fp8", bs, slot_mapping=slots, k_new=to_store(kn),
+                             v_new=to_store(vn), k_scale=ks, v_scale=vs)
+    for new, cache, s in ((kn, k2, ks), (vn, v2, vs)):
+        lib = (new.float() / torch.tensor(s, dtype=torch.float32)).to(
+            torch.float8_e4m3fn).view(torch.uint8).numpy()
+        flat = cache.reshape(NB * bs, Hkv, D)
+        if not (np.array_equal(flat[2], lib[0]) and np.array_equal(flat[9], lib[2])):
+            return "fp8 write: stored codes differ from torch's division + cast"
+    return None
+
+
 ALL_CHECKS = [check_single_key, check_zero_query_mean, check_position_code,
               check_constant_v_per_head, check_one_hot, check_brute_force,
               check_block_permutation, check_weights_sum, check_write_bytes,
-              check_kv_bytes_golden]
+              check_kv_bytes_golden, check_e4m3_values_golden, check_e4m3_nearest,
+              check_e4m3_scaled_quantize, check_fp8_brute_force]
 
 
 def failures():

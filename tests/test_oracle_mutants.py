@@ -5,11 +5,14 @@ continuous-batching sampler" (Evidence, item 5: gather drops the last key,
 slot mapping ignores the block offset, K heads flipped, causal mask off by
 one) plus mistakes a from-scratch oracle could make (operands swapped, scale
 dropped, unnormalised weights, wrong bf16 widening, row positions counted
-from the chunk start).
+from the chunk start), and for the e4m3 cache format: exponent bias off by
+one, subnormals read as normals, truncation instead of rounding, ties away
+from zero, no saturation, the scale ignored or applied the wrong way.
 """
 import numpy as np
 import pytest
 
+import oracle.e4m3 as e4m3
 import oracle.paged_attention as pa
 import oracle_pins
 
@@ -72,6 +75,77 @@ MUTANTS = {
     "bf16 widened with the wrong shift": ("widen", _widen_wrong),
     "kv bytes forget V": ("kv_bytes_per_token", _kv_bytes_no_v),
 }
+
+
+_orig_decode = e4m3.decode
+_orig_encode = e4m3.encode
+
+
+def _decode_bias8(codes):
+    v = _orig_decode(codes)
+    e = (np.asarray(codes).astype(np.int64) >> 3) & 0xF
+    return np.where(e > 0, v / 2.0, v)
+
+
+def _decode_subnormal_as_normal(codes):
+    c = np.asarray(codes).astype(np.int64)
+    v = _orig_decode(codes)
+    e, m = (c >> 3) & 0xF, (c & 7).astype(np.float64)
+    sign = np.where(c & 0x80, -1.0, 1.0)
+    return np.where((e == 0) & (m > 0), sign * (1 + m / 8) * 2.0 ** -7, v)
+
+
+def _encode_truncates(y):
+    # round toward zero: pick the code below, then step up only on exact hits
+    y = np.asarray(y)
+    c = _orig_encode(y)
+    back = np.abs(_orig_decode(c))
+    over = back > np.abs(y.astype(np.float64))
+    return np.where(over & ((c & 0x7F) > 0), c - 1, c).astype(np.uint8)
+
+
+def _encode_ties_away(y):
+    y = np.asarray(y)
+    c = _orig_encode(y)
+    a = np.abs(y.astype(np.float64))
+    nxt = (np.minimum((c & 0x7F) + 1, 126) | (c & 0x80)).astype(np.uint8)
+    v_c, v_n = np.abs(_orig_decode(c)), np.abs(_orig_decode(nxt))
+    tie = (v_c < a) & (a - v_c == v_n - a)  # a tie that went to the lower code
+    return np.where(tie, nxt, c).astype(np.uint8)
+
+
+def _encode_no_saturation(y):
+    y = np.asarray(y)
+    c = _orig_encode(y)
+    big = np.isfinite(y) & (np.abs(y.astype(np.float64)) > 464)
+    return np.where(big, (c & 0x80) | 0x7F, c).astype(np.uint8)
+
+
+def _dequantize_ignores_scale(codes, scale):
+    return _orig_decode(codes)
+
+
+def _quantize_multiplies(bits, scale):
+    return _orig_encode((e4m3.bf16_bits_to_f32(bits) * np.float32(scale)).astype(np.float32))
+
+
+E4M3_MUTANTS = {
+    "e4m3 exponent bias 8": ("decode", _decode_bias8),
+    "e4m3 subnormals read as normals": ("decode", _decode_subnormal_as_normal),
+    "e4m3 encode truncates": ("encode", _encode_truncates),
+    "e4m3 ties away from zero": ("encode", _encode_ties_away),
+    "e4m3 no saturation": ("encode", _encode_no_saturation),
+    "fp8 scale ignored on read": ("dequantize", _dequantize_ignores_scale),
+    "fp8 scale multiplied on write": ("quantize_bf16", _quantize_multiplies),
+}
+
+
+@pytest.mark.parametrize("name", sorted(E4M3_MUTANTS))
+def test_e4m3_mutant_is_caught(name, monkeypatch):
+    attr, fn = E4M3_MUTANTS[name]
+    monkeypatch.setattr(e4m3, attr, fn)
+    fails = oracle_pins.failures()
+    assert fails, f"no pin caught the mutant '{name}'"
 
 
 @pytest.mark.parametrize("name", sorted(MUTANTS))
