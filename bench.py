@@ -37,9 +37,17 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode-attention KV GB/s (% of GB300 HBM peak) and tokens/s per ragged step"
 FALLBACK_HBM_GBS = 6800.0
-PROFILE_SUMMARY = os.path.join(ROOT, "profiles", "decode_bf16_long_tail.md")
-KERNEL_SOURCES = ["invariant_paged_kv_gb300/csrc/pa_decode_bf16.cu",
-                  "invariant_paged_kv_gb300/csrc/pa_common.cuh"]
+# committed ncu summaries of the decode kernels and the sources they were taken on
+PROFILES = {
+    False: (os.path.join(ROOT, "profiles", "decode_bf16_long_tail.md"),
+            ["invariant_paged_kv_gb300/csrc/pa_decode_bf16.cu",
+             "invariant_paged_kv_gb300/csrc/pa_split_items.cuh",
+             "invariant_paged_kv_gb300/csrc/pa_common.cuh"]),
+    True: (os.path.join(ROOT, "profiles", "decode_fp8_long_tail.md"),
+           ["invariant_paged_kv_gb300/csrc/pa_decode_fp8.cu",
+            "invariant_paged_kv_gb300/csrc/pa_split_items.cuh",
+            "invariant_paged_kv_gb300/csrc/pa_common.cuh"]),
+}
 
 
 def parse():
@@ -58,6 +66,9 @@ def parse():
     ap.add_argument("--no-clocks", action="store_true")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of replaying a CUDA graph")
+    ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
+                    help="cache element type of the decode workloads: bf16, or e4m3 codes "
+                         "with per-tensor scales (q, new rows and out stay bf16)")
     ap.add_argument("--mode", choices=["batch", "row"], default="batch",
                     help="invariance mode: 'row' sends prefill rows down the split path too")
     return ap.parse_args()
@@ -77,12 +88,12 @@ def make_step(args, rank, free_bytes=None):
             pool, lanes, layers = 1.2e9, 48, args.layers or 1
         if free_bytes is not None:  # shared GPU: shrink the pool, never fail
             pool = min(pool, 0.8 * free_bytes / layers)
-        step = wl.long_tail(rank, lanes=lanes, pool_bytes_per_layer=pool)
-        name = "long_tail_decode"
+        step = wl.long_tail(rank, lanes=lanes, pool_bytes_per_layer=pool, dtype=args.kv)
+        name = "long_tail_decode" + ("_e4m3_kv" if args.kv == "fp8" else "")
     elif args.workload == "decode_batch":
         layers = args.layers or 1
-        step = wl.decode_batch(rank, lanes=16 if args.small else 64)
-        name = "decode_batch"
+        step = wl.decode_batch(rank, lanes=16 if args.small else 64, dtype=args.kv)
+        name = "decode_batch" + ("_e4m3_kv" if args.kv == "fp8" else "")
     else:
         layers = args.layers or 1
         step = wl.mixed_step(rank)
@@ -102,7 +113,14 @@ def workload_config(step, layers, name, args):
         "small": bool(args.small),
         "cuda_graph": not getattr(args, "no_graph", True),
         "invariance_mode": getattr(args, "mode", "batch"),
+        "kv_cache": ("e4m3 codes, per-tensor scales k %g / v %g; f16 products, fp32 accumulate"
+                     % (wl_scales()[0], wl_scales()[1])) if g.dtype == "fp8" else g.dtype,
     }
+
+
+def wl_scales():
+    from invariant_paged_kv_gb300 import workload as wl
+    return wl.FP8_K_SCALE, wl.FP8_V_SCALE
 
 
 # ---------------------------------------------------------------------------
@@ -123,14 +141,16 @@ def _oracle_lane_job(job):
 
     def store(x):
         x = x.contiguous()
-        return x.numpy() if x.dtype == torch.float32 else x.view(torch.int16).numpy().view(np.uint16)
+        if x.dtype in (torch.float32, torch.uint8):
+            return x.numpy()
+        return x.view(torch.int16).numpy().view(np.uint16)
 
     args = [store(t["q"][0]), store(t["k_cache"][0]), store(t["v_cache"][0])]
     t0 = time.perf_counter()
     opa.attention(*args, sub.block_tables, sub.cu_seqlens_q, sub.ctx_lens,
                   opa.default_scale(sub.geom.D), sub.geom.dtype, sub.geom.block_size,
                   slot_mapping=sub.slot_mapping, k_new=store(t["k_new"][0]),
-                  v_new=store(t["v_new"][0]))
+                  v_new=store(t["v_new"][0]), k_scale=wl.FP8_K_SCALE, v_scale=wl.FP8_V_SCALE)
     dt = time.perf_counter() - t0
     return wl.kv_bytes(sub), dt
 
@@ -284,21 +304,22 @@ def measured_bf16_peak(sustained):
         return (1700.0 if sustained else 1900.0), "fallback"
 
 
-def committed_traffic():
+def committed_traffic(fp8=False):
     """Per-launch DRAM bytes of the decode kernel from the committed ncu
     summary, if the kernel sources still match the ones it was taken on."""
+    summary, sources = PROFILES[bool(fp8)]
     h = hashlib.sha256()
-    for rel in KERNEL_SOURCES:
+    for rel in sources:
         with open(os.path.join(ROOT, rel), "rb") as f:
             h.update(f.read())
     sha = h.hexdigest()[:16]
     try:
-        text = open(PROFILE_SUMMARY).read()
+        text = open(summary).read()
     except OSError:
         return None, sha
     vals = dict(line.split(":", 1) for line in text.splitlines()
                 if line.startswith(("source_sha256_16:", "traffic_bytes_per_launch_full:")))
-    if vals.get("source_sha256_16:".rstrip(":"), "").strip() != sha:
+    if vals.get("source_sha256_16", "").strip() != sha:
         return None, sha
     try:
         return float(vals["traffic_bytes_per_launch_full"]), sha
@@ -326,7 +347,7 @@ def run_ours(args, rank, world, local_rank):
     outs = [torch.empty_like(q) for q in tens["q"]]
     ws = torch.empty(pa.workspace_bytes(step.B, step.T, step.max_q_len, step.max_ctx_len,
                                         int(step.ctx_lens.sum()), g.H, g.Hkv, g.D,
-                                        g.block_size, tens["q"][0].dtype, mode=args.mode),
+                                        g.block_size, tens["k_cache"][0].dtype, mode=args.mode),
                      dtype=torch.uint8, device=dev)
     status = pa.new_status(dev)
     scale = 1.0 / math.sqrt(g.D)
@@ -342,7 +363,7 @@ def run_ours(args, rank, world, local_rank):
                          workspace=ws, slot_mapping=dslots if dslots is not None else slots,
                          k_new=(kn or tens["k_new"])[l], v_new=(vn or tens["v_new"])[l],
                          status=status, events=None if events is None else events[l],
-                         mode=args.mode)
+                         mode=args.mode, k_scale=wl.FP8_K_SCALE, v_scale=wl.FP8_V_SCALE)
 
     def barrier():
         if world > 1:
@@ -465,12 +486,15 @@ def run_ours(args, rank, world, local_rank):
 
     peak, peak_kind = measured_hbm_peak()
     dec_ms = statistics.mean(decode_ms)
-    dec_bytes = wl.decode_rows_kv_bytes(step) + (step.q_lens == 1).sum() * g.H * g.D * g.elem_bytes \
+    dec_bytes = wl.decode_rows_kv_bytes(step) + (step.q_lens == 1).sum() * g.H * g.D * g.q_bytes \
         + 4 * int(sum(-(-int(c) // g.block_size) for c, q in zip(step.ctx_lens, step.q_lens) if q == 1))
     nbytes["decode_kernel"] = int(dec_bytes)
     achieved = nbytes["decode_kernel"] / (dec_ms * 1e-3) / 1e9
-    traffic, sha = committed_traffic()
-    roofline = {"bound": "hbm", "kernel": "decode_bf16_kernel (split-KV decode partials)",
+    fp8 = g.dtype == "fp8"
+    traffic, sha = committed_traffic(fp8)
+    roofline = {"bound": "hbm",
+                "kernel": ("decode_fp8_kernel (split-KV decode partials, e4m3 codes)" if fp8
+                           else "decode_bf16_kernel (split-KV decode partials)"),
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "peak_kind": peak_kind, "frac": round(achieved / peak, 4),
                 "traffic": traffic, "algorithmic_bytes_per_launch": nbytes["decode_kernel"],
@@ -500,7 +524,8 @@ def run_ours(args, rank, world, local_rank):
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
         "steps": K, "warmup": max(3, args.warmup), "ms_per_step": round(ms_max, 4),
-        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+        "dtype": "e4m3" if g.dtype == "fp8" else "bf16",
         "data": "synthetic (seeded N(0,1) q/K/V; seeded heavy-tailed lengths and block tables)",
         "config": workload_config(step, layers, name, args),
         "rows_per_s": round(rows_per_s, 1),

@@ -57,7 +57,22 @@ typedef enum {
   PA_ERR_CUDA = 4           /* a CUDA runtime call or launch failed           */
 } pa_status;
 
-typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
+/*
+ * Element types.
+ *   PA_F32       q, caches, new rows and out in fp32
+ *   PA_BF16      all of them in bf16
+ *   PA_FP8_E4M3  q, new rows and out in bf16; the caches hold float8 e4m3fn
+ *                codes (1 byte: sign, 4 exponent bits with bias 7, 3 mantissa
+ *                bits; S.1111.111 is NaN; largest finite 448) under one fp32
+ *                scale per tensor, k_scale for the K cache and v_scale for the
+ *                V cache: a code c stands for e4m3(c) * scale. New rows are
+ *                quantised on write as RN-even(x / scale) with x / scale in
+ *                fp32, finite overflow and infinities saturating to +-448.
+ *                ("P3: native paged-KV continuous-batching sampler", Review
+ *                (adversarial pass), kv_dtype: K/V are dequantised on read;
+ *                fp8 KV without per-tensor scales is visibly lossy.)
+ */
+typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
 
 /*
  * Invariance modes of pa_attention_ex.
@@ -76,8 +91,8 @@ typedef enum { PA_F32 = 0, PA_BF16 = 1 } pa_dtype;
  *                            ("Numerics envelopes", Prefix hits resume at any
  *                            token; "P3: native paged-KV continuous-batching
  *                            sampler", Evidence, batch invariance under
- *                            chunk sizes 1, 2 and 64). fp32 steps always
- *                            behave this way.
+ *                            chunk sizes 1, 2 and 64). fp32 and e4m3 steps
+ *                            always behave this way.
  */
 typedef enum { PA_MODE_BATCH_INVARIANT = 0, PA_MODE_ROW_INVARIANT = 1 } pa_mode;
 
@@ -111,6 +126,20 @@ pa_status pa_write_kv(const void* k_new, const void* v_new, void* k_cache, void*
                       const int64_t* slot_mapping, int32_t T, int32_t num_blocks,
                       int32_t block_size, int32_t Hkv, int32_t D, pa_dtype dtype,
                       int32_t* status, void* stream);
+
+/*
+ * pa_write_kv_scaled -- pa_write_kv for every element type, with the scales
+ * of PA_FP8_E4M3 caches (k_scale, v_scale: finite and > 0; ignored for the
+ * other types, whose bytes are copied unchanged). For PA_FP8_E4M3, k_new and
+ * v_new are bf16 [T, Hkv, D] and each element lands in the cache as its
+ * e4m3 code (see pa_dtype). pa_write_kv refuses PA_FP8_E4M3 with
+ * PA_ERR_UNSUPPORTED (it has no scales).
+ */
+pa_status pa_write_kv_scaled(const void* k_new, const void* v_new, void* k_cache,
+                             void* v_cache, const int64_t* slot_mapping, int32_t T,
+                             int32_t num_blocks, int32_t block_size, int32_t Hkv, int32_t D,
+                             pa_dtype dtype, float k_scale, float v_scale, int32_t* status,
+                             void* stream);
 
 /*
  * pa_attention_workspace_bytes -- device scratch pa_attention needs.
@@ -182,8 +211,16 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
                        size_t workspace_bytes, int32_t* status, void* stream);
 
 /*
- * pa_attention_ex -- pa_attention with an invariance mode and phase timing
- * hooks (pa_attention is this with PA_MODE_BATCH_INVARIANT and no events).
+ * pa_attention_ex -- pa_attention with cache scales, an invariance mode and
+ * phase timing hooks (pa_attention is this with scales 1,
+ * PA_MODE_BATCH_INVARIANT and no events; it refuses PA_FP8_E4M3 with
+ * PA_ERR_UNSUPPORTED).
+ *   k_scale, v_scale
+ *             scales of PA_FP8_E4M3 caches (finite and > 0, else
+ *             PA_ERR_INVALID_ARG); ignored for the other types. e4m3 steps
+ *             take the split path for every row (as fp32 steps do), so they
+ *             are row invariant in either mode; scores use
+ *             scale * k_scale and every output is multiplied by v_scale.
  *   mode      see pa_mode; an unknown value returns PA_ERR_INVALID_ARG. The
  *             workspace must hold what pa_attention_workspace_bytes_ex
  *             returns for the same mode.
@@ -203,8 +240,9 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
                           void* out, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t D,
                           int32_t block_size, int32_t num_blocks, int32_t max_q_len,
                           int32_t max_ctx_len, float scale, pa_dtype dtype, void* workspace,
-                          size_t workspace_bytes, int32_t* status, void* stream, pa_mode mode,
-                          void* const* events, int32_t n_events);
+                          size_t workspace_bytes, int32_t* status, void* stream,
+                          float k_scale, float v_scale, pa_mode mode, void* const* events,
+                          int32_t n_events);
 
 /*
  * pa_attention_static_scratch -- pa_attention for callers that cannot

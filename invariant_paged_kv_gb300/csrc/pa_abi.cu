@@ -14,6 +14,8 @@ namespace pa {
 cudaError_t launch_prologue(const StepParams& p, bool plan, bool write, cudaStream_t s);
 cudaError_t launch_decode_bf16(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
                                long long max_items, cudaStream_t s);
+cudaError_t launch_decode_fp8(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
+                              long long max_items, cudaStream_t s);
 cudaError_t launch_split_f32(const StepParams& p, long long max_items, cudaStream_t s);
 cudaError_t launch_combine(const StepParams& p, cudaStream_t s);
 cudaError_t launch_prefill_tc(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
@@ -42,22 +44,28 @@ inline size_t align_up(size_t x) { return (x + kAlign - 1) / kAlign * kAlign; }
 
 bool aligned16(const void* ptr) { return (reinterpret_cast<uintptr_t>(ptr) & 15u) == 0; }
 
-int elem_bytes_of(pa_dtype d) { return d == PA_F32 ? 4 : (d == PA_BF16 ? 2 : 0); }
+// Bytes of a q / out / new-row element (bf16 for e4m3 caches).
+int elem_bytes_of(pa_dtype d) { return d == PA_F32 ? 4 : 2; }
+
+bool scales_ok(float k_scale, float v_scale) {
+  return std::isfinite(k_scale) && k_scale > 0.f && std::isfinite(v_scale) && v_scale > 0.f;
+}
 
 pa_status check_geometry(int32_t H, int32_t Hkv, int32_t D, int32_t block_size, pa_dtype dtype) {
   if (H <= 0 || Hkv <= 0 || D <= 0 || block_size <= 0) return PA_ERR_INVALID_ARG;
-  if (dtype != PA_F32 && dtype != PA_BF16) return PA_ERR_UNSUPPORTED;
+  if (dtype != PA_F32 && dtype != PA_BF16 && dtype != PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;
   if (D != 64 && D != 128) return PA_ERR_UNSUPPORTED;
   if (block_size != 16 && block_size != 32) return PA_ERR_UNSUPPORTED;
   if (H % Hkv != 0 || H / Hkv > 16) return PA_ERR_UNSUPPORTED;
   return PA_OK;
 }
 
-// Every row takes the split path for fp32 (CUDA-core FMA, no TF32) and in
-// the row-invariant mode. Otherwise (bf16) only decode lanes (q_len == 1)
-// do; lanes with q_len >= 2 go to the tensor-core prefill kernel.
+// Every row takes the split path for fp32 (CUDA-core FMA, no TF32), for
+// e4m3 caches and in the row-invariant mode. Otherwise (bf16) only decode
+// lanes (q_len == 1) do; lanes with q_len >= 2 go to the tensor-core prefill
+// kernel.
 bool split_all_rows(pa_dtype dtype, pa_mode mode) {
-  return dtype == PA_F32 || mode == PA_MODE_ROW_INVARIANT;
+  return dtype != PA_BF16 || mode == PA_MODE_ROW_INVARIANT;
 }
 
 bool mode_known(pa_mode mode) {
@@ -166,6 +174,23 @@ bool encode_cache_map(CUtensorMap* map, const void* cache, int NB, int bs, int H
   return r == CUDA_SUCCESS;
 }
 
+// [NB * bs tokens, Hkv, D] e4m3 code cache; box = D bytes x 1 head x 16
+// tokens, 128-byte swizzle for D = 128 and 64-byte swizzle for D = 64 (the
+// box row is the whole swizzle span either way).
+bool encode_code_map(CUtensorMap* map, const void* cache, int NB, int bs, int Hkv, int D) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[3] = {(cuuint64_t)D, (cuuint64_t)Hkv, (cuuint64_t)NB * (cuuint64_t)bs};
+  cuuint64_t strides[2] = {(cuuint64_t)D, (cuuint64_t)Hkv * D};
+  cuuint32_t box[3] = {(cuuint32_t)D, 1, (cuuint32_t)kChunk};
+  cuuint32_t estr[3] = {1, 1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_UINT8, 3, const_cast<void*>(cache), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE,
+                  D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
 // q [T, H, D] bf16; box = 64 elements x 1 head x 128 rows, 128-byte swizzle.
 bool encode_q_map(CUtensorMap* map, const void* q, int T, int H, int D) {
   auto fn = encode_fn();
@@ -221,9 +246,21 @@ pa_status pa_write_kv(const void* k_new, const void* v_new, void* k_cache, void*
                       const int64_t* slot_mapping, int32_t T, int32_t num_blocks,
                       int32_t block_size, int32_t Hkv, int32_t D, pa_dtype dtype,
                       int32_t* status, void* stream) {
+  if (dtype == PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;  // needs the scales
+  return pa_write_kv_scaled(k_new, v_new, k_cache, v_cache, slot_mapping, T, num_blocks,
+                            block_size, Hkv, D, dtype, 1.f, 1.f, status, stream);
+}
+
+pa_status pa_write_kv_scaled(const void* k_new, const void* v_new, void* k_cache,
+                             void* v_cache, const int64_t* slot_mapping, int32_t T,
+                             int32_t num_blocks, int32_t block_size, int32_t Hkv, int32_t D,
+                             pa_dtype dtype, float k_scale, float v_scale, int32_t* status,
+                             void* stream) {
   if (T < 0 || num_blocks <= 0) return PA_ERR_INVALID_ARG;
   pa_status g = check_geometry(Hkv, Hkv, D, block_size, dtype);
   if (g != PA_OK) return g;
+  const bool fp8 = dtype == PA_FP8_E4M3;
+  if (fp8 && !scales_ok(k_scale, v_scale)) return PA_ERR_INVALID_ARG;
   if (T == 0) return PA_OK;
   if (!k_new || !v_new || !k_cache || !v_cache || !slot_mapping) return PA_ERR_INVALID_ARG;
   if (!aligned16(k_new) || !aligned16(v_new) || !aligned16(k_cache) || !aligned16(v_cache))
@@ -243,6 +280,9 @@ pa_status pa_write_kv(const void* k_new, const void* v_new, void* k_cache, void*
   p.bs = block_size;
   p.NB = num_blocks;
   p.elem_bytes = elem_bytes_of(dtype);
+  p.kv_fp8 = fp8 ? 1 : 0;
+  p.k_scale = fp8 ? k_scale : 1.f;
+  p.v_scale = fp8 ? v_scale : 1.f;
   cudaError_t e = launch_prologue(p, false, true, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
@@ -274,8 +314,9 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
                           void* out, int32_t B, int32_t T, int32_t H, int32_t Hkv, int32_t D,
                           int32_t block_size, int32_t num_blocks, int32_t max_q_len,
                           int32_t max_ctx_len, float scale, pa_dtype dtype, void* workspace,
-                          size_t workspace_bytes, int32_t* status, void* stream, pa_mode mode,
-                          void* const* events, int32_t n_events) {
+                          size_t workspace_bytes, int32_t* status, void* stream,
+                          float k_scale, float v_scale, pa_mode mode, void* const* events,
+                          int32_t n_events) {
   // ---- host validation: nothing below touches CUDA until it all passes ----
   if (B < 0 || T < 0 || num_blocks <= 0 || max_q_len < 0 || max_ctx_len < 0 || n_events < 0 ||
       !mode_known(mode))
@@ -283,6 +324,8 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
   pa_status g = check_geometry(H, Hkv, D, block_size, dtype);
   if (g != PA_OK) return g;
   if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
+  const bool fp8 = dtype == PA_FP8_E4M3;
+  if (fp8 && !scales_ok(k_scale, v_scale)) return PA_ERR_INVALID_ARG;
   const bool with_write = slot_mapping || k_new || v_new;
   if (with_write && !(slot_mapping && k_new && v_new)) return PA_ERR_INVALID_ARG;
   if ((long long)num_blocks * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
@@ -332,11 +375,20 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
   p.split_all_rows = split_all_rows(dtype, mode) ? 1 : 0;
   p.scale = scale;
   p.scale_log2 = scale * 1.4426950408889634f;
+  p.kv_fp8 = fp8 ? 1 : 0;
+  p.k_scale = fp8 ? k_scale : 1.f;
+  p.v_scale = fp8 ? v_scale : 1.f;
+  p.out_scale = p.v_scale;
+  if (fp8) p.scale_log2 *= k_scale;
   p.plan = carve(workspace, cap, B, T, H, D);
   const bool prefill_tc = !p.split_all_rows && max_q_len >= 2;
 
   CUtensorMap tmK, tmV, tmQ;
-  if (dtype == PA_BF16) {
+  if (fp8) {
+    if (!encode_code_map(&tmK, k_cache, num_blocks, block_size, Hkv, D) ||
+        !encode_code_map(&tmV, v_cache, num_blocks, block_size, Hkv, D))
+      return PA_ERR_CUDA;
+  } else if (dtype == PA_BF16) {
     if (!encode_cache_map(&tmK, k_cache, num_blocks, block_size, Hkv, D) ||
         !encode_cache_map(&tmV, v_cache, num_blocks, block_size, Hkv, D))
       return PA_ERR_CUDA;
@@ -350,8 +402,9 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
   if (launch_prologue(p, true, with_write, s) != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
   if (record(events, n_events, 1, s) != PA_OK) return PA_ERR_CUDA;
-  cudaError_t e = dtype == PA_BF16 ? launch_decode_bf16(p, tmK, tmV, items, s)
-                                   : launch_split_f32(p, items, s);
+  cudaError_t e = fp8 ? launch_decode_fp8(p, tmK, tmV, items, s)
+                      : dtype == PA_BF16 ? launch_decode_bf16(p, tmK, tmV, items, s)
+                                         : launch_split_f32(p, items, s);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
   if (record(events, n_events, 2, s) != PA_OK) return PA_ERR_CUDA;
@@ -375,10 +428,12 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
                        int32_t block_size, int32_t num_blocks, int32_t max_q_len,
                        int32_t max_ctx_len, float scale, pa_dtype dtype, void* workspace,
                        size_t workspace_bytes, int32_t* status, void* stream) {
+  if (dtype == PA_FP8_E4M3) return PA_ERR_UNSUPPORTED;  // needs the scales
   return pa_attention_ex(q, k_cache, v_cache, block_tables, max_blocks_per_seq, cu_seqlens_q,
                          ctx_lens, slot_mapping, k_new, v_new, out, B, T, H, Hkv, D, block_size,
                          num_blocks, max_q_len, max_ctx_len, scale, dtype, workspace,
-                         workspace_bytes, status, stream, PA_MODE_BATCH_INVARIANT, nullptr, 0);
+                         workspace_bytes, status, stream, 1.f, 1.f, PA_MODE_BATCH_INVARIANT,
+                         nullptr, 0);
 }
 
 pa_status pa_read_status(int32_t* status, void* stream, int32_t* flags_out, int32_t clear) {

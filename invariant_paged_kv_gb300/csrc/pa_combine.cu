@@ -9,7 +9,8 @@
 // 0..W-1 left to right in fp32, one rounding; Layout invariance of QCP:
 // combine_attention_partials with the ordered fold), applied to splits
 // instead of ranks. n depends only on the row's own key count, so the fold is
-// the same whatever else is in the step.
+// the same whatever else is in the step. The quotient is multiplied by
+// out_scale (the V scale of e4m3 caches; 1, an exact no-op, otherwise).
 #include <type_traits>
 
 #include "pa_common.cuh"
@@ -76,7 +77,7 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p
   const size_t o = ((size_t)row * p.H + h) * D + VPL * lane;
   float r[VPL];
 #pragma unroll
-  for (int j = 0; j < VPL; ++j) r[j] = finish_div(A[j], f.L);
+  for (int j = 0; j < VPL; ++j) r[j] = finish_div(A[j], f.L) * p.out_scale;
   if (p.elem_bytes == 4) {
     float* out = static_cast<float*>(p.out) + o;
 #pragma unroll

@@ -21,7 +21,7 @@
 // others leave (m, l, acc) for the fixed-order combine. Every item's
 // arithmetic depends only on its own row's q and keys: which warp runs it and
 // what else is in the step do not enter.
-#include "pa_common.cuh"
+#include "pa_split_items.cuh"
 
 namespace pa {
 
@@ -46,43 +46,6 @@ template <int D>
 __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int tok, int c16) {
   const int half = c16 >> 3, chunk = c16 & 7;
   return base + half * Tile<D>::kHalfBytes + tok * 128 + ((chunk ^ (tok & 7)) << 4);
-}
-
-struct Item {
-  int pair, kvh, row, lane, keys, t0, len, nchunks, single;
-};
-
-// k-th item of warp gw among nw warps: passes over the item list alternate
-// direction (snake order), so with items sorted by size every warp gets a
-// near-equal share of the work. Which warp runs an item never changes its
-// arithmetic.
-__device__ __forceinline__ long long item_at(long long k, long long gw, long long nw) {
-  return k * nw + ((k & 1) ? (nw - 1 - gw) : gw);
-}
-
-__device__ __forceinline__ Item load_item(const StepParams& p, long long item, int nfull) {
-  Item it;
-  const int k = (int)(item / p.Hkv);
-  it.kvh = (int)(item - (long long)k * p.Hkv);
-  it.pair = pair_slot(p.plan, k, nfull);
-  const int4 pr = p.plan.pairs[it.pair];
-  it.row = pr.x;
-  it.lane = pr.z;
-  it.keys = pr.w;
-  const int sl = split_len(it.keys);
-  it.t0 = pr.y * sl;
-  it.len = min(sl, it.keys - it.t0);
-  it.nchunks = (it.len + kChunk - 1) / kChunk;
-  it.single = it.keys <= sl;
-  return it;
-}
-
-// Block ids w0 .. w0 + 31 of the item's range (relative to its first block):
-// lane i holds entry w0 + i.
-__device__ __forceinline__ int load_blocks(const StepParams& p, const Item& it, int w0, int lane) {
-  const int nblk = (it.len + p.bs - 1) / p.bs;
-  if (w0 + lane >= nblk) return 0;
-  return p.block_tables[(size_t)it.lane * p.max_blocks + it.t0 / p.bs + w0 + lane];
 }
 
 template <int D, int NT>

@@ -7,7 +7,8 @@
 // (block, offset) = (slot / block_size, slot % block_size) in place. Rows of
 // the cache are contiguous [Hkv, D] runs, so a slot names the flat row
 // `slot` of the [num_blocks * block_size, Hkv, D] view; the copy moves 16-byte
-// vectors and never converts.
+// vectors and never converts, except into e4m3 caches, where each element is
+// quantised under its tensor's scale on the way in.
 //
 // Split plan: every row on the split path attends keys 0..position and is cut
 // into ranges [S i, S (i + 1)) with S = split_len(its key count) -- a function
@@ -200,7 +201,48 @@ __device__ void build_plan(const StepParams& p) {
   }
 }
 
+// e4m3 caches: each new bf16 row is quantised on the way in, code =
+// RN-even(x / scale) with the quotient in fp32 and saturation to +-448 (the
+// per-tensor scaling the kv_dtype item of "P3: native paged-KV
+// continuous-batching sampler", Review (adversarial pass), asks for). A thread
+// converts 8 elements: one 16-byte load, one 8-byte store.
+__device__ void write_rows_fp8(const StepParams& p, int cta, int ncta) {
+  const int n8 = p.Hkv * p.D / 8;  // 8-element groups per row
+  const long long nslots = (long long)p.NB * p.bs;
+  const long long total = (long long)p.T * n8;
+  const uint4* kn = static_cast<const uint4*>(p.k_new);
+  const uint4* vn = static_cast<const uint4*>(p.v_new);
+  uint2* kc = static_cast<uint2*>(const_cast<void*>(p.k_cache));
+  uint2* vc = static_cast<uint2*>(const_cast<void*>(p.v_cache));
+  for (long long i = (long long)cta * blockDim.x + threadIdx.x; i < total;
+       i += (long long)ncta * blockDim.x) {
+    const long long t = i / n8;
+    const int v = (int)(i - t * n8);
+    const long long slot = p.slot_mapping[t];
+    if (slot < 0) continue;
+    if (slot >= nslots) {
+      if (v == 0) raise_flag(p.status, PA_FLAG_SLOT_RANGE);
+      continue;
+    }
+#pragma unroll
+    for (int kv = 0; kv < 2; ++kv) {
+      const uint4 x = (kv ? vn : kn)[t * n8 + v];
+      const float sc = kv ? p.v_scale : p.k_scale;
+      const uint32_t w[4] = {x.x, x.y, x.z, x.w};
+      uint32_t c[4];
+#pragma unroll
+      for (int e = 0; e < 4; ++e)
+        c[e] = f32x2_to_e4m3x2(__fdiv_rn(bf16_lo(w[e]), sc), __fdiv_rn(bf16_hi(w[e]), sc));
+      (kv ? vc : kc)[slot * n8 + v] = make_uint2(c[0] | (c[1] << 16), c[2] | (c[3] << 16));
+    }
+  }
+}
+
 __device__ void write_rows(const StepParams& p, int cta, int ncta) {
+  if (p.kv_fp8) {
+    write_rows_fp8(p, cta, ncta);
+    return;
+  }
   const int n16 = p.Hkv * p.D * p.elem_bytes / 16;  // 16-byte vectors per row
   const long long nslots = (long long)p.NB * p.bs;
   const long long total = (long long)p.T * n16;
@@ -239,7 +281,7 @@ int num_sms();
 cudaError_t launch_prologue(const StepParams& p, bool plan, bool write, cudaStream_t s) {
   int write_ctas = 0;
   if (write && p.T > 0) {
-    const long long vecs = (long long)p.T * (p.Hkv * p.D * p.elem_bytes / 16);
+    const long long vecs = (long long)p.T * (p.Hkv * p.D * p.elem_bytes / 16);  // 16-byte loads
     long long want = (vecs + 1023) / 1024;
     const long long cap = 4LL * num_sms();
     write_ctas = (int)(want < cap ? want : cap);

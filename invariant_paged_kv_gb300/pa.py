@@ -16,7 +16,8 @@ import torch
 
 _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "libpa.so")
 
-PA_F32, PA_BF16 = 0, 1
+PA_F32, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
+FP8_CACHE_DTYPES = (torch.uint8, torch.float8_e4m3fn)  # e4m3 code caches
 MODES = {"batch": 0, "row": 1}  # pa_mode: PA_MODE_BATCH_INVARIANT, PA_MODE_ROW_INVARIANT
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
                 3: "PA_ERR_WORKSPACE", 4: "PA_ERR_CUDA"}
@@ -25,7 +26,8 @@ FLAGS = {
     "CU_SEQLENS": 0x10, "WORKSPACE": 0x20, "HOST_BOUND": 0x40, "TIMEOUT": 0x80,
 }
 
-EXPORTS = ("pa_write_kv", "pa_attention_workspace_bytes", "pa_attention_workspace_bytes_ex",
+EXPORTS = ("pa_write_kv", "pa_write_kv_scaled", "pa_attention_workspace_bytes",
+           "pa_attention_workspace_bytes_ex",
            "pa_attention", "pa_attention_ex", "pa_read_status", "pa_status_string",
            "pa_kernel_launches", "pa_split_tokens", "pa_attention_static_scratch")
 
@@ -55,6 +57,9 @@ def load() -> ctypes.CDLL:
     vp, i32, i64, sz, f32 = ctypes.c_void_p, ctypes.c_int32, ctypes.c_int64, ctypes.c_size_t, ctypes.c_float
     L.pa_write_kv.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, vp, vp]
     L.pa_write_kv.restype = ctypes.c_int
+    L.pa_write_kv_scaled.argtypes = [vp, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32, f32, f32,
+                                     vp, vp]
+    L.pa_write_kv_scaled.restype = ctypes.c_int
     L.pa_attention_workspace_bytes.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32, i32, i32]
     L.pa_attention_workspace_bytes.restype = sz
     L.pa_attention_workspace_bytes_ex.argtypes = [i32, i32, i32, i32, i64, i32, i32, i32, i32,
@@ -64,7 +69,7 @@ def load() -> ctypes.CDLL:
            i32, i32, f32, i32, vp, sz, vp, vp]
     L.pa_attention.argtypes = att
     L.pa_attention.restype = ctypes.c_int
-    L.pa_attention_ex.argtypes = att + [i32, ctypes.POINTER(vp), i32]
+    L.pa_attention_ex.argtypes = att + [f32, f32, i32, ctypes.POINTER(vp), i32]
     L.pa_attention_ex.restype = ctypes.c_int
     L.pa_read_status.argtypes = [vp, vp, ctypes.POINTER(i32), i32]
     L.pa_read_status.restype = ctypes.c_int
@@ -88,6 +93,17 @@ def _dtype_code(t: torch.Tensor) -> int:
     if t.dtype == torch.bfloat16:
         return PA_BF16
     raise TypeError(f"unsupported dtype {t.dtype}")
+
+
+def _cache_code(k_cache: torch.Tensor, q_dtype: torch.dtype) -> int:
+    """Element-type code of a step from its cache (e4m3 codes) or q."""
+    if k_cache.dtype in FP8_CACHE_DTYPES:
+        if q_dtype != torch.bfloat16:
+            raise TypeError("e4m3 caches take bf16 queries and new rows")
+        return PA_FP8_E4M3
+    if k_cache.dtype != q_dtype:
+        raise TypeError("caches and queries must share a dtype (or the caches hold e4m3 codes)")
+    return PA_F32 if q_dtype == torch.float32 else PA_BF16
 
 
 def _ptr(t: Optional[torch.Tensor]):
@@ -128,15 +144,19 @@ def read_status(status: torch.Tensor, stream=None, clear: bool = True) -> int:
     return int(out.value)
 
 
-def write_kv(k_new, v_new, k_cache, v_cache, slot_mapping, status=None, stream=None):
-    """pa_write_kv: scatter new rows [T, Hkv, D] into caches [NB, bs, Hkv, D]."""
+def write_kv(k_new, v_new, k_cache, v_cache, slot_mapping, status=None, stream=None,
+             k_scale: float = 1.0, v_scale: float = 1.0):
+    """pa_write_kv_scaled: scatter new rows [T, Hkv, D] into caches
+    [NB, bs, Hkv, D] (quantised under k_scale / v_scale into e4m3 caches)."""
     NB, bs, Hkv, D = k_cache.shape
     T = k_new.shape[0]
     if slot_mapping.dtype != torch.int64:
         raise TypeError("slot_mapping must be int64")
-    _check(load().pa_write_kv(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
-                              _ptr(slot_mapping), T, NB, bs, Hkv, D, _dtype_code(k_cache),
-                              _ptr(status), _stream(stream)), "pa_write_kv")
+    _check(load().pa_write_kv_scaled(_ptr(k_new), _ptr(v_new), _ptr(k_cache), _ptr(v_cache),
+                                     _ptr(slot_mapping), T, NB, bs, Hkv, D,
+                                     _cache_code(k_cache, k_new.dtype), float(k_scale),
+                                     float(v_scale), _ptr(status), _stream(stream)),
+           "pa_write_kv_scaled")
 
 
 def _mode_code(mode: str) -> int:
@@ -147,8 +167,10 @@ def _mode_code(mode: str) -> int:
 
 def workspace_bytes(B, T, max_q_len, max_ctx_len, total_ctx, H, Hkv, D, block_size,
                     dtype: torch.dtype, mode: str = "batch") -> int:
-    """pa_attention_workspace_bytes_ex for ``mode`` ("batch" or "row")."""
-    code = PA_F32 if dtype == torch.float32 else PA_BF16
+    """pa_attention_workspace_bytes_ex for ``mode`` ("batch" or "row");
+    ``dtype`` is the cache dtype (uint8 / float8_e4m3fn for e4m3 codes)."""
+    code = PA_FP8_E4M3 if dtype in FP8_CACHE_DTYPES else (
+        PA_F32 if dtype == torch.float32 else PA_BF16)
     n = int(load().pa_attention_workspace_bytes_ex(B, T, max_q_len, max_ctx_len, total_ctx, H,
                                                    Hkv, D, block_size, code, _mode_code(mode)))
     if n == 0:
@@ -159,8 +181,10 @@ def workspace_bytes(B, T, max_q_len, max_ctx_len, total_ctx, H, Hkv, D, block_si
 def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,
               max_q_len: int, max_ctx_len: int, scale: float, workspace: torch.Tensor,
               slot_mapping=None, k_new=None, v_new=None, status=None, stream=None,
-              events: Optional[Sequence[torch.cuda.Event]] = None, mode: str = "batch"):
-    """pa_attention, or pa_attention_ex when ``events`` or mode="row" is given.
+              events: Optional[Sequence[torch.cuda.Event]] = None, mode: str = "batch",
+              k_scale: float = 1.0, v_scale: float = 1.0):
+    """pa_attention, or pa_attention_ex when ``events``, mode="row" or e4m3
+    caches (uint8 / float8_e4m3fn, with k_scale and v_scale) are given.
 
     mode "batch": a row's bits depend only on its own lane. mode "row": also
     not on its lane's q_len (every row takes the split-KV path); the
@@ -177,11 +201,12 @@ def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,
     mb = block_tables.shape[1] if block_tables.dim() == 2 else 0
     args = [_ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mb, _ptr(cu_seqlens_q),
             _ptr(ctx_lens), _ptr(slot_mapping), _ptr(k_new), _ptr(v_new), _ptr(out), B, T, H,
-            Hkv, D, bs, NB, int(max_q_len), int(max_ctx_len), float(scale), _dtype_code(q),
-            _ptr(workspace), workspace.numel(), _ptr(status), _stream(stream)]
+            Hkv, D, bs, NB, int(max_q_len), int(max_ctx_len), float(scale),
+            _cache_code(k_cache, q.dtype), _ptr(workspace), workspace.numel(), _ptr(status),
+            _stream(stream)]
     L = load()
     code = _mode_code(mode)
-    if events is None and code == 0:
+    if events is None and code == 0 and k_cache.dtype not in FP8_CACHE_DTYPES:
         _check(L.pa_attention(*args), "pa_attention")
         return
     arr, n = None, 0
@@ -191,7 +216,8 @@ def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,
                 e.record(stream)
         arr = (ctypes.c_void_p * len(events))(*[ctypes.c_void_p(e.cuda_event) for e in events])
         n = len(events)
-    _check(L.pa_attention_ex(*args, code, arr, n), "pa_attention_ex")
+    _check(L.pa_attention_ex(*args, float(k_scale), float(v_scale), code, arr, n),
+           "pa_attention_ex")
 
 
 def attention_static_scratch(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,

@@ -26,7 +26,13 @@ from typing import List, Optional, Sequence
 
 import numpy as np
 
-DTYPES = ("f32", "bf16")
+DTYPES = ("f32", "bf16", "fp8")
+
+# Per-tensor scales of the synthetic e4m3 caches ("fp8" geometry): N(0, 1)
+# data over millions of elements reaches |x| ~ 5.6, and 5.6 / 448 = 0.0125;
+# V gets a slightly different scale so a K/V mix-up cannot go unseen.
+FP8_K_SCALE = 0.0125
+FP8_V_SCALE = 0.011
 
 
 class AllocatorError(RuntimeError):
@@ -112,7 +118,7 @@ class Geometry:
     Hkv: int
     D: int
     block_size: int
-    dtype: str  # "f32" | "bf16"
+    dtype: str  # "f32" | "bf16" | "fp8" (bf16 q / new rows, e4m3 code caches)
 
     def __post_init__(self):
         if self.dtype not in DTYPES:
@@ -122,6 +128,12 @@ class Geometry:
 
     @property
     def elem_bytes(self) -> int:
+        """Bytes of one cache element."""
+        return {"f32": 4, "bf16": 2, "fp8": 1}[self.dtype]
+
+    @property
+    def q_bytes(self) -> int:
+        """Bytes of one q / out / new-row element."""
         return 4 if self.dtype == "f32" else 2
 
     @property
@@ -247,10 +259,10 @@ def tiny_f32(sample: int = 0) -> Step:
     return build_step(geom, [1] * 4, ctx, 64, rng)
 
 
-def decode_batch(sample: int = 0, lanes: int = 64) -> Step:
+def decode_batch(sample: int = 0, lanes: int = 64, dtype: str = "bf16") -> Step:
     """Decode-only bf16: H32/Hkv8/D128/bs16, lognormal ctx (median 2048, sigma 1)."""
     rng = np.random.default_rng(1000 * 2 + sample)
-    geom = Geometry(32, 8, 128, 16, "bf16")
+    geom = Geometry(32, 8, 128, 16, dtype)
     ctx = np.clip(np.rint(2048.0 * np.exp(rng.standard_normal(lanes))), 16, 16384)
     ctx = ctx.astype(np.int32)
     return build_step(geom, [1] * lanes, ctx, _pool_for(ctx, 16), rng)
@@ -315,14 +327,14 @@ def invariance_step(t: int, sample: int = 0) -> (Step, int):
 
 
 def long_tail(sample: int = 0, lanes: int = 256, long_frac: float = 0.1,
-              pool_bytes_per_layer: float = 15e9) -> Step:
+              pool_bytes_per_layer: float = 15e9, dtype: str = "bf16") -> Step:
     """Long-context heavy tail bf16: H64/Hkv8/D128/bs32, 256 decode lanes.
 
     90% of lanes U{1024..4096}, 10% U{16384..40960} (230 + 26 at 256 lanes),
     order shuffled by the seed. The pool fills ``pool_bytes_per_layer`` of K+V.
     """
     rng = np.random.default_rng(1000 * 5 + sample)
-    geom = Geometry(64, 8, 128, 32, "bf16")
+    geom = Geometry(64, 8, 128, 32, dtype)
     n_long = int(round(lanes * long_frac))
     short = rng.integers(1024, 4096, size=lanes - n_long, endpoint=True)
     longs = rng.integers(16384, 40960, size=n_long, endpoint=True)
@@ -342,9 +354,11 @@ def make_tensors(step: Step, seed: int, device="cpu", layers: int = 1,
     """N(0, 1) q / caches / new rows in the step's dtype from one torch.Generator.
 
     Returns a dict with q [layers][T,H,D], k_cache / v_cache
-    [layers][NB,bs,Hkv,D], k_new / v_new [layers][T,Hkv,D].  With ``poison``
-    every cache position that is not one of the step's keys (tails of last
-    blocks and unreferenced blocks) holds NaN, so any stray read shows.
+    [layers][NB,bs,Hkv,D], k_new / v_new [layers][T,Hkv,D]; for the "fp8"
+    geometry q and new rows are bf16 and the caches uint8 e4m3 codes (scales
+    FP8_K_SCALE / FP8_V_SCALE). With ``poison`` every cache position that is
+    not one of the step's keys (tails of last blocks and unreferenced blocks)
+    holds NaN (the NaN code for e4m3), so any stray read shows.
     """
     import torch
 
@@ -353,11 +367,20 @@ def make_tensors(step: Step, seed: int, device="cpu", layers: int = 1,
     gen = torch.Generator(device=device).manual_seed(int(seed))
     out = {"q": [], "k_cache": [], "v_cache": [], "k_new": [], "v_new": []}
     T, NB = step.T, step.num_blocks
+
+    def cache(scale):
+        x = torch.randn(NB, g.block_size, g.Hkv, g.D, generator=gen, device=device, dtype=dt)
+        if g.dtype != "fp8":
+            return x
+        # e4m3 codes drawn with torch's own cast (a random-code generator
+        # here, not the library's quantiser): N(0, 1) / scale, clamped to
+        # the finite range
+        return (x.float() / scale).clamp_(-448.0, 448.0).to(torch.float8_e4m3fn).view(torch.uint8)
+
     for _ in range(layers):
         out["q"].append(torch.randn(T, g.H, g.D, generator=gen, device=device, dtype=dt))
-        for name in ("k_cache", "v_cache"):
-            out[name].append(torch.randn(NB, g.block_size, g.Hkv, g.D,
-                                         generator=gen, device=device, dtype=dt))
+        out["k_cache"].append(cache(FP8_K_SCALE))
+        out["v_cache"].append(cache(FP8_V_SCALE))
         for name in ("k_new", "v_new"):
             out[name].append(torch.randn(T, g.Hkv, g.D, generator=gen,
                                          device=device, dtype=dt))
@@ -366,7 +389,7 @@ def make_tensors(step: Step, seed: int, device="cpu", layers: int = 1,
         m = torch.from_numpy(~mask).to(device)
         for name in ("k_cache", "v_cache"):
             for c in out[name]:
-                c.view(NB * g.block_size, g.Hkv, g.D)[m] = float("nan")
+                c.view(NB * g.block_size, g.Hkv, g.D)[m] = 0x7F if g.dtype == "fp8" else float("nan")
     return out
 
 
@@ -433,12 +456,13 @@ def algorithmic_bytes(step: Step, write: bool = True) -> dict:
     written once, plus its 8-byte slot.
     """
     g = step.geom
-    e = g.elem_bytes
+    e = g.q_bytes
     bs = g.block_size
     qo = 2 * step.T * g.H * g.D * e
     bt = 4 * int(sum(-(-int(c) // bs) for c in step.ctx_lens))
     out = {"kv": kv_bytes(step), "q_out": qo, "block_table": bt}
-    out["write"] = (2 * 2 * step.T * g.kv_row_bytes + 8 * step.T) if write else 0
+    new_rows = 2 * step.T * g.Hkv * g.D * (g.q_bytes + g.elem_bytes)  # K and V: read + write
+    out["write"] = (new_rows + 8 * step.T) if write else 0
     out["decode_kernel"] = out["kv"] + step.T * g.H * g.D * e + bt
     out["total"] = out["kv"] + qo + bt + out["write"]
     return out

@@ -17,9 +17,13 @@ def device_step(step: wl.Step, device="cuda"):
     )
 
 
+def cache_torch_dtype(g: wl.Geometry):
+    return {"f32": torch.float32, "bf16": torch.bfloat16, "fp8": torch.uint8}[g.dtype]
+
+
 def workspace_for(step: wl.Step, mode="batch"):
     g = step.geom
-    dt = torch.float32 if g.dtype == "f32" else torch.bfloat16
+    dt = cache_torch_dtype(g)
     n = pa.workspace_bytes(step.B, step.T, step.max_q_len, step.max_ctx_len,
                            int(step.ctx_lens.sum()), g.H, g.Hkv, g.D, g.block_size, dt,
                            mode=mode)
@@ -44,9 +48,12 @@ def run_attention(step: wl.Step, t: dict, layer=0, write=True, scale=None, statu
                  dev["cu_seqlens_q"], dev["ctx_lens"], out,
                  max_q_len=step.max_q_len, max_ctx_len=step.max_ctx_len,
                  scale=opa.default_scale(g.D) if scale is None else scale,
-                 workspace=ws, status=st, mode=mode, **kw)
+                 workspace=ws, status=st, mode=mode, **SCALES, **kw)
     flags = pa.read_status(st)
     return out, flags
+
+
+SCALES = dict(k_scale=wl.FP8_K_SCALE, v_scale=wl.FP8_V_SCALE)
 
 
 def oracle_attention(step: wl.Step, t_cpu: dict, layer=0, write=True, rows=None, scale=None,
@@ -62,7 +69,7 @@ def oracle_attention(step: wl.Step, t_cpu: dict, layer=0, write=True, rows=None,
     return opa.attention(to_store(t_cpu["q"][layer]), kc, vc, step.block_tables,
                          step.cu_seqlens_q, step.ctx_lens,
                          opa.default_scale(g.D) if scale is None else scale, g.dtype,
-                         g.block_size, rows=rows, **kw)
+                         g.block_size, rows=rows, **SCALES, **kw)
 
 
 def to_cpu(t: dict) -> dict:
@@ -78,7 +85,7 @@ def max_abs(gpu_out: torch.Tensor, ref: np.ndarray, rows=None) -> float:
     return float(np.max(np.abs(got - ref))) if got.size else 0.0
 
 
-TOL = {"f32": 1e-5, "bf16": 2e-2}
+TOL = {"f32": 1e-5, "bf16": 2e-2, "fp8": 2e-2}
 
 
 def compact_lanes(step: wl.Step, t: dict, lanes, layer=0):

@@ -4,9 +4,10 @@ import torch
 
 
 def to_store(t: torch.Tensor) -> np.ndarray:
-    """Raw element storage: float32 stays float32, bfloat16 becomes uint16 bits."""
+    """Raw element storage: float32 stays float32, bfloat16 becomes uint16 bits,
+    e4m3 code caches (uint8) stay uint8."""
     t = t.detach().cpu().contiguous()
-    if t.dtype == torch.float32:
+    if t.dtype in (torch.float32, torch.uint8):
         return t.numpy()
     if t.dtype == torch.bfloat16:
         return t.view(torch.int16).numpy().view(np.uint16)

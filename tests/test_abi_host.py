@@ -139,7 +139,30 @@ def test_attention_ex_refuses_unknown_mode(lib):
     a = [1 << 12, 1 << 12, 1 << 12, 1 << 12, 4, 1 << 12, 1 << 12, None, None, None, 1 << 12,
          1, 1, 4, 2, 64, 16, 8, 1, 16, 0.125, 0, 1 << 12, 1 << 20, None, None]
     before = lib.pa_kernel_launches()
-    assert lib.pa_attention_ex(*a, 2, None, 0) == 1
-    assert lib.pa_attention_ex(*a, -1, None, 0) == 1
-    assert lib.pa_attention_ex(*(a[:15] + [96] + a[16:]), 1, None, 0) == 2
+    assert lib.pa_attention_ex(*a, 1.0, 1.0, 2, None, 0) == 1
+    assert lib.pa_attention_ex(*a, 1.0, 1.0, -1, None, 0) == 1
+    assert lib.pa_attention_ex(*(a[:15] + [96] + a[16:]), 1.0, 1.0, 1, None, 0) == 2
     assert lib.pa_kernel_launches() == before
+
+
+def test_e4m3_refusals_before_cuda(lib):
+    a = [1 << 12, 1 << 12, 1 << 12, 1 << 12, 4, 1 << 12, 1 << 12, None, None, None, 1 << 12,
+         1, 1, 4, 2, 64, 16, 8, 1, 16, 0.125, 2, 1 << 12, 1 << 20, None, None]
+    before = lib.pa_kernel_launches()
+    # the base entry points have no scales
+    assert lib.pa_attention(*a) == 2
+    assert lib.pa_write_kv(1 << 12, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 3, 8, 16, 2, 64, 2,
+                           None, None) == 2
+    # scales must be finite and positive
+    for ks, vs in ((0.0, 1.0), (1.0, -1.0), (float("nan"), 1.0), (1.0, float("inf"))):
+        assert lib.pa_attention_ex(*a, ks, vs, 0, None, 0) == 1
+        assert lib.pa_write_kv_scaled(1 << 12, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 3, 8, 16, 2,
+                                      64, 2, ks, vs, None, None) == 1
+    # other types ignore the scales
+    assert lib.pa_write_kv_scaled(None, None, None, None, None, 0, 8, 16, 2, 64, 1, 0.0, 0.0,
+                                  None, None) == 0
+    assert lib.pa_kernel_launches() == before
+    # workspace: e4m3 steps split every row, in either mode
+    f = lib.pa_attention_workspace_bytes_ex
+    args = (16, 600, 512, 4096, 10000, 32, 8, 128, 16, 2)
+    assert f(*args, 0) == f(*args, 1) == f(*(args[:-1] + (0,)), 0)

@@ -45,6 +45,38 @@ def test_write_kv_bit_exact(make, seed):
     assert np.array_equal(_bytes(t["v_cache"][0]), vc.view(np.uint8))
 
 
+@pytest.mark.parametrize("make,seed", [(lambda s: wl.decode_batch(s, dtype="fp8"), 2002),
+                                       (lambda s: wl.long_tail(s, lanes=24, pool_bytes_per_layer=2e8,
+                                                               dtype="fp8"), 5002)])
+def test_write_kv_e4m3_bit_exact(make, seed):
+    """New bf16 rows land in e4m3 caches as exactly the oracle's codes."""
+    step = make(0)
+    t = wl.make_tensors(step, seed, "cuda", poison=True)
+    # rows spanning the whole code range: tiny (subnormal codes), ordinary,
+    # ties, beyond 448 * scale (saturation) and exact zeros of both signs
+    g = torch.Generator(device="cuda").manual_seed(seed)
+    for name in ("k_new", "v_new"):
+        x = t[name][0]
+        mag = torch.exp2(torch.randint(-24, 6, x.shape, generator=g, device="cuda").float())
+        x.copy_((torch.randn(x.shape, generator=g, device="cuda") * mag).to(torch.bfloat16))
+        x.view(-1)[:64] = 0.0
+        x.view(-1)[64:128] = -0.0
+    slots = step.slot_mapping.copy()
+    slots[::5] = -1
+    tc = to_cpu(t)
+    pa.write_kv(t["k_new"][0], t["v_new"][0], t["k_cache"][0], t["v_cache"][0],
+                torch.from_numpy(slots).cuda(), k_scale=wl.FP8_K_SCALE, v_scale=wl.FP8_V_SCALE)
+    import oracle.e4m3 as e4m3
+    kn = e4m3.quantize_bf16(to_store(tc["k_new"][0]), wl.FP8_K_SCALE)
+    vn = e4m3.quantize_bf16(to_store(tc["v_new"][0]), wl.FP8_V_SCALE)
+    kc, vc = opa.write_kv(to_store(tc["k_cache"][0]), to_store(tc["v_cache"][0]), kn, vn, slots,
+                          step.geom.block_size)
+    assert np.array_equal(to_store(t["k_cache"][0]), kc)
+    assert np.array_equal(to_store(t["v_cache"][0]), vc)
+    # the inputs really reached saturation and subnormal codes
+    assert np.any((kn & 0x7F) == 0x7E) and np.any(((kn & 0x7F) > 0) & ((kn & 0x7F) < 8))
+
+
 def test_write_kv_flags_out_of_range_slot():
     step = wl.tiny_f32(0)
     t = wl.make_tensors(step, 5, "cuda")
@@ -108,7 +140,7 @@ def _ragged(geom, q_lens, ctx, seed, pool_extra=1.3):
 
 
 @pytest.mark.parametrize("mode", ["batch", "row"])
-@pytest.mark.parametrize("dtype", ["f32", "bf16"])
+@pytest.mark.parametrize("dtype", ["f32", "bf16", "fp8"])
 @pytest.mark.parametrize("D,bs", [(64, 16), (128, 32)])
 def test_ragged_edges(dtype, D, bs, mode):
     """ctx = 1, ctx on and off split / chunk / block edges, empty lanes, prefill chunks."""
@@ -120,10 +152,11 @@ def test_ragged_edges(dtype, D, bs, mode):
     _check_step(step, 77, mode=mode)
 
 
+@pytest.mark.parametrize("dtype", ["bf16", "fp8"])
 @pytest.mark.parametrize("H,Hkv", [(16, 1), (40, 8), (64, 4), (4, 4)])
-def test_gqa_groups_bf16(H, Hkv):
+def test_gqa_groups_bf16(H, Hkv, dtype):
     """Group sizes 16, 5, 16 and 1 (two n tiles, padded tile, MHA)."""
-    geom = wl.Geometry(H, Hkv, 128, 16, "bf16")
+    geom = wl.Geometry(H, Hkv, 128, 16, dtype)
     step = _ragged(geom, [1, 1, 1, 3], [700, 33, 1025, 80], 11)
     _check_step(step, 91)
 
@@ -139,6 +172,30 @@ def test_prefill_chunk_edges_bf16(D, bs, mode):
     ctx = [128, 300, 1000, 2, 384, 700, 64 + 191, 5]
     step = _ragged(geom, q, ctx, 21)
     _check_step(step, 211, mode=mode)
+
+
+@pytest.mark.parametrize("sample", range(2))
+def test_decode_batch_e4m3(sample):
+    """Decode-only step over e4m3 caches, all 64 lanes."""
+    _check_step(wl.decode_batch(sample, dtype="fp8"), 2100 + sample)
+
+
+@pytest.mark.parametrize("D,bs", [(128, 16), (64, 32)])
+def test_prefill_chunks_e4m3(D, bs):
+    """Prefill chunks over e4m3 caches take the split path, row by row."""
+    geom = wl.Geometry(16, 2, D, bs, "fp8")
+    q = [128, 129, 300, 2, 257, 1, 64, 1]
+    ctx = [128, 300, 1000, 2, 384, 700, 64 + 191, 5]
+    _check_step(_ragged(geom, q, ctx, 23), 213)
+
+
+def test_long_tail_e4m3_sampled():
+    """Long-context heavy tail over e4m3 caches (one layer), sampled rows."""
+    free, _ = torch.cuda.mem_get_info()
+    step = wl.long_tail(0, pool_bytes_per_layer=min(15e9, 0.4 * free), dtype="fp8")
+    order = np.argsort(step.ctx_lens)
+    rows = [int(x) for x in order[:3]] + [int(x) for x in order[-3:]] + [100, 200]
+    _check_step(step, 5100, rows=rows, poison=False)
 
 
 def test_mixed_small_full():

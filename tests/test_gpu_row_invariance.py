@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle.paged_attention as opa
-from gpu_harness import max_abs, run_attention
+from gpu_harness import SCALES, max_abs, run_attention
 from helpers import to_store
 from invariant_paged_kv_gb300 import build, pa, workload as wl
 
@@ -42,14 +42,20 @@ def _sequence(geom, P, seed, extra_blocks=7):
     dt = torch.float32 if geom.dtype == "f32" else torch.bfloat16
     g = torch.Generator(device="cuda").manual_seed(seed)
     shape = (NB, bs, geom.Hkv, geom.D)
-    kc = torch.full(shape, float("nan"), device="cuda", dtype=dt)
-    vc = torch.full(shape, float("nan"), device="cuda", dtype=dt)
     pos = np.arange(P)
     flat = torch.from_numpy(blocks[pos // bs].astype(np.int64) * bs + pos % bs).cuda()
-    kc.view(-1, geom.Hkv, geom.D)[flat] = torch.randn(P, geom.Hkv, geom.D, generator=g,
-                                                      device="cuda", dtype=dt)
-    vc.view(-1, geom.Hkv, geom.D)[flat] = torch.randn(P, geom.Hkv, geom.D, generator=g,
-                                                      device="cuda", dtype=dt)
+
+    def cache(scale):
+        x = torch.randn(P, geom.Hkv, geom.D, generator=g, device="cuda", dtype=dt)
+        if geom.dtype == "fp8":  # e4m3 codes (NaN code elsewhere)
+            c = torch.full(shape, 0x7F, device="cuda", dtype=torch.uint8)
+            x = (x.float() / scale).clamp(-448, 448).to(torch.float8_e4m3fn).view(torch.uint8)
+        else:
+            c = torch.full(shape, float("nan"), device="cuda", dtype=dt)
+        c.view(-1, geom.Hkv, geom.D)[flat] = x
+        return c
+
+    kc, vc = cache(wl.FP8_K_SCALE), cache(wl.FP8_V_SCALE)
     q = torch.randn(P, geom.H, geom.D, generator=g, device="cuda", dtype=dt)
     return NB, blocks, dict(k_cache=kc, v_cache=vc, q=q)
 
@@ -89,7 +95,7 @@ def _run_cuts(geom, NB, blocks, seq, cuts, mode, others=()):
 
 
 def _bits(x):
-    return x.view(torch.int32 if x.dtype == torch.float32 else torch.int16).cpu()
+    return x.contiguous().view(torch.int32 if x.dtype == torch.float32 else torch.int16).cpu()
 
 
 def _random_cuts(lo, hi, n, seed):
@@ -100,7 +106,8 @@ def _random_cuts(lo, hi, n, seed):
 
 
 GEOMS = [wl.Geometry(32, 8, 128, 16, "bf16"), wl.Geometry(40, 8, 128, 16, "bf16"),
-         wl.Geometry(8, 8, 64, 32, "bf16"), wl.Geometry(4, 2, 64, 16, "f32")]
+         wl.Geometry(8, 8, 64, 32, "bf16"), wl.Geometry(4, 2, 64, 16, "f32"),
+         wl.Geometry(40, 8, 128, 16, "fp8"), wl.Geometry(16, 1, 64, 32, "fp8")]
 
 
 @pytest.mark.parametrize("geom", GEOMS, ids=lambda g: f"H{g.H}kv{g.Hkv}D{g.D}bs{g.block_size}{g.dtype}")
@@ -131,7 +138,7 @@ def test_row_bits_independent_of_chunking(geom):
         q1 = to_store(seq["q"][p:p + 1].cpu())
         o, _, _ = opa.attention(q1, kc, vc, bt, np.array([0, 1], np.int32),
                                 np.array([p + 1], np.int32), opa.default_scale(geom.D),
-                                geom.dtype, geom.block_size)
+                                geom.dtype, geom.block_size, **SCALES)
         assert max_abs(ref[p:p + 1], o) <= (1e-5 if geom.dtype == "f32" else 2e-2), p
 
 

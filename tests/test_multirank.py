@@ -26,7 +26,7 @@ def _rank(rank, world, port, out):
     try:
         # every rank builds its own independent step (seed offset by rank)
         class A:
-            workload, small, layers = "decode_batch", True, None
+            workload, small, layers, kv = "decode_batch", True, None, "bf16"
         step, layers, name = bench.make_step(A, rank)
         ms_local = 1.0 + rank  # rank 1 is the slow one
         ms = bench.max_over_ranks(ms_local, world)
