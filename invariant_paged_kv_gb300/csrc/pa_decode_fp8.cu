@@ -2,12 +2,13 @@
 // paged-KV continuous-batching sampler", Review (adversarial pass), kv_dtype:
 // K/V dequantised on read; fp8 KV needs per-tensor scales).
 //
-// Same work decomposition, schedule and online softmax as the bf16 split
-// kernel -- item = (row, split, kv head), one warp per item, 16-key chunks
-// through a private ring of TMA-filled shared-memory stages -- with three
-// differences:
-//  * a chunk holds 1-byte codes, so a stage is half the bytes and the ring is
-//    twice as deep (the same bytes in flight);
+// Same work decomposition and schedule as the bf16 split kernel -- item =
+// (row, split, kv head), one warp per item, chunks of keys through a private
+// ring of TMA-filled shared-memory stages, online softmax in ascending key
+// order -- with three differences:
+//  * a chunk is 32 keys of 1-byte codes (the bytes of a 16-key bf16 chunk):
+//    its two 16-key halves give two independent S^T products per k step, and
+//    the running max, the rescale and the stage wait happen once per 32 keys;
 //  * the products run in f16: one cvt turns two codes into two f16 values
 //    exactly, and q is carried in f16 after an exact power-of-two prescale
 //    2^-k that brings the item's largest |q| below 2^15 (k is folded back
@@ -28,11 +29,12 @@ namespace pa {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kStages = 6;
+constexpr int kStages = 3;
+constexpr int kKeys = 2 * kChunk;  // keys per stage: two 16-key mma tiles
 
 template <int D>
 struct Tile8 {
-  static constexpr int kBytes = kChunk * D;           // one K (or V) chunk of codes
+  static constexpr int kBytes = kKeys * D;            // one K (or V) chunk of codes
   static constexpr int kStageBytes = 2 * kBytes;      // K + V
   static constexpr int kWarpBytes = kStages * kStageBytes;
   static constexpr int kSmemBytes = kWarps * kWarpBytes + 1024;  // + alignment slack
@@ -91,28 +93,37 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     p_blk = load_blocks(p, pi, 0, lane);
   }
   uint32_t issued = 0;
+  auto nchunks_of = [](const Item& x) { return (x.len + kKeys - 1) / kKeys; };
   auto produce = [&]() {
     if (p_item >= n_items) return;
     const int stage = issued % kStages;
-    const int off = p_chunk * kChunk;  // key offset inside the split
-    if (off / p.bs - p_w0 >= 32) {     // next window of block ids
+    const int off = p_chunk * kKeys;  // key offset inside the split (a multiple of 32)
+    if (off / p.bs - p_w0 >= 32) {    // next window of block ids
       p_w0 += 32;
       p_blk = load_blocks(p, pi, p_w0, lane);
     }
-    int blk = __shfl_sync(0xffffffffu, p_blk, off / p.bs - p_w0);
+    // the two 16-key boxes of the chunk (one block for bs = 32, two for
+    // bs = 16; off / bs is even then, so both stay inside the window)
+    int blk[2];
+#pragma unroll
+    for (int h = 0; h < 2; ++h) blk[h] = __shfl_sync(0xffffffffu, p_blk, (off + h * kChunk) / p.bs - p_w0);
     if (lane == 0) {
-      if (blk < 0 || blk >= p.NB) {
-        raise_flag(p.status, PA_FLAG_BLOCK_RANGE);
-        blk = 0;
-      }
-      const int tok = blk * p.bs + (pi.t0 + off) % p.bs;
       const uint32_t ks = wbase + stage * TL::kStageBytes;
       mbar_expect_tx(bar[stage], TL::kStageBytes);
-      tma_load_3d(ks, &tmK, 0, pi.kvh, tok, bar[stage]);
-      tma_load_3d(ks + TL::kBytes, &tmV, 0, pi.kvh, tok, bar[stage]);
+#pragma unroll
+      for (int h = 0; h < 2; ++h) {
+        int b = blk[h];
+        if (b < 0 || b >= p.NB) {
+          raise_flag(p.status, PA_FLAG_BLOCK_RANGE);
+          b = 0;
+        }
+        const int tok = b * p.bs + (pi.t0 + off + h * kChunk) % p.bs;
+        tma_load_3d(ks + h * kChunk * D, &tmK, 0, pi.kvh, tok, bar[stage]);
+        tma_load_3d(ks + TL::kBytes + h * kChunk * D, &tmV, 0, pi.kvh, tok, bar[stage]);
+      }
     }
     ++issued;
-    if (++p_chunk == pi.nchunks) {
+    if (++p_chunk == nchunks_of(pi)) {
       p_chunk = 0;
       p_w0 = 0;
       p_item = item_at(++p_k, gw, nw);
@@ -185,7 +196,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     }
 
 #pragma unroll 1
-    for (int ch = 0; ch < it.nchunks; ++ch) {
+    for (int ch = 0; ch < nchunks_of(it); ++ch) {
       const int stage = consumed % kStages;
       const uint32_t parity = (consumed / kStages) & 1u;
       const bool landed = __all_sync(0xffffffffu, mbar_wait_bounded(bar[stage], parity));
@@ -197,11 +208,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
       }
       const uint32_t ks = wbase + stage * TL::kStageBytes;
       const uint32_t vs = ks + TL::kBytes;
-      const int nvalid = min(kChunk, it.len - ch * kChunk);
-      if (nvalid < kChunk) {
+      const int nvalid = min(kKeys, it.len - ch * kKeys);
+      if (nvalid < kKeys) {
         // keys past the end: zero their V codes (a key row is one contiguous
         // run of D bytes whatever the swizzle) so 0 * stale code stays 0
-        const int nz = (kChunk - nvalid) * (D / 16);
+        const int nz = (kKeys - nvalid) * (D / 16);
         for (int i = lane; i < nz; i += 32) {
           const uint32_t a = vs + nvalid * D + i * 16;
           asm volatile("st.shared.v4.u32 [%0], {%1, %1, %1, %1};" ::"r"(a), "r"(0) : "memory");
@@ -210,52 +221,79 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         __syncwarp();
       }
 
-      // S^T = K Q^T: A rows gid and gid + 8 of the chunk, 16-byte run 4 s + tig
-      float s[NT][4];
+      // S^T = K Q^T for the two 16-key tiles: A rows 16 t + gid and
+      // 16 t + gid + 8, 16-byte run 4 sg + tig
+      float s[2][NT][4];
 #pragma unroll
-      for (int nt = 0; nt < NT; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+      for (int t = 0; t < 2; ++t)
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) s[t][nt][0] = s[t][nt][1] = s[t][nt][2] = s[t][nt][3] = 0.f;
 #pragma unroll
       for (int sg = 0; sg < SEG; ++sg) {
-        const uint4 k0 = lds128(ks + swz<D>(gid * D + 16 * (4 * sg + tig)));
-        const uint4 k1 = lds128(ks + swz<D>((gid + 8) * D + 16 * (4 * sg + tig)));
-        const uint32_t w0[4] = {k0.x, k0.y, k0.z, k0.w};
-        const uint32_t w1[4] = {k1.x, k1.y, k1.z, k1.w};
+        uint32_t w[2][2][4];  // [tile][row gid / gid + 8][word]
 #pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          const uint32_t a0 = e4m3x2_to_f16x2(w0[j]), a2 = e4m3x2_to_f16x2(w0[j] >> 16);
-          const uint32_t a1 = e4m3x2_to_f16x2(w1[j]), a3 = e4m3x2_to_f16x2(w1[j] >> 16);
+        for (int t = 0; t < 2; ++t)
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt)
-            mma_f16_16816(s[nt], a0, a1, a2, a3, qf[nt][4 * sg + j][0], qf[nt][4 * sg + j][1]);
-        }
+          for (int hr = 0; hr < 2; ++hr) {
+            const uint4 v = lds128(ks + swz<D>((16 * t + gid + 8 * hr) * D + 16 * (4 * sg + tig)));
+            w[t][hr][0] = v.x; w[t][hr][1] = v.y; w[t][hr][2] = v.z; w[t][hr][3] = v.w;
+          }
+#pragma unroll
+        for (int j = 0; j < 4; ++j)
+#pragma unroll
+          for (int t = 0; t < 2; ++t) {
+            const uint32_t a0 = e4m3x2_to_f16x2(w[t][0][j]), a2 = e4m3x2_to_f16x2(w[t][0][j] >> 16);
+            const uint32_t a1 = e4m3x2_to_f16x2(w[t][1][j]), a3 = e4m3x2_to_f16x2(w[t][1][j] >> 16);
+#pragma unroll
+            for (int nt = 0; nt < NT; ++nt)
+              mma_f16_16816(s[t][nt], a0, a1, a2, a3, qf[nt][4 * sg + j][0], qf[nt][4 * sg + j][1]);
+          }
       }
 
-      // online softmax over this chunk; this thread holds keys gid and gid + 8
-      // for heads 2 * tig and 2 * tig + 1 of each n tile
-      const bool va = gid < nvalid, vb = gid + 8 < nvalid;
-      uint32_t pb[NT][2];
+      // online softmax over the 32 keys; this thread holds keys 16 t + gid
+      // and 16 t + gid + 8 (t = 0, 1) for heads 2 tig and 2 tig + 1
+      bool vk[2][2];
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        vk[t][0] = 16 * t + gid < nvalid;
+        vk[t][1] = 16 * t + gid + 8 < nvalid;
+      }
+      uint32_t pb[2][NT][2];  // [tile][n tile][key gid / gid + 8]
       float alpha[NT][2];
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt) {
-        float pa[2], pc[2];
+        float pr[2][2][2];  // [tile][key half][head]
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float ta = va ? __fmul_rn(s[nt][e], sl2) : -INFINITY;
-          const float tb = vb ? __fmul_rn(s[nt][2 + e], sl2) : -INFINITY;
-          float mx = fmaxf(ta, tb);
+          float tv[2][2];
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr)
+              tv[t][hr] = vk[t][hr] ? __fmul_rn(s[t][nt][2 * hr + e], sl2) : -INFINITY;
+          float mx = fmaxf(fmaxf(tv[0][0], tv[0][1]), fmaxf(tv[1][0], tv[1][1]));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
           const float mn = fmaxf(m[nt][e], mx);
           alpha[nt][e] = ex2_approx(m[nt][e] - mn);
           m[nt][e] = mn;
-          pa[e] = ex2_approx(ta - mn);
-          pc[e] = ex2_approx(tb - mn);
+#pragma unroll
+          for (int t = 0; t < 2; ++t)
+#pragma unroll
+            for (int hr = 0; hr < 2; ++hr) pr[t][hr][e] = ex2_approx(tv[t][hr] - mn);
         }
-        pb[nt][0] = pack_f16x2(pa[0], pa[1]);  // key gid,     heads 2tig, 2tig+1
-        pb[nt][1] = pack_f16x2(pc[0], pc[1]);  // key gid + 8, heads 2tig, 2tig+1
-        l[nt][0] = fmaf(l[nt][0], alpha[nt][0], f16_lo(pb[nt][0]) + f16_lo(pb[nt][1]));
-        l[nt][1] = fmaf(l[nt][1], alpha[nt][1], f16_hi(pb[nt][0]) + f16_hi(pb[nt][1]));
+#pragma unroll
+        for (int t = 0; t < 2; ++t)
+#pragma unroll
+          for (int hr = 0; hr < 2; ++hr) pb[t][nt][hr] = pack_f16x2(pr[t][hr][0], pr[t][hr][1]);
+        // the chunk's weights in a fixed order: tile 0 (gid, gid + 8), tile 1
+        const float s0 = (f16_lo(pb[0][nt][0]) + f16_lo(pb[0][nt][1])) +
+                         (f16_lo(pb[1][nt][0]) + f16_lo(pb[1][nt][1]));
+        const float s1 = (f16_hi(pb[0][nt][0]) + f16_hi(pb[0][nt][1])) +
+                         (f16_hi(pb[1][nt][0]) + f16_hi(pb[1][nt][1]));
+        l[nt][0] = fmaf(l[nt][0], alpha[nt][0], s0);
+        l[nt][1] = fmaf(l[nt][1], alpha[nt][1], s1);
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           o[mt][nt][0] *= alpha[nt][0];
@@ -264,22 +302,23 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
           o[mt][nt][3] *= alpha[nt][1];
         }
       }
-      uint32_t pbt[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        pbt[nt][0] = movmatrix_trans(pb[nt][0]);
-        pbt[nt][1] = movmatrix_trans(pb[nt][1]);
-      }
 
-      // O^T += V^T P^T: m tile mt, row gid + 8 h is output dim
-      // kBPT * gid + 2 mt + h; this thread reads those kBPT bytes of keys
-      // 2tig, 2tig+1, 2tig+8 and 2tig+9
-      {
+      // O^T += V^T P^T, one 16-key tile (k step) after the other: m tile mt,
+      // row gid + 8 h is output dim kBPT * gid + 2 mt + h; this thread reads
+      // those kBPT bytes of keys 16 t + {2tig, 2tig+1, 2tig+8, 2tig+9}
+#pragma unroll
+      for (int t = 0; t < 2; ++t) {
+        uint32_t pbt[NT][2];
+#pragma unroll
+        for (int nt = 0; nt < NT; ++nt) {
+          pbt[nt][0] = movmatrix_trans(pb[t][nt][0]);
+          pbt[nt][1] = movmatrix_trans(pb[t][nt][1]);
+        }
         uint32_t vw[4][TL::kBPT / 4];
-        const int keys4[4] = {2 * tig, 2 * tig + 1, 2 * tig + 8, 2 * tig + 9};
 #pragma unroll
         for (int r = 0; r < 4; ++r) {
-          const uint32_t a = vs + swz<D>(keys4[r] * D + TL::kBPT * gid);
+          const int key = 16 * t + 2 * tig + (r & 1) + 8 * (r >> 1);
+          const uint32_t a = vs + swz<D>(key * D + TL::kBPT * gid);
           if constexpr (TL::kBPT == 16) {
             const uint4 v = lds128(a);
             vw[r][0] = v.x; vw[r][1] = v.y; vw[r][2] = v.z; vw[r][3] = v.w;
