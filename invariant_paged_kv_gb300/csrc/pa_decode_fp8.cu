@@ -29,7 +29,7 @@ namespace pa {
 namespace {
 
 constexpr int kWarps = 4;
-constexpr int kStages = 3;
+constexpr int kStages = 2;  // x 8 KB per warp; 3 CTAs per SM
 constexpr int kKeys = 2 * kChunk;  // keys per stage: two 16-key mma tiles
 
 template <int D>
@@ -51,7 +51,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t off) {
 }
 
 template <int D, int NT>
-__global__ void __launch_bounds__(kWarps * 32, 2)
+__global__ void __launch_bounds__(kWarps * 32, 3)
     decode_fp8_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
   using TL = Tile8<D>;
@@ -418,7 +418,7 @@ int num_sms();
 cudaError_t launch_decode_fp8(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
                               long long max_items, cudaStream_t s) {
   long long want = (max_items + kWarps - 1) / kWarps;
-  const long long cap = 2LL * num_sms();
+  const long long cap = 3LL * num_sms();  // 3 CTAs (12 independent warps) per SM
   int grid = (int)(want < cap ? want : cap);
   if (grid < 1) grid = 1;
   const int g = p.H / p.Hkv;
