@@ -105,6 +105,8 @@ typedef enum { PA_MODE_BATCH_INVARIANT = 0, PA_MODE_ROW_INVARIANT = 1 } pa_mode;
 #define PA_FLAG_WORKSPACE    0x20  /* the step needs more splits than the workspace holds */
 #define PA_FLAG_HOST_BOUND   0x40  /* a lane exceeds the host's max_q_len / max_ctx_len   */
 #define PA_FLAG_TIMEOUT      0x80  /* a bounded wait inside a kernel gave up              */
+#define PA_FLAG_OWNER_RANGE  0x100 /* KV-parallel key ranges not split-aligned / not a
+                                      partition of the lane's keys: lane skipped          */
 
 /*
  * pa_write_kv -- scatter T new K/V rows into the caches.
@@ -243,6 +245,77 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
                           size_t workspace_bytes, int32_t* status, void* stream,
                           float k_scale, float v_scale, pa_mode mode, void* const* events,
                           int32_t n_events);
+
+/*
+ * KV-parallel page owners ("Numerics envelopes", Layout invariance of query
+ * context parallelism: combine_attention_partials merges the partials of the
+ * KV-parallel page owners with the ordered fold; The hierarchy: a reduction
+ * is data movement plus a fixed-order fp32 fold of ranks 0..W-1).
+ *
+ * The keys of each lane are spread over W owners: owner w holds keys
+ * [bound_w, bound_{w+1}) of lane b, with bound_0 = 0, bound_W >= ctx_len and
+ * every interior bound a multiple of split_len(ctx_len) (the split length of
+ * the lane's longest row; see pa_attention), so every split of every row
+ * belongs to exactly one owner. Every row of the step (decode or prefill)
+ * takes the split path, as in PA_MODE_ROW_INVARIANT. Each owner computes the
+ * partials of its own splits into its copy of a partial buffer, the copies
+ * are gathered (an all-gather: W buffers back to back), and the merge folds
+ * every row's splits in global split order. The result is bitwise the
+ * single-owner PA_MODE_ROW_INVARIANT result, for any W and any bounds.
+ *
+ * Partial buffer (pa_partials_bytes bytes, 256-byte aligned): entry
+ * e(row, i) = base(row) + i for split i of flat row `row`, base(row) = the
+ * number of splits of all earlier rows; an entry holds (m, l) per head
+ * (float2 [H], m in the log2 domain) in the first region and acc per head
+ * (float [H][D]) in the second, both sized for T * ceil(max_ctx_len / 512)
+ * entries. Entries of splits another owner holds are left untouched.
+ */
+size_t pa_partials_bytes(int32_t T, int32_t max_ctx_len, int32_t H, int32_t D);
+
+/* Device scratch of pa_attention_partials / pa_merge_partials (their split
+ * plans); 0 for negative sizes. */
+size_t pa_partials_workspace_bytes(int32_t B, int32_t T, int32_t max_ctx_len);
+
+/*
+ * pa_attention_partials -- this owner's split partials.
+ *   key_lo, key_hi  int32 [B] (device): the keys [key_lo[b], key_hi[b]) of
+ *                   lane b this owner holds (split-aligned as above, else
+ *                   PA_FLAG_OWNER_RANGE and the lane is skipped). Only block
+ *                   table entries of those keys are read.
+ *   partials        this owner's partial buffer (partials_bytes >=
+ *                   pa_partials_bytes(T, max_ctx_len, H, D))
+ * The other arguments are pa_attention_ex's (no KV write: the owner of a new
+ * row's page writes it with pa_write_kv_scaled). out is not written.
+ */
+pa_status pa_attention_partials(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                const int32_t* key_lo, const int32_t* key_hi, int32_t B,
+                                int32_t T, int32_t H, int32_t Hkv, int32_t D,
+                                int32_t block_size, int32_t num_blocks, int32_t max_q_len,
+                                int32_t max_ctx_len, float scale, pa_dtype dtype, float k_scale,
+                                float v_scale, void* partials, size_t partials_bytes,
+                                void* workspace, size_t workspace_bytes, int32_t* status,
+                                void* stream);
+
+/*
+ * pa_merge_partials -- fold the gathered partials of W owners into out.
+ *   partials     W owner buffers of partials_bytes each, back to back (owner
+ *                w at byte w * partials_bytes), as an all-gather leaves them
+ *   key_bounds   int32 [W + 1][B] (device): row w holds bound_w of every lane
+ *   v_scale      the V scale of PA_FP8_E4M3 caches (outputs are multiplied
+ *                by it), ignored otherwise
+ * Every row's splits are folded left to right in fp32, split i read from the
+ * owner whose range holds its first key; out gets A / L (times v_scale)
+ * rounded to the q dtype. Lanes with malformed bounds set
+ * PA_FLAG_OWNER_RANGE and are skipped.
+ */
+pa_status pa_merge_partials(const void* partials, size_t partials_bytes, int32_t W,
+                            const int32_t* key_bounds, const int32_t* cu_seqlens_q,
+                            const int32_t* ctx_lens, void* out, int32_t B, int32_t T, int32_t H,
+                            int32_t D, int32_t max_q_len, int32_t max_ctx_len, pa_dtype dtype,
+                            float v_scale, void* workspace, size_t workspace_bytes,
+                            int32_t* status, void* stream);
 
 /*
  * pa_attention_static_scratch -- pa_attention for callers that cannot

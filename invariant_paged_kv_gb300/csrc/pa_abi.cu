@@ -145,6 +145,51 @@ SplitPlan carve(void* ws, int cap, int32_t B, int32_t T, int32_t H, int32_t D) {
   return pl;
 }
 
+// ---- KV-parallel partial buffers ----
+// Entries of a step's partial buffer: every row has at most
+// ceil(max_ctx_len / kSplit) splits.
+long long partial_entries(int32_t T, int32_t max_ctx_len) {
+  return (long long)T * ceil_div(max_ctx_len > 0 ? max_ctx_len : 1, kSplit);
+}
+
+size_t partials_ml_bytes(long long entries, int32_t H) {
+  return align_up((size_t)entries * H * sizeof(float2));
+}
+
+size_t partials_bytes_for(int32_t T, int32_t max_ctx_len, int32_t H, int32_t D) {
+  const long long e = partial_entries(T, max_ctx_len);
+  return partials_ml_bytes(e, H) + align_up((size_t)e * H * D * sizeof(float));
+}
+
+// Workspace of the KV-parallel calls: the plan's fixed part and one pair
+// record per split this owner may compute (no partials: those go to the
+// caller's buffer).
+size_t partials_ws_bytes(int32_t B, int32_t T, int32_t max_ctx_len) {
+  const Layout L = layout_for(B, T, 1, 1);
+  return L.fixed + align_up((size_t)partial_entries(T, max_ctx_len) * sizeof(int4));
+}
+
+SplitPlan carve_partials(void* ws, size_t ws_bytes, void* partials, int32_t B, int32_t T,
+                         int32_t H, int32_t max_ctx_len) {
+  const Layout L = layout_for(B, T, 1, 1);
+  char* b = static_cast<char*>(ws);
+  SplitPlan pl;
+  pl.header = reinterpret_cast<int*>(b + L.header);
+  pl.row_info = reinterpret_cast<int4*>(b + L.row_info);
+  pl.ptiles = reinterpret_cast<int4*>(b + L.ptiles);
+  pl.ptiles_tmp = reinterpret_cast<int4*>(b + L.ptiles_tmp);
+  pl.ptile_capacity = L.ptile_capacity;
+  pl.pairs = reinterpret_cast<int4*>(b + L.pairs);
+  long long cap = ws_bytes > L.fixed ? (long long)((ws_bytes - L.fixed) / sizeof(int4)) : 0;
+  pl.capacity = (int)(cap > 0x7fffffffLL ? 0x7fffffffLL : cap);
+  const long long e = partial_entries(T, max_ctx_len);
+  char* pb = static_cast<char*>(partials);
+  pl.ml = reinterpret_cast<float2*>(pb);
+  pl.acc = reinterpret_cast<float*>(pb + partials_ml_bytes(e, H));
+  pl.entry_capacity = e;
+  return pl;
+}
+
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
   static std::once_flag once;
@@ -434,6 +479,158 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
                          num_blocks, max_q_len, max_ctx_len, scale, dtype, workspace,
                          workspace_bytes, status, stream, 1.f, 1.f, PA_MODE_BATCH_INVARIANT,
                          nullptr, 0);
+}
+
+size_t pa_partials_bytes(int32_t T, int32_t max_ctx_len, int32_t H, int32_t D) {
+  if (T < 0 || max_ctx_len < 0 || H <= 0 || (D != 64 && D != 128)) return 0;
+  return partials_bytes_for(T > 0 ? T : 1, max_ctx_len, H, D);
+}
+
+size_t pa_partials_workspace_bytes(int32_t B, int32_t T, int32_t max_ctx_len) {
+  if (B < 0 || T < 0 || max_ctx_len < 0) return 0;
+  return partials_ws_bytes(B, T, max_ctx_len);
+}
+
+pa_status pa_attention_partials(const void* q, const void* k_cache, const void* v_cache,
+                                const int32_t* block_tables, int32_t max_blocks_per_seq,
+                                const int32_t* cu_seqlens_q, const int32_t* ctx_lens,
+                                const int32_t* key_lo, const int32_t* key_hi, int32_t B,
+                                int32_t T, int32_t H, int32_t Hkv, int32_t D,
+                                int32_t block_size, int32_t num_blocks, int32_t max_q_len,
+                                int32_t max_ctx_len, float scale, pa_dtype dtype, float k_scale,
+                                float v_scale, void* partials, size_t partials_bytes,
+                                void* workspace, size_t workspace_bytes, int32_t* status,
+                                void* stream) {
+  if (B < 0 || T < 0 || num_blocks <= 0 || max_q_len < 0 || max_ctx_len < 0)
+    return PA_ERR_INVALID_ARG;
+  pa_status g = check_geometry(H, Hkv, D, block_size, dtype);
+  if (g != PA_OK) return g;
+  if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
+  const bool fp8 = dtype == PA_FP8_E4M3;
+  if (fp8 && !scales_ok(k_scale, v_scale)) return PA_ERR_INVALID_ARG;
+  if ((long long)num_blocks * block_size > 0x7fffffffLL) return PA_ERR_UNSUPPORTED;
+  if (T > 0 && B == 0) return PA_ERR_INVALID_ARG;
+  if (T == 0 || B == 0) return PA_OK;
+  if (!q || !k_cache || !v_cache || !block_tables || !cu_seqlens_q || !ctx_lens || !key_lo ||
+      !key_hi || max_blocks_per_seq <= 0)
+    return PA_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k_cache) || !aligned16(v_cache)) return PA_ERR_INVALID_ARG;
+  if (!partials || (reinterpret_cast<uintptr_t>(partials) & (kAlign - 1)) ||
+      partials_bytes < partials_bytes_for(T, max_ctx_len, H, D))
+    return PA_ERR_WORKSPACE;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) ||
+      workspace_bytes < partials_ws_bytes(B, T, max_ctx_len))
+    return PA_ERR_WORKSPACE;
+
+  StepParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.q = q;
+  p.k_cache = k_cache;
+  p.v_cache = v_cache;
+  p.block_tables = block_tables;
+  p.cu_seqlens = cu_seqlens_q;
+  p.ctx_lens = ctx_lens;
+  p.status = status;
+  p.max_blocks = max_blocks_per_seq;
+  p.B = B;
+  p.T = T;
+  p.H = H;
+  p.Hkv = Hkv;
+  p.D = D;
+  p.bs = block_size;
+  p.NB = num_blocks;
+  p.max_q_len = max_q_len;
+  p.max_ctx_len = max_ctx_len;
+  p.elem_bytes = elem_bytes_of(dtype);
+  p.split_all_rows = 1;
+  p.scale = scale;
+  p.scale_log2 = scale * 1.4426950408889634f;
+  p.kv_fp8 = fp8 ? 1 : 0;
+  p.k_scale = fp8 ? k_scale : 1.f;
+  p.v_scale = fp8 ? v_scale : 1.f;
+  p.out_scale = p.v_scale;
+  if (fp8) p.scale_log2 *= k_scale;
+  p.partials_mode = 1;
+  p.key_lo = key_lo;
+  p.key_hi = key_hi;
+  p.plan = carve_partials(workspace, workspace_bytes, partials, B, T, H, max_ctx_len);
+
+  CUtensorMap tmK, tmV;
+  if (fp8) {
+    if (!encode_code_map(&tmK, k_cache, num_blocks, block_size, Hkv, D) ||
+        !encode_code_map(&tmV, v_cache, num_blocks, block_size, Hkv, D))
+      return PA_ERR_CUDA;
+  } else if (dtype == PA_BF16) {
+    if (!encode_cache_map(&tmK, k_cache, num_blocks, block_size, Hkv, D) ||
+        !encode_cache_map(&tmV, v_cache, num_blocks, block_size, Hkv, D))
+      return PA_ERR_CUDA;
+  }
+  long long items = partial_entries(T, max_ctx_len);
+  if (items > p.plan.capacity) items = p.plan.capacity;
+  items *= Hkv;
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_prologue(p, true, false, s) != cudaSuccess) return PA_ERR_CUDA;
+  count_launches(1);
+  cudaError_t e = fp8 ? launch_decode_fp8(p, tmK, tmV, items, s)
+                      : dtype == PA_BF16 ? launch_decode_bf16(p, tmK, tmV, items, s)
+                                         : launch_split_f32(p, items, s);
+  if (e != cudaSuccess) return PA_ERR_CUDA;
+  count_launches(1);
+  return PA_OK;
+}
+
+pa_status pa_merge_partials(const void* partials, size_t partials_bytes, int32_t W,
+                            const int32_t* key_bounds, const int32_t* cu_seqlens_q,
+                            const int32_t* ctx_lens, void* out, int32_t B, int32_t T, int32_t H,
+                            int32_t D, int32_t max_q_len, int32_t max_ctx_len, pa_dtype dtype,
+                            float v_scale, void* workspace, size_t workspace_bytes,
+                            int32_t* status, void* stream) {
+  if (B < 0 || T < 0 || W <= 0 || max_q_len < 0 || max_ctx_len < 0) return PA_ERR_INVALID_ARG;
+  pa_status g = check_geometry(H, H, D, 16, dtype);
+  if (g != PA_OK) return g;
+  const bool fp8 = dtype == PA_FP8_E4M3;
+  if (fp8 && !scales_ok(1.f, v_scale)) return PA_ERR_INVALID_ARG;
+  if (T > 0 && B == 0) return PA_ERR_INVALID_ARG;
+  if (T == 0 || B == 0) return PA_OK;
+  if (!partials || !key_bounds || !cu_seqlens_q || !ctx_lens || !out) return PA_ERR_INVALID_ARG;
+  if (!aligned16(out)) return PA_ERR_INVALID_ARG;
+  if ((reinterpret_cast<uintptr_t>(partials) & (kAlign - 1)) || (partials_bytes & (kAlign - 1)) ||
+      partials_bytes < partials_bytes_for(T, max_ctx_len, H, D))
+    return PA_ERR_WORKSPACE;
+  if (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) ||
+      workspace_bytes < partials_ws_bytes(B, T, max_ctx_len))
+    return PA_ERR_WORKSPACE;
+
+  StepParams p;
+  std::memset(&p, 0, sizeof(p));
+  p.out = out;
+  p.cu_seqlens = cu_seqlens_q;
+  p.ctx_lens = ctx_lens;
+  p.status = status;
+  p.max_blocks = 0x7fffffff / 32;  // no block table here; the ctx range check is moot
+  p.B = B;
+  p.T = T;
+  p.H = H;
+  p.Hkv = H;
+  p.D = D;
+  p.bs = 32;
+  p.max_q_len = max_q_len;
+  p.max_ctx_len = max_ctx_len;
+  p.elem_bytes = elem_bytes_of(dtype);
+  p.split_all_rows = 1;
+  p.out_scale = fp8 ? v_scale : 1.f;
+  p.partials_mode = 2;
+  p.key_bounds = key_bounds;
+  p.owners = W;
+  p.owner_stride = (long long)partials_bytes;
+  p.plan = carve_partials(workspace, workspace_bytes, const_cast<void*>(partials), B, T, H,
+                          max_ctx_len);
+  cudaStream_t s = static_cast<cudaStream_t>(stream);
+  if (launch_prologue(p, true, false, s) != cudaSuccess) return PA_ERR_CUDA;
+  count_launches(1);
+  if (launch_combine(p, s) != cudaSuccess) return PA_ERR_CUDA;
+  count_launches(1);
+  return PA_OK;
 }
 
 pa_status pa_read_status(int32_t* status, void* stream, int32_t* flags_out, int32_t clear) {

@@ -35,10 +35,20 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p
   const int h = blockIdx.y * kWarps + warp;
   if (h >= p.H) return;
   const int4 info = p.plan.row_info[row];
-  if (info.w < 0 || info.z <= 1) return;  // not on the split path, or written directly
+  if (info.w < 0) return;                                  // not on the split path
+  if (p.partials_mode != 2 && info.z <= 1) return;         // written directly
   const int n = info.z;
   const int nfull = info.y >= 0 ? n - 1 : n;
   const Vec* acc = reinterpret_cast<const Vec*>(p.plan.acc);
+  // merge of KV-parallel owners: split i comes from the owner whose key
+  // range holds its first key; its entry is info.x + i in that owner's buffer
+  const int sl = p.partials_mode == 2 ? split_len(info.y) : 0;
+  auto owner_of = [&](int i) {
+    int w = 0;
+    const long long k0 = (long long)i * sl;
+    while (w + 1 < p.owners && p.key_bounds[(size_t)(w + 1) * p.B + info.w] <= k0) ++w;
+    return w;
+  };
 
   Fold f;
   float A[VPL];
@@ -51,9 +61,20 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p
     for (int u = 0; u < kAhead; ++u) {
       const int i = i0 + u;
       if (i < n) {
-        const int pair = i < nfull ? info.x + i : info.y;
-        ml[u] = p.plan.ml[(size_t)pair * p.H + h];
-        a[u] = acc[((size_t)pair * p.H + h) * 32 + lane];
+        if (p.partials_mode == 2) {
+          const long long e = (long long)info.x + i;
+          const size_t off = (size_t)owner_of(i) * (size_t)p.owner_stride;
+          const float2* mlw = reinterpret_cast<const float2*>(
+              reinterpret_cast<const char*>(p.plan.ml) + off);
+          const Vec* accw = reinterpret_cast<const Vec*>(
+              reinterpret_cast<const char*>(p.plan.acc) + off);
+          ml[u] = mlw[(size_t)e * p.H + h];
+          a[u] = accw[((size_t)e * p.H + h) * 32 + lane];
+        } else {
+          const int pair = i < nfull ? info.x + i : info.y;
+          ml[u] = p.plan.ml[(size_t)pair * p.H + h];
+          a[u] = acc[((size_t)pair * p.H + h) * 32 + lane];
+        }
       }
     }
 #pragma unroll

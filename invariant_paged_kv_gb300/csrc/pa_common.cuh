@@ -58,6 +58,7 @@ struct SplitPlan {
   float* acc;
   int capacity;        // pairs the workspace holds
   int ptile_capacity;  // prefill tiles the workspace holds
+  long long entry_capacity;  // KV-parallel modes: entries the partial buffer holds
 };
 
 // Slot of the k-th pair in work order: full pairs from the front of the
@@ -91,8 +92,27 @@ struct StepParams {
   float scale_log2;  // scale * log2(e) (* k_scale for e4m3 caches): base-2 score domain
   float k_scale, v_scale;  // per-tensor scales of e4m3 caches (1 otherwise)
   float out_scale;   // factor on every normalised output: v_scale for e4m3, else 1
+  // KV-parallel page owners: 0 = an ordinary step; 1 = this owner's partials
+  // (splits whose first key lies in [key_lo, key_hi) of the lane) written to
+  // canonical entries row_info[row].x + split of the plan's ml / acc;
+  // 2 = merge: fold every row's splits, split i read from the owner whose
+  // range [key_bounds[w][lane], key_bounds[w + 1][lane]) holds its first key.
+  // In modes 1 and 2 row_info[row] = {first entry, key count, splits, lane}.
+  int partials_mode;
+  const int* key_lo;
+  const int* key_hi;
+  const int* key_bounds;        // [owners + 1][B]
+  int owners;
+  long long owner_stride;       // bytes between owners' buffers
   SplitPlan plan;
 };
+
+// Canonical partial entry of (row, split) in the KV-parallel modes, else the
+// pair's own slot.
+__device__ __forceinline__ long long partial_entry(const StepParams& p, int pair, int row,
+                                                   int split) {
+  return p.partials_mode ? (long long)p.plan.row_info[row].x + split : (long long)pair;
+}
 
 // Opt a kernel in to `bytes` of dynamic shared memory once per device (the
 // attribute is per device and sticky; later calls only read a flag).

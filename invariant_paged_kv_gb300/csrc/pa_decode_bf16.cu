@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         l[nt][e] = v;
       }
     }
-    const bool single = it.single;
+    const bool single = it.single && !p.partials_mode;
     const size_t head0 = (size_t)it.row * p.H + (size_t)it.kvh * g;  // first head of the group
     if (single) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
@@ -296,7 +296,9 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
           }
         }
     } else {
-      const size_t ph0 = (size_t)it.pair * p.H + (size_t)it.kvh * g;
+      const size_t ph0 =
+          (size_t)partial_entry(p, it.pair, it.row, it.t0 / split_len(it.keys)) * p.H +
+          (size_t)it.kvh * g;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
 #pragma unroll

@@ -22,6 +22,28 @@ namespace pa {
 
 namespace {
 
+// KV-parallel key ranges of lane b (ctx c): this owner's [key_lo, key_hi)
+// in mode 1, the owners' partition in mode 2. Interior bounds must be
+// multiples of split_len(c), the split length of the lane's longest row (a
+// multiple of every shorter row's), so no split straddles two owners.
+__device__ bool owner_ranges_bad(const StepParams& p, int b, int c) {
+  const int sl = split_len(c > 0 ? c : 1);
+  auto aligned = [&](long long x) { return x >= c || x % sl == 0; };
+  if (p.partials_mode == 1) {
+    const long long lo = p.key_lo[b], hi = p.key_hi[b];
+    return lo < 0 || hi < lo || !aligned(lo) || !aligned(hi);
+  }
+  const int W = p.owners;
+  long long prev = p.key_bounds[b];
+  if (prev != 0) return true;
+  for (int w = 1; w <= W; ++w) {
+    const long long x = p.key_bounds[(size_t)w * p.B + b];
+    if (x < prev || !aligned(x)) return true;
+    prev = x;
+  }
+  return prev < c;
+}
+
 // Validates lane b (raising status flags when `report`) and returns whether
 // it is well formed; q, c, cu0 are its q_len, ctx_len and first row.
 __device__ bool lane_valid(const StepParams& p, int b, bool report, int& q, int& c, int& cu0) {
@@ -81,6 +103,23 @@ __device__ void block_scan4(const long long (&v)[4], long long (&ex)[4], long lo
   __syncthreads();
 }
 
+// Splits [i0, i1) of a row (split length sl, n splits) this call computes:
+// all of them in an ordinary step, the ones whose first key lies in
+// [key_lo, key_hi) for a KV-parallel owner, none for the merge.
+__device__ __forceinline__ void owned_splits(const StepParams& p, int b, int sl, int n, int& i0,
+                                             int& i1) {
+  if (p.partials_mode == 0) {
+    i0 = 0;
+    i1 = n;
+  } else if (p.partials_mode == 1) {
+    const long long lo = p.key_lo[b], hi = p.key_hi[b];
+    i0 = (int)min((long long)n, (lo + sl - 1) / sl);
+    i1 = (int)min((long long)n, (hi + sl - 1) / sl);
+  } else {
+    i0 = i1 = 0;
+  }
+}
+
 // Two passes over the lanes (blockDim at a time); each lane's data is read
 // once per pass. Pass 1 counts full split pairs of rows with splits longer
 // than kSplit ("long"), full kSplit pairs ("short"), tail pairs and prefill
@@ -88,19 +127,33 @@ __device__ void block_scan4(const long long (&v)[4], long long (&ex)[4], long lo
 // front of the list, short full pairs after all long ones, tail pairs from
 // the back of the list, prefill tiles to a scratch list. Totals are checked
 // against the workspace; on overflow nothing runs.
+// In the KV-parallel modes the canonical entries of a lane depend on its
+// q_len and ctx_len alone (every owner and the merge lay them out alike);
+// malformed owner ranges only empty this owner's share (mode 1) or take the
+// lane's rows out of the merge (mode 2, owner_ok false).
 __device__ bool lane_counts(const StepParams& p, int b, bool report, int& q, int& c, int& cu0,
-                            long long (&cnt)[4], bool& split, bool& tiles) {
+                            long long (&cnt)[4], bool& split, bool& tiles, bool& owner_ok) {
   cnt[0] = cnt[1] = cnt[2] = cnt[3] = 0;
   split = tiles = false;
+  owner_ok = true;
   if (!lane_valid(p, b, report, q, c, cu0)) return false;
+  if (p.partials_mode && owner_ranges_bad(p, b, c)) {
+    owner_ok = false;
+    if (report) raise_flag(p.status, PA_FLAG_OWNER_RANGE);
+  }
   split = q >= 1 && (p.split_all_rows || q == 1);
   tiles = !p.split_all_rows && q >= 2;
   if (split) {  // row j attends c - q + j + 1 keys
     for (int j = 0; j < q; ++j) {
       const int keys = c - q + j + 1;
       const int sl = split_len(keys);
-      cnt[sl > kSplit ? 0 : 1] += keys / sl;
-      cnt[2] += (keys % sl) != 0;
+      const int nf = keys / sl, n = nf + ((keys % sl) != 0);
+      if (p.partials_mode) cnt[3] += n;  // canonical entries (no prefill tiles here)
+      int i0, i1;
+      owned_splits(p, b, sl, n, i0, i1);
+      if (!owner_ok) i0 = i1 = 0;
+      cnt[sl > kSplit ? 0 : 1] += max(0, min(i1, nf) - i0);
+      cnt[2] += (n > nf && n - 1 >= i0 && n - 1 < i1);
     }
   }
   if (tiles) cnt[3] = (q + kPrefillRows - 1) / kPrefillRows;
@@ -118,8 +171,8 @@ __device__ void build_plan(const StepParams& p) {
     const int b = base + tid;
     int q, c, cu0;
     long long cnt[4] = {0, 0, 0, 0};
-    bool split, tiles;
-    if (b < p.B) lane_counts(p, b, true, q, c, cu0, cnt, split, tiles);
+    bool split, tiles, owner_ok;
+    if (b < p.B) lane_counts(p, b, true, q, c, cu0, cnt, split, tiles, owner_ok);
     long long ex[4], tot[4];
     block_scan4(cnt, ex, tot);
 #pragma unroll
@@ -127,7 +180,8 @@ __device__ void build_plan(const StepParams& p) {
   }
   const int cap = pl.capacity;
   const long long nfull = total[0] + total[1];
-  const bool overflow = nfull + total[2] > cap || total[3] > pl.ptile_capacity;
+  const bool overflow = nfull + total[2] > cap ||
+                        total[3] > (p.partials_mode ? pl.entry_capacity : (long long)pl.ptile_capacity);
   if (overflow && tid == 0) raise_flag(p.status, PA_FLAG_WORKSPACE);
   __syncthreads();
 
@@ -137,27 +191,35 @@ __device__ void build_plan(const StepParams& p) {
       const int b = base + tid;
       int q = 0, c = 0, cu0 = 0;
       long long cnt[4] = {0, 0, 0, 0};
-      bool split = false, tiles = false;
-      if (b < p.B) lane_counts(p, b, false, q, c, cu0, cnt, split, tiles);
+      bool split = false, tiles = false, owner_ok = true;
+      if (b < p.B) lane_counts(p, b, false, q, c, cu0, cnt, split, tiles, owner_ok);
       long long ex[4], tot[4];
       block_scan4(cnt, ex, tot);
       if (split) {
         long long lb = carry[0] + ex[0];             // long full pairs
         long long sb = total[0] + carry[1] + ex[1];  // short full pairs
         long long tb = carry[2] + ex[2];             // tail pair k sits at cap - 1 - k
+        long long eb = carry[3] + ex[3];             // KV-parallel: the lane's first entry
         for (int j = 0; j < q; ++j) {
           const int keys = c - q + j + 1;
           const int sl = split_len(keys);
           const int nf = keys / sl;
           const bool has_tail = (keys % sl) != 0;
+          const int n = nf + (has_tail ? 1 : 0);
           const int row = cu0 + j;
           long long& fb = sl > kSplit ? lb : sb;
           const long long tslot = cap - 1 - tb;
-          pl.row_info[row] =
-              make_int4((int)fb, has_tail ? (int)tslot : -1, nf + (has_tail ? 1 : 0), b);
-          for (int i = 0; i < nf; ++i) pl.pairs[fb + i] = make_int4(row, i, b, keys);
-          fb += nf;
-          if (has_tail) {
+          int i0, i1;
+          owned_splits(p, b, sl, n, i0, i1);
+          if (!owner_ok) i0 = i1 = 0;
+          if (p.partials_mode) {
+            pl.row_info[row] = make_int4((int)eb, keys, n, owner_ok ? b : -1);
+            eb += n;
+          } else {
+            pl.row_info[row] = make_int4((int)fb, has_tail ? (int)tslot : -1, n, b);
+          }
+          for (int i = i0; i < min(i1, nf); ++i) pl.pairs[fb++] = make_int4(row, i, b, keys);
+          if (has_tail && n - 1 >= i0 && n - 1 < i1) {
             pl.pairs[tslot] = make_int4(row, nf, b, keys);
             ++tb;
           }
@@ -174,7 +236,7 @@ __device__ void build_plan(const StepParams& p) {
       for (int k = 0; k < 4; ++k) carry[k] += tot[k];
     }
   }
-  const int n = overflow ? 0 : (int)total[3];
+  const int n = (overflow || p.partials_mode) ? 0 : (int)total[3];
   __syncthreads();
   // prefill tiles heaviest first (position of the tile's last row; ties by
   // list order) when there are at most blockDim of them: the order only

@@ -84,8 +84,8 @@ __global__ void __launch_bounds__(kWarps * 32) split_f32_kernel(const StepParams
       }
     }
     float* out = static_cast<float*>(p.out);
-    const bool single = keys <= sl;
-    const size_t ph0 = (size_t)pair * p.H + (size_t)kvh * g;
+    const bool single = keys <= sl && !p.partials_mode;
+    const size_t ph0 = (size_t)partial_entry(p, pair, row, pr.y) * p.H + (size_t)kvh * g;
 #pragma unroll
     for (int h = 0; h < GMAX; ++h) {
       if (h < g) {

@@ -24,12 +24,15 @@ STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
 FLAGS = {
     "SLOT_RANGE": 0x01, "BLOCK_RANGE": 0x02, "CTX_RANGE": 0x04, "QLEN_RANGE": 0x08,
     "CU_SEQLENS": 0x10, "WORKSPACE": 0x20, "HOST_BOUND": 0x40, "TIMEOUT": 0x80,
+    "OWNER_RANGE": 0x100,
 }
 
 EXPORTS = ("pa_write_kv", "pa_write_kv_scaled", "pa_attention_workspace_bytes",
            "pa_attention_workspace_bytes_ex",
            "pa_attention", "pa_attention_ex", "pa_read_status", "pa_status_string",
-           "pa_kernel_launches", "pa_split_tokens", "pa_attention_static_scratch")
+           "pa_kernel_launches", "pa_split_tokens", "pa_attention_static_scratch",
+           "pa_partials_bytes", "pa_partials_workspace_bytes", "pa_attention_partials",
+           "pa_merge_partials")
 
 
 class PaError(RuntimeError):
@@ -83,6 +86,17 @@ def load() -> ctypes.CDLL:
                                               i32, i32, i32, i32, i32, i32, i32, i32, i64, f32,
                                               i32, vp, vp]
     L.pa_attention_static_scratch.restype = ctypes.c_int
+    L.pa_partials_bytes.argtypes = [i32, i32, i32, i32]
+    L.pa_partials_bytes.restype = sz
+    L.pa_partials_workspace_bytes.argtypes = [i32, i32, i32]
+    L.pa_partials_workspace_bytes.restype = sz
+    L.pa_attention_partials.argtypes = [vp, vp, vp, vp, i32, vp, vp, vp, vp, i32, i32, i32, i32,
+                                        i32, i32, i32, i32, i32, f32, i32, f32, f32, vp, sz, vp,
+                                        sz, vp, vp]
+    L.pa_attention_partials.restype = ctypes.c_int
+    L.pa_merge_partials.argtypes = [vp, sz, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
+                                    i32, f32, vp, sz, vp, vp]
+    L.pa_merge_partials.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -243,3 +257,62 @@ def attention_static_scratch(q, k_cache, v_cache, block_tables, cu_seqlens_q, ct
         _ptr(ctx_lens), _ptr(slot_mapping), _ptr(k_new), _ptr(v_new), _ptr(out), B, T, H, Hkv,
         D, bs, NB, int(max_q_len), int(max_ctx_len), int(total_ctx), float(scale),
         _dtype_code(q), _ptr(status), _stream(stream)), "pa_attention_static_scratch")
+
+
+# ---------------------------------------------------------------------------
+# KV-parallel page owners
+# ---------------------------------------------------------------------------
+
+def partials_bytes(T: int, max_ctx_len: int, H: int, D: int) -> int:
+    """pa_partials_bytes: one owner's partial buffer."""
+    n = int(load().pa_partials_bytes(T, max_ctx_len, H, D))
+    if n == 0:
+        raise PaError(1, "pa_partials_bytes")
+    return n
+
+
+def partials_workspace_bytes(B: int, T: int, max_ctx_len: int) -> int:
+    return int(load().pa_partials_workspace_bytes(B, T, max_ctx_len))
+
+
+def attention_partials(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, key_lo,
+                       key_hi, partials, *, max_q_len: int, max_ctx_len: int, scale: float,
+                       workspace: torch.Tensor, k_scale: float = 1.0, v_scale: float = 1.0,
+                       status=None, stream=None):
+    """pa_attention_partials: this owner's split partials into ``partials``
+    (a uint8 tensor of partials_bytes(...)); key_lo / key_hi int32 [B]."""
+    T, H, D = q.shape
+    NB, bs, Hkv, _ = k_cache.shape
+    B = ctx_lens.shape[0]
+    for t in (block_tables, cu_seqlens_q, ctx_lens, key_lo, key_hi):
+        if t.dtype != torch.int32:
+            raise TypeError("tables, lengths and key ranges must be int32")
+    mb = block_tables.shape[1] if block_tables.dim() == 2 else 0
+    _check(load().pa_attention_partials(
+        _ptr(q), _ptr(k_cache), _ptr(v_cache), _ptr(block_tables), mb, _ptr(cu_seqlens_q),
+        _ptr(ctx_lens), _ptr(key_lo), _ptr(key_hi), B, T, H, Hkv, D, bs, NB, int(max_q_len),
+        int(max_ctx_len), float(scale), _cache_code(k_cache, q.dtype), float(k_scale),
+        float(v_scale), _ptr(partials), partials.numel(), _ptr(workspace), workspace.numel(),
+        _ptr(status), _stream(stream)), "pa_attention_partials")
+
+
+def merge_partials(gathered, owners: int, key_bounds, cu_seqlens_q, ctx_lens, out, *,
+                   max_q_len: int, max_ctx_len: int, workspace: torch.Tensor,
+                   kv_dtype: torch.dtype = None, v_scale: float = 1.0, status=None,
+                   stream=None):
+    """pa_merge_partials: fold the owners' gathered buffers (uint8,
+    owners x partials_bytes, back to back) into out [T, H, D];
+    key_bounds int32 [owners + 1, B]; kv_dtype is the caches' dtype."""
+    T, H, D = out.shape
+    B = ctx_lens.shape[0]
+    if key_bounds.dtype != torch.int32 or tuple(key_bounds.shape) != (owners + 1, B):
+        raise TypeError("key_bounds must be int32 [owners + 1, B]")
+    if gathered.numel() % owners:
+        raise ValueError("gathered buffer is not owners equal parts")
+    code = PA_FP8_E4M3 if kv_dtype in FP8_CACHE_DTYPES else (
+        PA_F32 if out.dtype == torch.float32 else PA_BF16)
+    _check(load().pa_merge_partials(
+        _ptr(gathered), gathered.numel() // owners, owners, _ptr(key_bounds),
+        _ptr(cu_seqlens_q), _ptr(ctx_lens), _ptr(out), B, T, H, D, int(max_q_len),
+        int(max_ctx_len), code, float(v_scale), _ptr(workspace), workspace.numel(),
+        _ptr(status), _stream(stream)), "pa_merge_partials")

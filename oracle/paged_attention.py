@@ -215,6 +215,56 @@ def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens,
     return out, k_cache, v_cache
 
 
+# ---------------------------------------------------------------------------
+# partials and their ordered fold (KV-parallel page owners)
+# ---------------------------------------------------------------------------
+
+def split_length(keys: int, base: int = 512, max_splits: int = 128) -> int:
+    """Keys per split of a row with ``keys`` keys: base * 2^j for the smallest
+    j that leaves at most ``max_splits`` splits (a function of the row's own
+    key count only: "Numerics envelopes", The hierarchy, invariance.batch, no
+    split count that scales with batch or occupancy)."""
+    s = base
+    while -(-keys // s) > max_splits:
+        s *= 2
+    return s
+
+
+def split_starts(keys: int):
+    """First key of every split of a row with ``keys`` keys."""
+    s = split_length(keys)
+    return list(range(0, keys, s))
+
+
+def row_partial(q_row, K, V, lo: int, hi: int, scale: float, h: int):
+    """Unnormalised softmax partial of head h over keys [lo, hi), float64:
+    m = max s_i, l = sum exp(s_i - m), acc = sum exp(s_i - m) V_i."""
+    H = q_row.shape[0]
+    kv = kv_head_of(h, H, K.shape[1])
+    s = scale * (K[lo:hi, kv, :] @ q_row[h])
+    m = float(np.max(s))
+    e = np.exp(s - m)
+    return m, float(np.sum(e)), e @ V[lo:hi, kv, :]
+
+
+def fold_partials(parts):
+    """Ordered fold of partials (m_i, l_i, acc_i), i = 0, 1, ... in list
+    order ("Numerics envelopes", The hierarchy: a reduction is data movement
+    plus a fixed-order fold of ranks 0..W-1; Layout invariance of query
+    context parallelism: combine_attention_partials merges the partials of
+    KV-parallel page owners with that fold): M, L, A from the first; for each
+    next M' = max(M, m), L = L e^(M - M') + l e^(m - M'), A likewise; the
+    result is A / L."""
+    M, L, A = parts[0][0], parts[0][1], np.array(parts[0][2], dtype=np.float64)
+    for m, l, a in parts[1:]:
+        Mn = max(M, m)
+        ea, eb = math.exp(M - Mn), math.exp(m - Mn)
+        L = L * ea + l * eb
+        A = A * ea + np.asarray(a, dtype=np.float64) * eb
+        M = Mn
+    return A / L
+
+
 def default_scale(D: int) -> float:
     """1/sqrt(D) rounded to float32, the scale the workloads use."""
     return float(np.float32(1.0 / math.sqrt(D)))

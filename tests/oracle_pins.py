@@ -24,6 +24,10 @@ What pins what:
                              float8_e4m3fn cast (inside the finite range)
   * fp8 brute force       -> fp8 paged oracle == codes read by torch, scaled,
                              scipy softmax on the unpaged sequence
+  * split length          -> its defining property (fewest splits <= 128 with
+                             the shortest length 512 * 2^j) and named values
+  * fold of partials      -> any key partition folds back to the row's
+                             attention (1e-12); one partial folds to acc / l
 """
 import json
 import math
@@ -425,11 +429,53 @@ def check_fp8_brute_force():
     return None
 
 
+def check_split_length():
+    cases = {1: 512, 512: 512, 65536: 512, 65537: 1024, 131072: 1024, 131073: 2048,
+             10 ** 6: 8192}
+    for keys, want in cases.items():
+        if pa.split_length(keys) != want:
+            return f"split_length({keys}) = {pa.split_length(keys)}, want {want}"
+    for keys in (1, 7, 513, 40000, 70000, 300000, 2 ** 21 + 3):
+        s = pa.split_length(keys)
+        if -(-keys // s) > 128 or (s > 512 and -(-keys // (s // 2)) <= 128):
+            return f"split_length({keys}) = {s} is not the smallest length with <= 128 splits"
+        st = pa.split_starts(keys)
+        if st[0] != 0 or any(b - a != s for a, b in zip(st, st[1:])) or st[-1] >= keys:
+            return f"split_starts({keys}) do not tile the row"
+    return None
+
+
+def check_fold_partials():
+    """Folding the partials of any partition of a row's keys, in key order,
+    gives the row's attention (a partition-independence identity of softmax)."""
+    rng = np.random.default_rng(91)
+    H, Hkv, D = 6, 2, 16
+    for L in (1, 2, 9, 700):
+        K = rng.standard_normal((L, Hkv, D)) * 2.0
+        V = rng.standard_normal((L, Hkv, D))
+        q = rng.standard_normal((H, D))
+        want = pa.attend_row(q, K, V, L - 1, 0.3)
+        for cuts in ([0, L], sorted(set([0, L] + list(rng.integers(1, max(L, 2), size=3))))):
+            cuts = [c for c in cuts if 0 <= c <= L]
+            for h in range(H):
+                parts = [pa.row_partial(q, K, V, a, b, 0.3, h) for a, b in zip(cuts, cuts[1:])
+                         if b > a]
+                got = pa.fold_partials(parts)
+                if np.max(np.abs(got - want[h])) > 1e-12:
+                    return f"fold of partials over cuts {cuts} differs from the row's attention"
+        # a single partial folds to acc / l
+        m, l, a = pa.row_partial(q, K, V, 0, L, 0.3, 0)
+        if not np.array_equal(pa.fold_partials([(m, l, a)]), a / l):
+            return "a single partial does not fold to acc / l"
+    return None
+
+
 ALL_CHECKS = [check_single_key, check_zero_query_mean, check_position_code,
               check_constant_v_per_head, check_one_hot, check_brute_force,
               check_block_permutation, check_weights_sum, check_write_bytes,
               check_kv_bytes_golden, check_e4m3_values_golden, check_e4m3_nearest,
-              check_e4m3_scaled_quantize, check_fp8_brute_force]
+              check_e4m3_scaled_quantize, check_fp8_brute_force, check_split_length,
+              check_fold_partials]
 
 
 def failures():

@@ -166,3 +166,28 @@ def test_e4m3_refusals_before_cuda(lib):
     f = lib.pa_attention_workspace_bytes_ex
     args = (16, 600, 512, 4096, 10000, 32, 8, 128, 16, 2)
     assert f(*args, 0) == f(*args, 1) == f(*(args[:-1] + (0,)), 0)
+
+
+def test_kv_parallel_refusals_before_cuda(lib):
+    before = lib.pa_kernel_launches()
+    pb = lib.pa_partials_bytes(64, 4096, 32, 128)
+    assert pb >= 64 * 8 * 32 * (128 + 2) * 4 and pb % 256 == 0
+    assert lib.pa_partials_bytes(64, 4096, 32, 96) == 0
+    ws = lib.pa_partials_workspace_bytes(8, 64, 4096)
+    assert ws > 64 * 8 * 16
+    base = [1 << 12, 1 << 12, 1 << 12, 1 << 12, 4, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 1, 1, 4,
+            2, 64, 16, 8, 1, 16, 0.125, 0, 1.0, 1.0, 1 << 12, 1 << 20, 1 << 12, 1 << 20, None,
+            None]
+    f = lib.pa_attention_partials
+    assert f(*(base[:7] + [None] + base[8:])) == 1          # key_lo missing
+    assert f(*(base[:13] + [96] + base[14:])) == 2          # D unsupported
+    assert f(*(base[:22] + [(1 << 12) + 16] + base[23:])) == 3  # partials misaligned
+    assert f(*(base[:23] + [64] + base[24:])) == 3          # partials too small
+    assert f(*(base[:25] + [16] + base[26:])) == 3          # workspace too small
+    m = lib.pa_merge_partials
+    mb = [1 << 12, 1 << 20, 2, 1 << 12, 1 << 12, 1 << 12, 1 << 12, 1, 1, 4, 64, 1, 16, 0, 1.0,
+          1 << 12, 1 << 20, None, None]
+    assert m(*(mb[:2] + [0] + mb[3:])) == 1                  # no owners
+    assert m(*(mb[:3] + [None] + mb[4:])) == 1               # no bounds
+    assert m(*(mb[:1] + [1 << 20 | 8] + mb[2:])) == 3        # owner stride not 256-aligned
+    assert lib.pa_kernel_launches() == before

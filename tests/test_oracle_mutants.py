@@ -9,6 +9,8 @@ from the chunk start), and for the e4m3 cache format: exponent bias off by
 one, subnormals read as normals, truncation instead of rounding, ties away
 from zero, no saturation, the scale ignored or applied the wrong way.
 """
+import math
+
 import numpy as np
 import pytest
 
@@ -127,6 +129,42 @@ def _dequantize_ignores_scale(codes, scale):
 
 def _quantize_multiplies(bits, scale):
     return _orig_encode((e4m3.bf16_bits_to_f32(bits) * np.float32(scale)).astype(np.float32))
+
+
+_orig_fold = pa.fold_partials
+
+
+def _fold_unordered_max(parts):
+    # uses the last partial's max as the reference without rescaling the others
+    M = parts[-1][0]
+    L = sum(l * math.exp(m - M) for m, l, _ in parts[:-1]) + parts[-1][1]
+    A = sum(np.asarray(a) for _, _, a in parts)
+    return A / L
+
+
+def _fold_drops_first(parts):
+    return _orig_fold(parts[1:] if len(parts) > 1 else parts)
+
+
+def _split_length_off(keys, base=512, max_splits=128):
+    s = base
+    while -(-keys // s) >= max_splits:
+        s *= 2
+    return s
+
+
+FOLD_MUTANTS = {
+    "fold forgets to rescale": ("fold_partials", _fold_unordered_max),
+    "fold drops the first partial": ("fold_partials", _fold_drops_first),
+    "split length off by one split": ("split_length", _split_length_off),
+}
+
+
+@pytest.mark.parametrize("name", sorted(FOLD_MUTANTS))
+def test_fold_mutant_is_caught(name, monkeypatch):
+    attr, fn = FOLD_MUTANTS[name]
+    monkeypatch.setattr(pa, attr, fn)
+    assert oracle_pins.failures(), f"no pin caught the mutant '{name}'"
 
 
 E4M3_MUTANTS = {
