@@ -28,6 +28,8 @@ What pins what:
                              the shortest length 512 * 2^j) and named values
   * fold of partials      -> any key partition folds back to the row's
                              attention (1e-12); one partial folds to acc / l
+  * decode linear         -> explicit triple loops on small shapes; identity
+                             weights return x
 """
 import json
 import math
@@ -37,6 +39,7 @@ import numpy as np
 import scipy.special
 import torch
 
+import oracle.decode_gemm as dg
 import oracle.e4m3 as e4m3
 import oracle.paged_attention as pa
 from helpers import as_f64, to_store
@@ -470,12 +473,37 @@ def check_fold_partials():
     return None
 
 
+def check_decode_gemm_brute_force():
+    """The decode linear layer against explicit loops (and torch's own bf16
+    widening) on small shapes; identity weights return x exactly."""
+    g = torch.Generator().manual_seed(101)
+    for T, N, K in ((1, 1, 1), (3, 5, 7), (4, 8, 16)):
+        x = torch.randn(T, K, generator=g).to(torch.bfloat16)
+        w = torch.randn(N, K, generator=g).to(torch.bfloat16)
+        got = dg.linear(to_store(x), to_store(w))
+        xf, wf = as_f64(x), as_f64(w)
+        for t in range(T):
+            for n in range(N):
+                acc = 0.0
+                for k in range(K):
+                    acc += xf[t, k] * wf[n, k]
+                if abs(got[t, n] - acc) > 1e-12 * max(1.0, abs(acc)):
+                    return f"decode linear [{T}x{K}]x[{N}x{K}]^T differs from loops at ({t},{n})"
+        if got.shape != (T, N):
+            return "decode linear has the wrong shape"
+    x = torch.randn(3, 8, generator=g).to(torch.bfloat16)
+    eye = torch.eye(8).to(torch.bfloat16)
+    if not np.array_equal(dg.linear(to_store(x), to_store(eye)), as_f64(x)):
+        return "identity weights do not return x"
+    return None
+
+
 ALL_CHECKS = [check_single_key, check_zero_query_mean, check_position_code,
               check_constant_v_per_head, check_one_hot, check_brute_force,
               check_block_permutation, check_weights_sum, check_write_bytes,
               check_kv_bytes_golden, check_e4m3_values_golden, check_e4m3_nearest,
               check_e4m3_scaled_quantize, check_fp8_brute_force, check_split_length,
-              check_fold_partials]
+              check_fold_partials, check_decode_gemm_brute_force]
 
 
 def failures():

@@ -14,6 +14,7 @@ import math
 import numpy as np
 import pytest
 
+import oracle.decode_gemm as dg
 import oracle.e4m3 as e4m3
 import oracle.paged_attention as pa
 import oracle_pins
@@ -158,6 +159,36 @@ FOLD_MUTANTS = {
     "fold drops the first partial": ("fold_partials", _fold_drops_first),
     "split length off by one split": ("split_length", _split_length_off),
 }
+
+
+_orig_linear = dg.linear
+
+
+def _linear_k_reversed(x_bits, w_bits):
+    return dg.widen_bf16(x_bits) @ dg.widen_bf16(w_bits)[:, ::-1].T
+
+
+def _linear_drops_last_k(x_bits, w_bits):
+    return _orig_linear(np.asarray(x_bits)[:, :-1], np.asarray(w_bits)[:, :-1])
+
+
+def _linear_wrong_widening(x_bits, w_bits):
+    x = (np.asarray(x_bits).astype(np.uint32) << np.uint32(15)).view(np.float32).astype(np.float64)
+    return x @ dg.widen_bf16(w_bits).T
+
+
+GEMM_MUTANTS = {
+    "gemm pairs x and w along reversed k": ("linear", _linear_k_reversed),
+    "gemm drops the last k": ("linear", _linear_drops_last_k),
+    "gemm widens x with the wrong shift": ("linear", _linear_wrong_widening),
+}
+
+
+@pytest.mark.parametrize("name", sorted(GEMM_MUTANTS))
+def test_gemm_mutant_is_caught(name, monkeypatch):
+    attr, fn = GEMM_MUTANTS[name]
+    monkeypatch.setattr(dg, attr, fn)
+    assert oracle_pins.failures(), f"no pin caught the mutant '{name}'"
 
 
 @pytest.mark.parametrize("name", sorted(FOLD_MUTANTS))
