@@ -56,8 +56,11 @@ def parse():
     ap.add_argument("--steps", type=int, default=100)
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", choices=["long_tail", "decode_batch", "mixed_step"],
-                    default="long_tail")
+    ap.add_argument("--workload", choices=["long_tail", "decode_batch", "mixed_step",
+                                           "decode_gemm"],
+                    default="long_tail",
+                    help="decode_gemm: the fixed-width decode linear layer (vocabulary head "
+                         "248320 x 5120, T_pad 64), a second workload with its own metric")
     ap.add_argument("--layers", type=int, default=None)
     ap.add_argument("--small", action="store_true",
                     help="a few-GB version of the workload (for profiler captures)")
@@ -539,6 +542,194 @@ def run_ours(args, rank, world, local_rank):
 
 
 # ---------------------------------------------------------------------------
+# second workload: the batch-invariant decode GEMM at a fixed token width
+# ---------------------------------------------------------------------------
+
+GEMM_METRIC = "decode GEMM weight GB/s at a fixed token width (% of GB300 HBM peak)"
+GEMM_PROFILE = (os.path.join(ROOT, "profiles", "decode_gemm_vocab_head.md"),
+                ["invariant_paged_kv_gb300/csrc/pa_decode_gemm.cu",
+                 "invariant_paged_kv_gb300/csrc/pa_tcgen05.cuh",
+                 "invariant_paged_kv_gb300/csrc/pa_common.cuh"])
+
+
+def gemm_shape(args):
+    # the vocabulary head of the shapes "ninfer" issue 80 lists, T_pad = 64
+    # --small: 38912 rows (398 MB of weights, > L2) keep one K split, as the
+    # full head does, so a capture of it scales to the full launch
+    return (38912, 5120, 64) if args.small else (248320, 5120, 64)
+
+
+def _gemm_oracle_job(job):
+    """Oracle on rows [r0, r1) of the weight; returns (weight bytes, compute s)."""
+    import torch
+
+    import oracle.decode_gemm as dg
+    N, K, T_pad, r0, r1, seed = job
+    g = torch.Generator().manual_seed(seed)
+    x = torch.randn(T_pad, K, generator=g).to(torch.bfloat16)
+    w = (torch.randn(r1 - r0, K, generator=g) / K ** 0.5).to(torch.bfloat16)
+    xs = x.view(torch.int16).numpy().view(np.uint16)
+    ws = w.view(torch.int16).numpy().view(np.uint16)
+    t0 = time.perf_counter()
+    dg.linear(xs, ws)
+    return (r1 - r0) * K * 2, time.perf_counter() - t0
+
+
+def gemm_cpu_rate(N, K, T_pad, seconds_budget=10.0):
+    pool = OraclePool()
+    try:
+        rows, per = 0, 2048
+        done_bytes, busy = 0, 0.0
+        t_start = time.perf_counter()
+        while time.perf_counter() - t_start < seconds_budget and rows < N:
+            jobs = [(N, K, T_pad, rows + i * per, min(N, rows + (i + 1) * per), 31 + rows + i)
+                    for i in range(pool.workers) if rows + i * per < N]
+            for nbytes, dt in pool.pool.map(_gemm_oracle_job, jobs, chunksize=1):
+                done_bytes += nbytes
+                busy += dt
+            rows += len(jobs) * per
+        rate = done_bytes / (busy / pool.workers) / 1e9
+        desc = (f"{min(rows, N)} of {N} weight rows ({done_bytes / 1e9:.2f} GB of bf16 weights), "
+                f"{pool.workers} spawn workers x 1 BLAS thread, fp64 oracle matmul timed")
+        return rate, pool.workers, desc
+    finally:
+        pool.close()
+
+
+def run_gemm(args, rank, world, local_rank):
+    import torch
+    import torch.distributed as dist
+
+    from invariant_paged_kv_gb300 import build, pa
+
+    build.build()
+    pa.load()
+    dev = torch.device("cuda", local_rank)
+    torch.cuda.set_device(dev)
+    N, K, T_pad = gemm_shape(args)
+    gen = torch.Generator(device=dev).manual_seed(6000 + rank)
+    w = torch.empty(N, K, dtype=torch.bfloat16, device=dev)
+    for r in range(0, N, 16384):  # fill in slices: bounded fp32 temporaries
+        n = min(16384, N - r)
+        w[r:r + n] = (torch.randn(n, K, generator=gen, device=dev) / K ** 0.5).to(torch.bfloat16)
+    x = torch.randn(T_pad, K, generator=gen, device=dev).to(torch.bfloat16)
+    y = torch.empty(T_pad, N, dtype=torch.bfloat16, device=dev)
+    ws = pa.decode_gemm_workspace(T_pad, N, K, dev)
+    status = pa.new_status(dev)
+    stream = torch.cuda.current_stream()
+    S = pa.decode_gemm_splits(N, K)
+
+    def barrier():
+        if world > 1:
+            dist.barrier()
+        torch.cuda.synchronize()
+
+    for _ in range(max(3, args.warmup)):
+        pa.decode_gemm(x, w, y, ws, status)
+    Ksteps = args.steps
+    graph = None
+    if not args.no_graph:
+        graph = torch.cuda.CUDAGraph()
+        l0 = pa.kernel_launches()
+        with torch.cuda.graph(graph):
+            for _ in range(Ksteps):
+                pa.decode_gemm(x, w, y, ws, status)
+        launches = pa.kernel_launches() - l0
+        graph.replay()
+    barrier()
+    clocks = ClockSampler(local_rank) if not args.no_clocks else None
+    if clocks:
+        clocks.start()
+        time.sleep(0.3)
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    l0 = pa.kernel_launches()
+    a.record(stream)
+    if graph is None:
+        for _ in range(Ksteps):
+            pa.decode_gemm(x, w, y, ws, status)
+    else:
+        graph.replay()
+    b.record(stream)
+    barrier()
+    clk = clocks.stop() if clocks else None
+    if graph is None:
+        launches = pa.kernel_launches() - l0
+    ms = a.elapsed_time(b) / Ksteps
+    if pa.read_status(status):
+        raise RuntimeError("device status flags set")
+    ms_max = max_over_ranks(ms, world, dev)
+    step_bytes = N * K * 2 + T_pad * K * 2 + T_pad * N * 2 + (2 * S * T_pad * N * 4 if S > 1 else 0)
+    alg_bytes = N * K * 2 + T_pad * K * 2 + T_pad * N * 2
+    value = weak_scaling_value(alg_bytes, world, ms_max)
+
+    e2e = None
+    if not args.no_e2e:
+        hx = x.cpu().pin_memory()
+        hy = torch.empty(y.shape, dtype=y.dtype, pin_memory=True)
+        dx = torch.empty_like(x)
+
+        def e2e_step():
+            dx.copy_(hx, non_blocking=True)
+            pa.decode_gemm(dx, w, y, ws, status)
+            hy.copy_(y, non_blocking=True)
+
+        for _ in range(2):
+            e2e_step()
+        barrier()
+        c, d = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+        c.record(stream)
+        for _ in range(Ksteps):
+            e2e_step()
+        d.record(stream)
+        barrier()
+        e_ms = max_over_ranks(c.elapsed_time(d) / Ksteps, world, dev)
+        e2e = {"value": round(weak_scaling_value(alg_bytes, world, e_ms), 1), "unit": "GB/s",
+               "ms_per_step": round(e_ms, 4), "h2d_bytes_per_step": hx.numel() * 2,
+               "d2h_bytes_per_step": hy.numel() * 2,
+               "what": "pinned host -> device copy of x, pa_decode_gemm, device -> host copy of y"}
+
+    peak, peak_kind = measured_hbm_peak()
+    summary, sources = GEMM_PROFILE
+    h = hashlib.sha256()
+    for rel in sources:
+        with open(os.path.join(ROOT, rel), "rb") as f:
+            h.update(f.read())
+    sha = h.hexdigest()[:16]
+    traffic = None
+    try:
+        vals = dict(line.split(":", 1) for line in open(summary).read().splitlines()
+                    if line.startswith(("source_sha256_16:", "traffic_bytes_per_launch_full:")))
+        if vals.get("source_sha256_16", "").strip() == sha and not args.small:
+            traffic = float(vals["traffic_bytes_per_launch_full"])
+    except (OSError, KeyError, ValueError):
+        pass
+    achieved = alg_bytes / (ms * 1e-3) / 1e9
+    roofline = {"bound": "hbm", "kernel": "decode_gemm_kernel (tcgen05, M = 128 weight rows, "
+                "N = T_pad tokens)", "achieved": round(achieved, 1), "peak": peak,
+                "unit": "GB/s", "peak_kind": peak_kind, "frac": round(achieved / peak, 4),
+                "traffic": traffic, "algorithmic_bytes_per_launch": alg_bytes,
+                "avg_launch_ms": round(ms, 4), "source_sha256_16": sha}
+    cpu = None
+    if rank == 0 and world == 1 and not args.no_cpu_baseline:
+        rate, cores, desc = gemm_cpu_rate(N, K, T_pad)
+        cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
+               "sample": desc}
+    return {
+        "metric": GEMM_METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
+        "steps": Ksteps, "warmup": max(3, args.warmup), "ms_per_step": round(ms_max, 4),
+        "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "bf16",
+        "data": "synthetic (seeded N(0,1) x, N(0,1/K) weights)",
+        "config": {"workload": "decode_gemm_vocab_head", "N": N, "K": K, "T_pad": T_pad,
+                   "t_real": T_pad, "splits": S, "bytes_moved_per_step": step_bytes,
+                   "l2": "no flush: the 2.5 GB weight exceeds the 129 MB L2",
+                   "small": bool(args.small), "cuda_graph": not args.no_graph},
+        "frac_of_hbm_peak": round(value / peak, 4),
+        "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+        "clocks": clk,
+    }
+
+
+# ---------------------------------------------------------------------------
 # reference arm: the CPU oracle on the same config
 # ---------------------------------------------------------------------------
 
@@ -581,6 +772,22 @@ def main():
     if args.impl == "reference":
         if rank != 0:
             return 0
+        if args.workload == "decode_gemm":
+            N, K, T_pad = gemm_shape(args)
+            rate, cores, desc = gemm_cpu_rate(N, K, T_pad, seconds_budget=30.0)
+            ms = (N * K * 2) / (rate * 1e9) * 1e3
+            print(json.dumps({
+                "metric": GEMM_METRIC, "value": round(rate, 4), "unit": "GB/s", "n_gpus": 1,
+                "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 1),
+                "higher_is_better": True, "scaling": "weak", "vs_baseline": None,
+                "dtype": "f64", "data": "synthetic", "impl": "reference",
+                "config": {"workload": "decode_gemm_vocab_head", "N": N, "K": K,
+                           "T_pad": T_pad},
+                "cpu_baseline": {"value": round(rate, 4), "unit": "GB/s", "cores": cores,
+                                 "kind": "oracle", "sample": desc},
+                "e2e": {"value": round(rate, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
+                        "d2h_bytes_per_step": 0}}), flush=True)
+            return 0
         print(json.dumps(run_reference(args)), flush=True)
         return 0
     if world > 1:
@@ -588,7 +795,10 @@ def main():
         import torch.distributed as dist
         torch.cuda.set_device(local_rank)
         dist.init_process_group("nccl")
-    line = run_ours(args, rank, world, local_rank)
+    if args.workload == "decode_gemm":
+        line = run_gemm(args, rank, world, local_rank)
+    else:
+        line = run_ours(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:

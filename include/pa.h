@@ -318,6 +318,34 @@ pa_status pa_merge_partials(const void* partials, size_t partials_bytes, int32_t
                             int32_t* status, void* stream);
 
 /*
+ * pa_decode_gemm -- batch-invariant decode linear layer at a fixed token width
+ * ("ninfer" issue 80, Proposal: opt-in fixed decode width: every GEMM-class
+ * decode op runs at a fixed width T_pad with padded activations, so its
+ * kernel and internal schedule are the same for every real token count
+ * t <= T_pad, and padding columns never mix into real ones).
+ *
+ *   x  [T_pad, K] bf16   rows t >= the real token count are padding (any
+ *                        bits, NaN included); they only reach their own
+ *                        output rows
+ *   w  [N, K] bf16       the weight, row-major (y = x w^T)
+ *   y  [T_pad, N] bf16   y[t, n] = sum_k x[t, k] w[n, k]: fp32 accumulation,
+ *                        rounded once to bf16
+ *   T_pad in {32, 64, 96, 128, 192, 256}; N a multiple of 128; K a multiple
+ *   of 64 (else PA_ERR_UNSUPPORTED); pointers 16-byte aligned.
+ * The schedule -- 128-row weight tiles, S splits of K whose partial sums
+ * are added in split order -- is a function of (N, K) only
+ * (pa_decode_gemm_splits); so y[t, :] depends on x[t, :] and w alone, never
+ * on the other rows of x or on how many of them are real.
+ * workspace: pa_decode_gemm_workspace_bytes(T_pad, N, K) bytes, 256-byte
+ * aligned (0 bytes, and NULL allowed, when S = 1).
+ */
+int32_t pa_decode_gemm_splits(int32_t N, int32_t K);
+size_t pa_decode_gemm_workspace_bytes(int32_t T_pad, int32_t N, int32_t K);
+pa_status pa_decode_gemm(const void* x, const void* w, void* y, int32_t T_pad, int32_t N,
+                         int32_t K, void* workspace, size_t workspace_bytes, int32_t* status,
+                         void* stream);
+
+/*
  * pa_attention_static_scratch -- pa_attention for callers that cannot
  * allocate device memory. (No counterpart in the paper: this entry point
  * exists for integration, not for the method.)

@@ -21,6 +21,11 @@ cudaError_t launch_combine(const StepParams& p, cudaStream_t s);
 cudaError_t launch_prefill_tc(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
                               const CUtensorMap& v, long long max_items, cudaStream_t s);
 
+void decode_gemm_plan(int N, int K, int* S, int* chunks_per_split);
+cudaError_t launch_decode_gemm(void* y, float* part, int T_pad, int N, int K, int S, int cps,
+                               int* status, const CUtensorMap& w, const CUtensorMap& x,
+                               cudaStream_t s);
+
 static std::atomic<long long> g_launches{0};
 
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
@@ -234,6 +239,26 @@ bool encode_code_map(CUtensorMap* map, const void* cache, int NB, int bs, int Hk
                   D == 128 ? CU_TENSOR_MAP_SWIZZLE_128B : CU_TENSOR_MAP_SWIZZLE_64B,
                   CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
   return r == CUDA_SUCCESS;
+}
+
+// Row-major [rows, K] bf16 matrix; box = 64 elements x box_rows rows, 128-byte swizzle.
+bool encode_rows_map(CUtensorMap* map, const void* ptr, int rows, int K, int box_rows) {
+  auto fn = encode_fn();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)K, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)K * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)box_rows};
+  cuuint32_t estr[2] = {1, 1};
+  CUresult r = fn(map, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(ptr), dims, strides,
+                  box, estr, CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B,
+                  CU_TENSOR_MAP_L2_PROMOTION_L2_256B, CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE);
+  return r == CUDA_SUCCESS;
+}
+
+bool gemm_shape_ok(int32_t T_pad, int32_t N, int32_t K) {
+  const bool tp = T_pad == 32 || T_pad == 64 || T_pad == 96 || T_pad == 128 || T_pad == 192 ||
+                  T_pad == 256;
+  return tp && N > 0 && K > 0 && N % 128 == 0 && K % 64 == 0 && (long long)N * K < (1LL << 40);
 }
 
 // q [T, H, D] bf16; box = 64 elements x 1 head x 128 rows, 128-byte swizzle.
@@ -630,6 +655,40 @@ pa_status pa_merge_partials(const void* partials, size_t partials_bytes, int32_t
   count_launches(1);
   if (launch_combine(p, s) != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
+  return PA_OK;
+}
+
+int32_t pa_decode_gemm_splits(int32_t N, int32_t K) {
+  if (N <= 0 || K <= 0 || N % 128 || K % 64) return 0;
+  int S, cps;
+  decode_gemm_plan(N, K, &S, &cps);
+  return S;
+}
+
+size_t pa_decode_gemm_workspace_bytes(int32_t T_pad, int32_t N, int32_t K) {
+  if (!gemm_shape_ok(T_pad, N, K)) return 0;
+  const int S = pa_decode_gemm_splits(N, K);
+  return S > 1 ? align_up((size_t)S * T_pad * N * sizeof(float)) : 0;
+}
+
+pa_status pa_decode_gemm(const void* x, const void* w, void* y, int32_t T_pad, int32_t N,
+                         int32_t K, void* workspace, size_t workspace_bytes, int32_t* status,
+                         void* stream) {
+  if (!gemm_shape_ok(T_pad, N, K)) return PA_ERR_UNSUPPORTED;
+  if (!x || !w || !y || !aligned16(x) || !aligned16(w) || !aligned16(y)) return PA_ERR_INVALID_ARG;
+  int S, cps;
+  decode_gemm_plan(N, K, &S, &cps);
+  const size_t need = pa_decode_gemm_workspace_bytes(T_pad, N, K);
+  if (need && (!workspace || (reinterpret_cast<uintptr_t>(workspace) & (kAlign - 1)) ||
+               workspace_bytes < need))
+    return PA_ERR_WORKSPACE;
+  CUtensorMap tmW, tmX;
+  if (!encode_rows_map(&tmW, w, N, K, 128) || !encode_rows_map(&tmX, x, T_pad, K, T_pad))
+    return PA_ERR_CUDA;
+  if (launch_decode_gemm(y, static_cast<float*>(workspace), T_pad, N, K, S, cps, status, tmW,
+                         tmX, static_cast<cudaStream_t>(stream)) != cudaSuccess)
+    return PA_ERR_CUDA;
+  count_launches(S > 1 ? 2 : 1);
   return PA_OK;
 }
 

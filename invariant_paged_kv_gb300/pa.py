@@ -32,7 +32,8 @@ EXPORTS = ("pa_write_kv", "pa_write_kv_scaled", "pa_attention_workspace_bytes",
            "pa_attention", "pa_attention_ex", "pa_read_status", "pa_status_string",
            "pa_kernel_launches", "pa_split_tokens", "pa_attention_static_scratch",
            "pa_partials_bytes", "pa_partials_workspace_bytes", "pa_attention_partials",
-           "pa_merge_partials")
+           "pa_merge_partials", "pa_decode_gemm_splits", "pa_decode_gemm_workspace_bytes",
+           "pa_decode_gemm")
 
 
 class PaError(RuntimeError):
@@ -97,6 +98,12 @@ def load() -> ctypes.CDLL:
     L.pa_merge_partials.argtypes = [vp, sz, i32, vp, vp, vp, vp, i32, i32, i32, i32, i32, i32,
                                     i32, f32, vp, sz, vp, vp]
     L.pa_merge_partials.restype = ctypes.c_int
+    L.pa_decode_gemm_splits.argtypes = [i32, i32]
+    L.pa_decode_gemm_splits.restype = i32
+    L.pa_decode_gemm_workspace_bytes.argtypes = [i32, i32, i32]
+    L.pa_decode_gemm_workspace_bytes.restype = sz
+    L.pa_decode_gemm.argtypes = [vp, vp, vp, i32, i32, i32, vp, sz, vp, vp]
+    L.pa_decode_gemm.restype = ctypes.c_int
     _lib = L
     return L
 
@@ -316,3 +323,33 @@ def merge_partials(gathered, owners: int, key_bounds, cu_seqlens_q, ctx_lens, ou
         _ptr(cu_seqlens_q), _ptr(ctx_lens), _ptr(out), B, T, H, D, int(max_q_len),
         int(max_ctx_len), code, float(v_scale), _ptr(workspace), workspace.numel(),
         _ptr(status), _stream(stream)), "pa_merge_partials")
+
+
+# ---------------------------------------------------------------------------
+# batch-invariant decode GEMM at a fixed token width
+# ---------------------------------------------------------------------------
+
+def decode_gemm_splits(N: int, K: int) -> int:
+    return int(load().pa_decode_gemm_splits(N, K))
+
+
+def decode_gemm_workspace(T_pad: int, N: int, K: int, device=None) -> torch.Tensor:
+    n = int(load().pa_decode_gemm_workspace_bytes(T_pad, N, K))
+    return torch.empty(max(n, 256), dtype=torch.uint8, device=device or "cuda")
+
+
+def decode_gemm(x, w, y, workspace=None, status=None, stream=None):
+    """pa_decode_gemm: y [T_pad, N] = x [T_pad, K] w [N, K]^T (bf16, fp32
+    accumulate) with a schedule fixed by (N, K); x's padding rows reach only
+    their own rows of y."""
+    T_pad, K = x.shape
+    N = w.shape[0]
+    if x.dtype != torch.bfloat16 or w.dtype != torch.bfloat16 or y.dtype != torch.bfloat16:
+        raise TypeError("decode_gemm takes bf16 x, w and y")
+    if tuple(w.shape) != (N, K) or tuple(y.shape) != (T_pad, N):
+        raise ValueError("shapes: x [T_pad, K], w [N, K], y [T_pad, N]")
+    if workspace is None:
+        workspace = decode_gemm_workspace(T_pad, N, K, x.device)
+    _check(load().pa_decode_gemm(_ptr(x), _ptr(w), _ptr(y), T_pad, N, K, _ptr(workspace),
+                                 workspace.numel(), _ptr(status), _stream(stream)),
+           "pa_decode_gemm")

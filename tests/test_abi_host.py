@@ -191,3 +191,20 @@ def test_kv_parallel_refusals_before_cuda(lib):
     assert m(*(mb[:3] + [None] + mb[4:])) == 1               # no bounds
     assert m(*(mb[:1] + [1 << 20 | 8] + mb[2:])) == 3        # owner stride not 256-aligned
     assert lib.pa_kernel_launches() == before
+
+
+def test_decode_gemm_refusals_before_cuda(lib):
+    before = lib.pa_kernel_launches()
+    f = lib.pa_decode_gemm
+    assert f(1 << 12, 1 << 12, 1 << 12, 48, 1024, 5120, None, 0, None, None) == 2   # T_pad
+    assert f(1 << 12, 1 << 12, 1 << 12, 64, 1000, 5120, None, 0, None, None) == 2   # N % 128
+    assert f(1 << 12, 1 << 12, 1 << 12, 64, 1024, 5000, None, 0, None, None) == 2   # K % 64
+    assert f(None, 1 << 12, 1 << 12, 64, 1024, 5120, None, 0, None, None) == 1
+    assert f(1 << 12, 1 << 12, (1 << 12) + 2, 64, 1024, 5120, None, 0, None, None) == 1
+    assert f(1 << 12, 1 << 12, 1 << 12, 64, 1024, 5120, None, 0, None, None) == 3   # needs split-K scratch
+    assert lib.pa_kernel_launches() == before
+    # the plan is a function of the shape only
+    assert lib.pa_decode_gemm_splits(1024, 5120) == 20
+    assert lib.pa_decode_gemm_splits(248320, 5120) == 1
+    assert lib.pa_decode_gemm_workspace_bytes(64, 248320, 5120) == 0
+    assert lib.pa_decode_gemm_workspace_bytes(64, 1024, 5120) >= 20 * 64 * 1024 * 4
