@@ -48,7 +48,7 @@ __device__ __forceinline__ uint32_t tile_addr(uint32_t base, int tok, int c16) {
   return base + half * Tile<D>::kHalfBytes + tok * 128 + ((chunk ^ (tok & 7)) << 4);
 }
 
-template <int D, int NT>
+template <int D, int NT, bool kOwner>
 __global__ void __launch_bounds__(kWarps * 32, 2)
     decode_bf16_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV) {
@@ -218,8 +218,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         float pa[2], pc[2];
 #pragma unroll
         for (int e = 0; e < 2; ++e) {
-          const float ta = va ? s[nt][e] * p.scale_log2 : -INFINITY;
-          const float tb = vb ? s[nt][2 + e] * p.scale_log2 : -INFINITY;
+          const float ta = va ? __fmul_rn(s[nt][e], p.scale_log2) : -INFINITY;
+          const float tb = vb ? __fmul_rn(s[nt][2 + e], p.scale_log2) : -INFINITY;
           float mx = fmaxf(ta, tb);
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
           mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
@@ -278,7 +278,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         l[nt][e] = v;
       }
     }
-    const bool single = it.single && !p.partials_mode;
+    const bool single = it.single && !kOwner;
     const size_t head0 = (size_t)it.row * p.H + (size_t)it.kvh * g;  // first head of the group
     if (single) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
@@ -297,7 +297,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
         }
     } else {
       const size_t ph0 =
-          (size_t)partial_entry(p, it.pair, it.row, it.t0 / split_len(it.keys)) * p.H +
+          (size_t)(kOwner ? (long long)p.plan.row_info[it.row].x + it.t0 / split_len(it.keys)
+                          : (long long)it.pair) * p.H +
           (size_t)it.kvh * g;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -325,15 +326,25 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   }
 }
 
-template <int D, int NT>
-cudaError_t launch_t(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v, int grid,
+template <int D, int NT, bool kOwner>
+cudaError_t launch_o(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v, int grid,
                      cudaStream_t s) {
-  auto kern = decode_bf16_kernel<D, NT>;
+  auto kern = decode_bf16_kernel<D, NT, kOwner>;
   static unsigned long long done = 0;
   cudaError_t e = smem_opt_in(kern, Tile<D>::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
   kern<<<grid, kWarps * 32, Tile<D>::kSmemBytes, s>>>(p, k, v);
   return cudaGetLastError();
+}
+
+// The KV-parallel owner variant (partials to canonical entries, never a
+// direct write) is a separate instantiation so ordinary steps run the plain
+// kernel; both share every line of the arithmetic.
+template <int D, int NT>
+cudaError_t launch_t(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v, int grid,
+                     cudaStream_t s) {
+  return p.partials_mode ? launch_o<D, NT, true>(p, k, v, grid, s)
+                         : launch_o<D, NT, false>(p, k, v, grid, s);
 }
 
 }  // namespace

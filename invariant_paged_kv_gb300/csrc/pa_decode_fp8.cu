@@ -50,7 +50,7 @@ __device__ __forceinline__ uint32_t swz(uint32_t off) {
   return off ^ (((off >> 7) & 3u) << 4);
 }
 
-template <int D, int NT>
+template <int D, int NT, bool kOwner>
 __global__ void __launch_bounds__(kWarps * 32, 3)
     decode_fp8_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
                       const __grid_constant__ CUtensorMap tmV) {
@@ -356,7 +356,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
       }
     }
     const size_t head0 = (size_t)it.row * p.H + (size_t)it.kvh * g;
-    if (it.single && !p.partials_mode) {
+    if (it.single && !kOwner) {
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -374,7 +374,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
         }
     } else {
       const size_t ph0 =
-          (size_t)partial_entry(p, it.pair, it.row, it.t0 / split_len(it.keys)) * p.H +
+          (size_t)(kOwner ? (long long)p.plan.row_info[it.row].x + it.t0 / split_len(it.keys)
+                          : (long long)it.pair) * p.H +
           (size_t)it.kvh * g;
 #pragma unroll
       for (int nt = 0; nt < NT; ++nt)
@@ -402,15 +403,25 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   }
 }
 
-template <int D, int NT>
-cudaError_t launch_t(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v, int grid,
+template <int D, int NT, bool kOwner>
+cudaError_t launch_o(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v, int grid,
                      cudaStream_t s) {
-  auto kern = decode_fp8_kernel<D, NT>;
+  auto kern = decode_fp8_kernel<D, NT, kOwner>;
   static unsigned long long done = 0;
   cudaError_t e = smem_opt_in(kern, Tile8<D>::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
   kern<<<grid, kWarps * 32, Tile8<D>::kSmemBytes, s>>>(p, k, v);
   return cudaGetLastError();
+}
+
+// The KV-parallel owner variant (partials to canonical entries, never a
+// direct write) is a separate instantiation so ordinary steps run the plain
+// kernel; both share every line of the arithmetic.
+template <int D, int NT>
+cudaError_t launch_t(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v, int grid,
+                     cudaStream_t s) {
+  return p.partials_mode ? launch_o<D, NT, true>(p, k, v, grid, s)
+                         : launch_o<D, NT, false>(p, k, v, grid, s);
 }
 
 }  // namespace
