@@ -5,9 +5,9 @@
 // tokens share one flat step; Evidence, mutant "prefill causal mask off by
 // one"): its row j sits at position ctx - q_len + j and attends keys
 // 0..position. Work item = (128-row q tile of one lane, a pair of query heads
-// that read the same kv head). Per item, key tiles of 64 keys go in ascending
-// order; for each head of the pair and each key tile:
-//   S = Q K^T           tcgen05.mma, M = 128 rows, N = 64 keys, K = D, fp32 in TMEM
+// that read the same kv head). Per item, key tiles of 128 keys go in
+// ascending order; for each head of the pair and each key tile:
+//   S = Q K^T           tcgen05.mma, M = 128 rows, N = 128 keys, K = D, fp32 in TMEM
 //   m, p, l             one thread per row: running max, p = 2^(t - m) rounded
 //                       to bf16 and written back over S in TMEM, l += sum of
 //                       the rounded p -- all within the thread
@@ -15,20 +15,21 @@
 //                       smem), O in TMEM
 // and finally out = O / l. The running max moves only when a tile's max
 // exceeds it by more than 8 (log2 units), so O is rescaled rarely. A row's
-// arithmetic depends on its q row, its keys and the fixed 64-key tiling from
-// key 0 -- never on other lanes.
+// arithmetic depends on its q row, its keys and the fixed 128-key tiling from
+// key 0 -- never on other lanes. (N = 128 keys: a 128 x 128 x 16 product runs
+// at the tensor core's full rate, where a 128 x 64 x 16 one reaches ~70%.)
 //
 // Warp roles (320 threads): warps 0-3 and 4-7 are two softmax groups (one per
 // head of the pair; thread r of a group owns row r = TMEM lane r), warp 8
-// issues the MMAs (one elected thread), warp 9 streams Q / K / V in by TMA
-// (K / V through the block table, 16 keys per box) into 4-deep K and V rings
-// shared by both heads. Each head has two S/P buffers, so S of tile f + 1 is
-// computed while the softmax works on tile f and P V of tile f - 1 runs; the
-// tensor core also alternates between the two heads. TMEM (512 columns):
-// S/P buffers 0 and 1 and O of head A, then the same for head B. Every wait
-// is bounded (timeout -> PA_FLAG_TIMEOUT). No parity wait ever meets a barrier
-// more than one phase away from the awaited one, ahead or behind (see the P V
-// barriers, which alternate by tile parity for that reason).
+// issues the MMAs (one elected thread), warp 9 streams Q / K / V in by TMA (K /
+// V through the block table, 16 keys per box) into 2-deep K and V rings shared
+// by both heads. TMEM per head slot (256 of the 512 columns): S / P (128), O
+// (128). Each head has one S / P buffer; the MMA warp serves the two heads in
+// turn -- P V of tile t for a head, then (once that P is consumed) its S of
+// tile t + 1 -- so one head's softmax runs while the tensor core works for the
+// other. Every wait is bounded (timeout -> PA_FLAG_TIMEOUT). No parity wait
+// ever meets a barrier more than one phase away from the awaited one, ahead
+// or behind (the P V barriers alternate by tile parity for that reason).
 #include "pa_tcgen05.cuh"
 
 namespace pa {
@@ -36,8 +37,8 @@ namespace pa {
 namespace {
 
 constexpr int kRows = 128;  // query rows per item (M)
-constexpr int kKeys = 64;   // keys per tile (N of S, K of PV)
-constexpr int kStages = 4;  // depth of the K and V rings
+constexpr int kKeys = 128;  // keys per tile (N of S, K of PV)
+constexpr int kStages = 2;  // depth of the K and V rings
 constexpr int kThreads = 320;
 constexpr uint32_t kTmemCols = 512;
 constexpr float kRescaleLog2 = 8.f;
@@ -46,7 +47,7 @@ template <int D>
 struct PfLayout {
   static constexpr int kHalves = D / 64;
   static constexpr int kHalfBytes = kRows * 128;         // Q: 128 rows x 128 bytes
-  static constexpr int kKHalfBytes = kKeys * 128;        // K / V: 64 keys x 128 bytes
+  static constexpr int kKHalfBytes = kKeys * 128;        // K / V: 128 keys x 128 bytes
   static constexpr int kQBytes = kHalves * kHalfBytes;   // one Q tile
   static constexpr int kKBytes = kHalves * kKHalfBytes;  // one K tile
   static constexpr int kVBytes = kHalves * kKHalfBytes;  // one V tile
@@ -60,8 +61,8 @@ struct PfLayout {
 };
 
 struct Bars {
-  uint64_t q, kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
-  uint64_t s[2][2], p[2][2], o[2][2];  // [head][buffer / tile parity]
+  uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
+  uint64_t q, s[2], p[2], o[2][2];  // [head slot] ([tile parity] for o)
 };
 
 struct ItemInfo {
@@ -139,18 +140,16 @@ __global__ void __launch_bounds__(kThreads, 1)
     bve[i] = smem_u32(&bars.vempty[i]);
   }
   if (threadIdx.x == 0) {
-    mbar_init(bq, 1);
     for (int i = 0; i < kStages; ++i) {
       mbar_init(bkf[i], 1);
       mbar_init(bke[i], 1);
       mbar_init(bvf[i], 1);
       mbar_init(bve[i], 1);
     }
+    mbar_init(bq, 1);
     for (int h = 0; h < 2; ++h) {
-      for (int b = 0; b < 2; ++b) {
-        mbar_init(smem_u32(&bars.s[h][b]), 1);
-        mbar_init(smem_u32(&bars.p[h][b]), kRows);
-      }
+      mbar_init(smem_u32(&bars.s[h]), 1);
+      mbar_init(smem_u32(&bars.p[h]), kRows);
       mbar_init(smem_u32(&bars.o[h][0]), 1);
       mbar_init(smem_u32(&bars.o[h][1]), 1);
     }
@@ -167,29 +166,32 @@ __global__ void __launch_bounds__(kThreads, 1)
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  // S / P buffer b of head slot h at column 256 h + 64 b; O of head slot h at 256 h + 128
-  auto tS = [&](int h, uint32_t b) -> uint32_t { return tmem + 256 * h + kKeys * b; };
+  // head slot h: S / P at column 256 h, O at 256 h + 128
+  auto tS = [&](int h) -> uint32_t { return tmem + 256 * h; };
   auto tO = [&](int h) -> uint32_t { return tmem + 256 * h + 128; };
-  auto bS = [&](int h, uint32_t b) -> uint32_t { return smem_u32(&bars.s[h][b]); };
-  auto bP = [&](int h, uint32_t b) -> uint32_t { return smem_u32(&bars.p[h][b]); };
+  auto bS = [&](int h) -> uint32_t { return smem_u32(&bars.s[h]); };
+  auto bP = [&](int h) -> uint32_t { return smem_u32(&bars.p[h]); };
   // P V of tile t completes on o[head][t & 1]
   auto bO = [&](int h, uint32_t t) -> uint32_t { return smem_u32(&bars.o[h][t & 1]); };
 
   const int g = p.H / p.Hkv;
   const int n_items = p.plan.header[2] * p.Hkv * ((g + 1) / 2);
   const float c2 = p.scale_log2;  // > 0 (validated on the host)
-  // running use counters, identical in every role: K/V ring fills, and key
-  // tiles done by each head slot
+  // running use counters, identical in every role: items, K/V ring fills,
+  // key tiles done by each head slot
   uint32_t n_item = 0, n_kv = 0, n_t[2] = {0, 0};
 
   for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
     const ItemInfo it = item_info(p, item, g);
+    const int nh = 1 + it.has_b;
 
     if (warp == 9) {
       // ------------------------------ producer ------------------------------
+      // Q of this item's heads (the previous item's S products, which read
+      // this buffer, all finished before the item boundary)
       if (lane == 0) {
-        mbar_expect_tx(bq, (it.has_b ? 2 : 1) * L::kQBytes);
-        for (int hb = 0; hb < 1 + it.has_b; ++hb)
+        mbar_expect_tx(bq, nh * L::kQBytes);
+        for (int hb = 0; hb < nh; ++hb)
 #pragma unroll
           for (int h = 0; h < L::kHalves; ++h)
             tma_load_3d(sQ + hb * L::kQBytes + h * L::kHalfBytes, &tmQ, h * 64, it.head0 + hb,
@@ -199,7 +201,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         const uint32_t f = n_kv + kt, st = f % kStages, use = f / kStages;
         const int key0 = kt * kKeys;
         const int nchunk = min(kKeys / kChunk, (it.ctx - key0 + kChunk - 1) / kChunk);
-        int blk = 0;  // block id of chunk `lane` (lanes 0..3)
+        int blk = 0;  // block id of chunk `lane` (lanes 0..7)
         if (lane < nchunk) {
           blk = p.block_tables[(size_t)it.lane * p.max_blocks + (key0 + lane * kChunk) / p.bs];
           if (blk < 0 || blk >= p.NB) {
@@ -233,13 +235,41 @@ __global__ void __launch_bounds__(kThreads, 1)
       // ------------------------------ MMA issuer ----------------------------
       constexpr uint32_t idS = umma_idesc_bf16(kRows, kKeys, 0, 0);
       constexpr uint32_t idPV = umma_idesc_bf16(kRows, D, 0, 1);
-      const int nh = 1 + it.has_b;
-      bool ok = wait_or_abort(bq, n_item & 1, &s_abort, p.status);
-      // P V of key tile j (both heads), once its P and V are there
-      auto issue_pv = [&](int j) -> bool {
-        const uint32_t f = n_kv + j, st = f % kStages;
-        if (!wait_or_abort(bvf[st], (f / kStages) & 1, &s_abort, p.status)) return false;
-        const int key0 = j * kKeys;
+      // S of key tile j for head slot hb: A = Q tile, B = K tile (both smem)
+      auto issue_s = [&](int hb, int j) {
+        const uint32_t st = (n_kv + j) % kStages;
+        if (lane == 0) {
+#pragma unroll
+          for (int kk = 0; kk < D / 16; ++kk) {
+            const uint32_t off_q = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
+            const uint32_t off_k = (kk >> 2) * L::kKHalfBytes + (kk & 3) * 32;
+            const uint64_t ad = umma_desc_sw128(sQ + hb * L::kQBytes + off_q, 16, 1024);
+            const uint64_t bd = umma_desc_sw128(sK0 + st * L::kKBytes + off_k, 16, 1024);
+            umma_bf16(tS(hb), ad, bd, idS, kk > 0 ? 1u : 0u);
+          }
+          umma_commit(bS(hb));
+        }
+        __syncwarp();
+      };
+      bool ok = true;
+      // first S of the item, once Q is in TMEM and K tile 0 has landed
+      {
+        const uint32_t f = n_kv, st = f % kStages;
+        ok = wait_or_abort(bkf[st], (f / kStages) & 1, &s_abort, p.status) &&
+             wait_or_abort(bq, n_item & 1, &s_abort, p.status);
+        for (int hb = 0; ok && hb < nh; ++hb) {
+          tc_fence_after();
+          issue_s(hb, 0);
+        }
+        if (ok && lane == 0) umma_commit(bke[st]);
+        __syncwarp();
+      }
+      for (int kt = 0; ok && kt < it.nkt; ++kt) {
+        const uint32_t f = n_kv + kt, st = f % kStages;
+        const bool next = kt + 1 < it.nkt;
+        const uint32_t f1 = f + 1, st1 = f1 % kStages;
+        if (!wait_or_abort(bvf[st], (f / kStages) & 1, &s_abort, p.status)) break;
+        const int key0 = kt * kKeys;
         if (key0 + kKeys > it.ctx) {
           // keys past the lane's end: zero their V rows (stale bytes must not
           // meet p = 0 as 0 * NaN)
@@ -255,55 +285,39 @@ __global__ void __launch_bounds__(kThreads, 1)
           __syncwarp();
         }
         for (int hb = 0; hb < nh; ++hb) {
-          const uint32_t th = n_t[hb] + j;
-          if (!wait_or_abort(bP(hb, th & 1), (th >> 1) & 1, &s_abort, p.status)) return false;
+          const uint32_t th = n_t[hb] + kt;
+          // P V of tile kt, once this head's softmax has written P
+          if (!wait_or_abort(bP(hb), th & 1, &s_abort, p.status)) { ok = false; break; }
           tc_fence_after();
           if (lane == 0) {
 #pragma unroll
             for (int k = 0; k < kKeys / 16; ++k) {
               const uint64_t bd = umma_desc_sw128(sV0 + st * L::kVBytes + k * 16 * 128,
                                                   L::kKHalfBytes, 1024);
-              umma_bf16_tmem_a(tO(hb), tS(hb, th & 1) + k * 8, bd, idPV,
-                               (j > 0 || k > 0) ? 1u : 0u);
+              umma_bf16_tmem_a(tO(hb), tS(hb) + k * 8, bd, idPV, (kt > 0 || k > 0) ? 1u : 0u);
             }
             umma_commit(bO(hb, th));
           }
           __syncwarp();
-        }
-        if (lane == 0) umma_commit(bve[st]);
-        __syncwarp();
-        return true;
-      };
-      for (int kt = 0; ok && kt < it.nkt; ++kt) {
-        const uint32_t f = n_kv + kt, st = f % kStages;
-        if (!wait_or_abort(bkf[st], (f / kStages) & 1, &s_abort, p.status)) break;
-        for (int hb = 0; hb < nh; ++hb) {
-          const uint32_t th = n_t[hb] + kt;
-          // buffer th & 1 last held P of tile kt - 2: its P V must be done
-          if (kt >= 2 && !wait_or_abort(bO(hb, th - 2), ((th - 2) >> 1) & 1, &s_abort, p.status)) {
-            ok = false;
-            break;
-          }
-          tc_fence_after();
-          if (lane == 0) {
-#pragma unroll
-            for (int kk = 0; kk < D / 16; ++kk) {
-              const uint32_t off_q = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-              const uint32_t off_k = (kk >> 2) * L::kKHalfBytes + (kk & 3) * 32;
-              const uint64_t ad = umma_desc_sw128(sQ + hb * L::kQBytes + off_q, 16, 1024);
-              const uint64_t bd = umma_desc_sw128(sK0 + st * L::kKBytes + off_k, 16, 1024);
-              umma_bf16(tS(hb, th & 1), ad, bd, idS, kk > 0 ? 1u : 0u);
+          if (next) {
+            // S of tile kt + 1 needs its K tile, and it overwrites P of tile
+            // kt: wait for that P V
+            if (hb == 0 && !wait_or_abort(bkf[st1], (f1 / kStages) & 1, &s_abort, p.status)) {
+              ok = false;
+              break;
             }
-            umma_commit(bS(hb, th & 1));
+            if (!wait_or_abort(bO(hb, th), (th >> 1) & 1, &s_abort, p.status)) { ok = false; break; }
+            tc_fence_after();
+            issue_s(hb, kt + 1);
           }
-          __syncwarp();
         }
         if (!ok) break;
-        if (lane == 0) umma_commit(bke[st]);
+        if (lane == 0) {
+          umma_commit(bve[st]);
+          if (next) umma_commit(bke[st1]);
+        }
         __syncwarp();
-        if (kt >= 1 && !issue_pv(kt - 1)) break;
       }
-      if (__all_sync(0xffffffffu, s_abort == 0)) issue_pv(it.nkt - 1);
     } else if (warp < 4 || it.has_b) {
       // ------------------------------ softmax rows --------------------------
       const int hb = warp >> 2;         // head slot of this group
@@ -311,17 +325,18 @@ __global__ void __launch_bounds__(kThreads, 1)
       const int pos = it.p_first + min(r, it.nrows - 1);
       const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
       const uint32_t tOr = tO(hb) + lane_off;
+      const uint32_t tSr = tS(hb) + lane_off;
       float m = -INFINITY, l = 0.f;
       bool ok = true;
 #pragma unroll 1
       for (int kt = 0; kt < it.nkt; ++kt) {
-        const uint32_t th = n_t[hb] + kt, b = th & 1;
-        const uint32_t tSr = tS(hb, b) + lane_off;
-        if (!wait_or_abort(bS(hb, b), (th >> 1) & 1, &s_abort, p.status)) { ok = false; break; }
+        const uint32_t th = n_t[hb] + kt;
+        if (!wait_or_abort(bS(hb), th & 1, &s_abort, p.status)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[kKeys];
-        tmem_ld32(tSr, *reinterpret_cast<uint32_t(*)[32]>(&sv[0]));
-        tmem_ld32(tSr + 32, *reinterpret_cast<uint32_t(*)[32]>(&sv[32]));
+#pragma unroll
+        for (int c = 0; c < kKeys / 32; ++c)
+          tmem_ld32(tSr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
         tmem_wait_ld();
         const int lim = pos - kt * kKeys;  // columns c <= lim are visible to this row
         const bool full = __all_sync(0xffffffffu, lim >= kKeys - 1);
@@ -349,38 +364,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = mn;
         const float neg = -mn;
         // p = 2^(s c2 - m) rounded to bf16, written over S as P (two per
-        // column); their sum in eight independent partial sums folded by a
-        // fixed tree
+        // column, 32 columns at a time); their sum in eight independent
+        // partial sums folded by a fixed tree
         float r8[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) r8[j] = 0.f;
-        uint32_t pk[kKeys / 2];
 #pragma unroll
-        for (int i = 0; i < kKeys / 2; ++i) {
-          float e0 = ex2_approx(fmaf(__uint_as_float(sv[2 * i]), c2, neg));
-          float e1 = ex2_approx(fmaf(__uint_as_float(sv[2 * i + 1]), c2, neg));
-          if (!full) {
-            e0 = (2 * i <= lim) ? e0 : 0.f;
-            e1 = (2 * i + 1 <= lim) ? e1 : 0.f;
+        for (int hh = 0; hh < 2; ++hh) {
+          uint32_t pk[kKeys / 4];
+#pragma unroll
+          for (int i = 0; i < kKeys / 4; ++i) {
+            const int c0 = hh * (kKeys / 2) + 2 * i;
+            float e0 = ex2_approx(fmaf(__uint_as_float(sv[c0]), c2, neg));
+            float e1 = ex2_approx(fmaf(__uint_as_float(sv[c0 + 1]), c2, neg));
+            if (!full) {
+              e0 = (c0 <= lim) ? e0 : 0.f;
+              e1 = (c0 + 1 <= lim) ? e1 : 0.f;
+            }
+            pk[i] = pack_bf16x2(e0, e1);
+            r8[i & 7] += bf16_lo(pk[i]) + bf16_hi(pk[i]);
           }
-          pk[i] = pack_bf16x2(e0, e1);
-          r8[i & 7] += bf16_lo(pk[i]) + bf16_hi(pk[i]);
+          tmem_st16(tSr + hh * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
+          tmem_st16(tSr + hh * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
         }
 #pragma unroll
         for (int w = 4; w >= 1; w >>= 1)
 #pragma unroll
           for (int j = 0; j < w; ++j) r8[j] += r8[j + w];
         const float rs = r8[0];
-        tmem_st16(tSr, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-        tmem_st16(tSr + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
         tmem_wait_st();
         l = fmaf(l, alpha, rs);
-        // P V of the previous tile must be done before O is rescaled. P V
-        // completions alternate between two barriers by tile parity, so a
-        // barrier is never more than one phase away from any wait on it even
-        // when tiles without a rescale skip the wait (S of this tile was
-        // issued after P V of tile th - 2 finished, and P V of tile th + 1
-        // needs this tile's P).
+        // O is rescaled after P V of the previous tile has finished (it has:
+        // S of this tile was issued after it); P V completions alternate
+        // between two barriers by tile parity, so a barrier is never more
+        // than one phase away from any wait on it even when tiles without a
+        // rescale skip the wait.
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
           if (!wait_or_abort(bO(hb, th - 1), ((th - 1) >> 1) & 1, &s_abort, p.status)) {
             ok = false;
@@ -399,7 +417,7 @@ __global__ void __launch_bounds__(kThreads, 1)
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(bP(hb, b));
+        mbar_arrive(bP(hb));
       }
       const uint32_t last = n_t[hb] + it.nkt - 1;
       if (ok && wait_or_abort(bO(hb, last), (last >> 1) & 1, &s_abort, p.status)) {
