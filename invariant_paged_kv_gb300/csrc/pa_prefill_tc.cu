@@ -10,10 +10,10 @@
 //   S = Q K^T           tcgen05.mma, M = 128 rows, N = 128 keys, K = D, fp32 in TMEM
 //   m, p, l             one thread per row: running max, p = 2^(t - m) rounded
 //                       to bf16 and written back over S in TMEM, l += sum of
-//                       the rounded p -- all within the thread
+//                       the p (fp32, before rounding) -- all within the thread
 //   O = O * alpha + P V tcgen05.mma with A = P read from TMEM, B = V (MN-major
 //                       smem), O in TMEM
-// and finally out = O / l. The running max moves only when a tile's max
+// and finally out = O * (1 / l). The running max moves only when a tile's max
 // exceeds it by more than 8 (log2 units), so O is rescaled rarely. A row's
 // arithmetic depends on its q row, its keys and the fixed 128-key tiling from
 // key 0 -- never on other lanes. (N = 128 keys: a 128 x 128 x 16 product runs
@@ -116,6 +116,8 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
   return __all_sync(0xffffffffu, wait_or_abort_1(bar, parity, abort_flag, status));
 }
 
+// 320 threads put three warps on two of the four SM sub-partitions, whose
+// register files hold 16384 each: 168 registers per thread is the ceiling.
 template <int D>
 __global__ void __launch_bounds__(kThreads, 1)
     prefill_tc_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmQ,
@@ -347,7 +349,9 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int j = 0; j < 8; ++j) m8[j] = -INFINITY;
         if (full) {
 #pragma unroll
-          for (int i = 0; i < kKeys; ++i) m8[i & 7] = fmaxf(m8[i & 7], __uint_as_float(sv[i]));
+          for (int i = 0; i < kKeys; i += 2)
+            m8[(i >> 1) & 7] =
+                fmax3(m8[(i >> 1) & 7], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
         } else {
 #pragma unroll
           for (int i = 0; i < kKeys; ++i)
@@ -364,34 +368,41 @@ __global__ void __launch_bounds__(kThreads, 1)
         m = mn;
         const float neg = -mn;
         // p = 2^(s c2 - m) rounded to bf16, written over S as P (two per
-        // column, 32 columns at a time); their sum in eight independent
-        // partial sums folded by a fixed tree
-        float r8[8];
+        // column, 32 columns at a time); l adds the p before rounding, in
+        // four independent pairs of partial sums folded by a fixed tree.
+        // The scaling runs on packed fp32 pairs (lane by lane the same fmaf).
+        const uint64_t c2x2 = f32x2(c2, c2), negx2 = f32x2(neg, neg);
+        uint64_t r4[4];
 #pragma unroll
-        for (int j = 0; j < 8; ++j) r8[j] = 0.f;
+        for (int j = 0; j < 4; ++j) r4[j] = f32x2(0.f, 0.f);
 #pragma unroll
         for (int hh = 0; hh < 2; ++hh) {
           uint32_t pk[kKeys / 4];
 #pragma unroll
           for (int i = 0; i < kKeys / 4; ++i) {
             const int c0 = hh * (kKeys / 2) + 2 * i;
-            float e0 = ex2_approx(fmaf(__uint_as_float(sv[c0]), c2, neg));
-            float e1 = ex2_approx(fmaf(__uint_as_float(sv[c0 + 1]), c2, neg));
+            float t0, t1;
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1])),
+                                  c2x2, negx2),
+                        t0, t1);
+            float e0 = ex2_approx(t0);
+            float e1 = ex2_approx(t1);
             if (!full) {
               e0 = (c0 <= lim) ? e0 : 0.f;
               e1 = (c0 + 1 <= lim) ? e1 : 0.f;
             }
             pk[i] = pack_bf16x2(e0, e1);
-            r8[i & 7] += bf16_lo(pk[i]) + bf16_hi(pk[i]);
+            r4[i & 3] = add_f32x2(r4[i & 3], f32x2(e0, e1));
           }
           tmem_st16(tSr + hh * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
           tmem_st16(tSr + hh * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
         }
-#pragma unroll
-        for (int w = 4; w >= 1; w >>= 1)
-#pragma unroll
-          for (int j = 0; j < w; ++j) r8[j] += r8[j + w];
-        const float rs = r8[0];
+        r4[0] = add_f32x2(r4[0], r4[2]);
+        r4[1] = add_f32x2(r4[1], r4[3]);
+        r4[0] = add_f32x2(r4[0], r4[1]);
+        float rlo, rhi;
+        f32x2_split(r4[0], rlo, rhi);
+        const float rs = rlo + rhi;
         tmem_wait_st();
         l = fmaf(l, alpha, rs);
         // O is rescaled after P V of the previous tile has finished (it has:
@@ -423,6 +434,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       if (ok && wait_or_abort(bO(hb, last), (last >> 1) & 1, &s_abort, p.status)) {
         tc_fence_after();
         const bool valid = r < it.nrows;
+        const float inv_l = 1.f / l;  // one division per row; out = O * (1 / l)
         __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
                              ((size_t)(it.cu0 + it.tile * kRows + r) * p.H + it.head0 + hb) * D;
 #pragma unroll 1
@@ -434,14 +446,10 @@ __global__ void __launch_bounds__(kThreads, 1)
 #pragma unroll
             for (int i = 0; i < 32; i += 8) {
               uint4 v;
-              v.x = pack_bf16x2(finish_div(__uint_as_float(ov[i]), l),
-                                finish_div(__uint_as_float(ov[i + 1]), l));
-              v.y = pack_bf16x2(finish_div(__uint_as_float(ov[i + 2]), l),
-                                finish_div(__uint_as_float(ov[i + 3]), l));
-              v.z = pack_bf16x2(finish_div(__uint_as_float(ov[i + 4]), l),
-                                finish_div(__uint_as_float(ov[i + 5]), l));
-              v.w = pack_bf16x2(finish_div(__uint_as_float(ov[i + 6]), l),
-                                finish_div(__uint_as_float(ov[i + 7]), l));
+              v.x = pack_bf16x2(__uint_as_float(ov[i]) * inv_l, __uint_as_float(ov[i + 1]) * inv_l);
+              v.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv_l, __uint_as_float(ov[i + 3]) * inv_l);
+              v.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv_l, __uint_as_float(ov[i + 5]) * inv_l);
+              v.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv_l, __uint_as_float(ov[i + 7]) * inv_l);
               *reinterpret_cast<uint4*>(out + c * 32 + i) = v;
             }
           }
