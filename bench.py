@@ -505,7 +505,7 @@ def run_ours(args, rank, world, local_rank):
 
     prefill = None
     pf = wl.prefill_flops(step)
-    if pf:
+    if pf and args.mode == "batch" and g.dtype == "bf16":  # the tensor-core prefill ran
         pf_ms = statistics.mean(prefill_ms)
         tpeak, tkind = measured_bf16_peak(sustained=True)
         ach = pf / (pf_ms * 1e-3) / 1e12
