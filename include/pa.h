@@ -101,7 +101,8 @@ typedef enum { PA_MODE_BATCH_INVARIANT = 0, PA_MODE_ROW_INVARIANT = 1 } pa_mode;
 #define PA_FLAG_BLOCK_RANGE  0x02  /* block-table entry outside [0, num_blocks)          */
 #define PA_FLAG_CTX_RANGE    0x04  /* ctx_len < 0 or > max_blocks_per_seq * block_size    */
 #define PA_FLAG_QLEN_RANGE   0x08  /* q_len > ctx_len                                     */
-#define PA_FLAG_CU_SEQLENS   0x10  /* cu_seqlens_q not 0 .. T and non-decreasing          */
+#define PA_FLAG_CU_SEQLENS   0x10  /* cu_seqlens_q not 0 .. T and non-decreasing (then any
+                                      row, of any lane, may be left unwritten)            */
 #define PA_FLAG_WORKSPACE    0x20  /* the step needs more splits than the workspace holds */
 #define PA_FLAG_HOST_BOUND   0x40  /* a lane exceeds the host's max_q_len / max_ctx_len   */
 #define PA_FLAG_TIMEOUT      0x80  /* a bounded wait inside a kernel gave up              */

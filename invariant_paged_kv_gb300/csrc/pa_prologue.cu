@@ -120,59 +120,117 @@ __device__ __forceinline__ void owned_splits(const StepParams& p, int b, int sl,
   }
 }
 
-// Two passes over the lanes (blockDim at a time); each lane's data is read
-// once per pass. Pass 1 counts full split pairs of rows with splits longer
-// than kSplit ("long"), full kSplit pairs ("short"), tail pairs and prefill
-// tiles. Pass 2 scans the same counts and writes: long full pairs from the
-// front of the list, short full pairs after all long ones, tail pairs from
-// the back of the list, prefill tiles to a scratch list. Totals are checked
-// against the workspace; on overflow nothing runs.
-// In the KV-parallel modes the canonical entries of a lane depend on its
-// q_len and ctx_len alone (every owner and the merge lay them out alike);
-// malformed owner ranges only empty this owner's share (mode 1) or take the
-// lane's rows out of the merge (mode 2, owner_ok false).
-__device__ bool lane_counts(const StepParams& p, int b, bool report, int& q, int& c, int& cu0,
-                            long long (&cnt)[4], bool& split, bool& tiles, bool& owner_ok) {
+// Steps of up to kLaneCache lanes keep cu_seqlens_q, ctx_lens and each lane's
+// verdict in shared memory while the plan is built; larger ones read global
+// memory.
+constexpr int kLaneCache = 1024;
+struct LaneCache {
+  int cu[kLaneCache + 1];
+  int ctx[kLaneCache];
+  unsigned char ok[kLaneCache];
+};
+
+// Lane of flat row r: the b with cu[b] <= r < cu[b + 1] (binary search over
+// cu_seqlens_q), or -1 when cu_seqlens_q is not ordered around r.
+__device__ int lane_of_row(const StepParams& p, const LaneCache* lc, int r) {
+  const int* cu = lc ? lc->cu : p.cu_seqlens;
+  int lo = 0, hi = p.B - 1;  // the last b with cu[b] <= r
+  while (lo < hi) {
+    const int mid = (lo + hi + 1) >> 1;
+    if (cu[mid] <= r) lo = mid;
+    else hi = mid - 1;
+  }
+  return (cu[lo] <= r && r < cu[lo + 1]) ? lo : -1;
+}
+
+// What one flat row contributes to the plan. Four counters: full split pairs
+// of rows with splits longer than kSplit ("long"), full kSplit pairs
+// ("short"), tail pairs, and [3] -- prefill tiles of the row's lane (counted
+// at its first row) or, in the KV-parallel modes, the row's canonical
+// entries. In those modes the entries depend on q_len and ctx_len alone (every
+// owner and the merge lay them out alike); malformed owner ranges only empty
+// this owner's share (mode 1) or take the rows out of the merge (mode 2).
+struct RowPlan {
+  int b, q, c, cu0, j, keys, sl, nf, n, i0, i1;
+  bool split, tiles, owner_ok;
+};
+
+// A unit of the plan is a flat row when every row takes the split path, else
+// a lane (whose split path has at most its one decode row; a prefill lane
+// only adds its tiles). Returns the unit's row in r.
+__device__ bool row_counts(const StepParams& p, const LaneCache* lc, int u, int& r,
+                           long long (&cnt)[4], RowPlan& rp) {
   cnt[0] = cnt[1] = cnt[2] = cnt[3] = 0;
-  split = tiles = false;
-  owner_ok = true;
-  if (!lane_valid(p, b, report, q, c, cu0)) return false;
-  if (p.partials_mode && owner_ranges_bad(p, b, c)) {
-    owner_ok = false;
-    if (report) raise_flag(p.status, PA_FLAG_OWNER_RANGE);
+  rp.split = rp.tiles = false;
+  rp.owner_ok = true;
+  const bool by_row = p.split_all_rows;
+  if (u >= (by_row ? p.T : p.B)) return false;
+  rp.b = by_row ? lane_of_row(p, lc, u) : u;
+  if (rp.b < 0) return false;
+  if (lc) {
+    if (!lc->ok[rp.b]) return false;
+    rp.cu0 = lc->cu[rp.b];
+    rp.q = lc->cu[rp.b + 1] - rp.cu0;
+    rp.c = lc->ctx[rp.b];
+  } else if (!lane_valid(p, rp.b, false, rp.q, rp.c, rp.cu0)) {
+    return false;
   }
-  split = q >= 1 && (p.split_all_rows || q == 1);
-  tiles = !p.split_all_rows && q >= 2;
-  if (split) {  // row j attends c - q + j + 1 keys
-    for (int j = 0; j < q; ++j) {
-      const int keys = c - q + j + 1;
-      const int sl = split_len(keys);
-      const int nf = keys / sl, n = nf + ((keys % sl) != 0);
-      if (p.partials_mode) cnt[3] += n;  // canonical entries (no prefill tiles here)
-      int i0, i1;
-      owned_splits(p, b, sl, n, i0, i1);
-      if (!owner_ok) i0 = i1 = 0;
-      cnt[sl > kSplit ? 0 : 1] += max(0, min(i1, nf) - i0);
-      cnt[2] += (n > nf && n - 1 >= i0 && n - 1 < i1);
-    }
+  if (p.partials_mode && owner_ranges_bad(p, rp.b, rp.c)) rp.owner_ok = false;
+  r = by_row ? u : rp.cu0;
+  rp.j = r - rp.cu0;
+  rp.split = rp.q >= 1 && (p.split_all_rows || rp.q == 1);
+  rp.tiles = !p.split_all_rows && rp.q >= 2;
+  if (rp.split) {  // row j attends c - q + j + 1 keys
+    rp.keys = rp.c - rp.q + rp.j + 1;
+    rp.sl = split_len(rp.keys);
+    rp.nf = rp.keys / rp.sl;
+    rp.n = rp.nf + ((rp.keys % rp.sl) != 0);
+    if (p.partials_mode) cnt[3] = rp.n;  // canonical entries (no prefill tiles here)
+    owned_splits(p, rp.b, rp.sl, rp.n, rp.i0, rp.i1);
+    if (!rp.owner_ok) rp.i0 = rp.i1 = 0;
+    cnt[rp.sl > kSplit ? 0 : 1] = max(0, min(rp.i1, rp.nf) - rp.i0);
+    cnt[2] = (rp.n > rp.nf && rp.n - 1 >= rp.i0 && rp.n - 1 < rp.i1);
   }
-  if (tiles) cnt[3] = (q + kPrefillRows - 1) / kPrefillRows;
+  if (rp.tiles && rp.j == 0) cnt[3] = (rp.q + kPrefillRows - 1) / kPrefillRows;
   return true;
 }
 
+// The plan is built over units (blockDim at a time, two passes): pass 1
+// counts and scans, pass 2 scans again and writes -- long full pairs from the
+// front of the list, short full pairs after all long ones, tail pairs from the
+// back, prefill tiles to a scratch list. Units are in lane order, so the list
+// order is lane-major, row by row; when every row takes the split path each
+// row (of a 4000-row chunk as of a decode lane) is handled by its own thread. Lanes are validated (and their
+// flags raised) in a pass of their own. Totals are checked against the
+// workspace; on overflow nothing runs.
 __device__ void build_plan(const StepParams& p) {
   __shared__ int s_work[1024];
+  __shared__ LaneCache s_lanes;
   const int tid = threadIdx.x, nth = blockDim.x;
   const SplitPlan& pl = p.plan;
+  const LaneCache* lc = p.B <= kLaneCache ? &s_lanes : nullptr;
   for (int r = tid; r < p.T; r += nth) pl.row_info[r] = make_int4(0, -1, 0, -1);
-
-  long long total[4] = {0, 0, 0, 0};
-  for (int base = 0; base < p.B; base += nth) {
-    const int b = base + tid;
+  for (int b = tid; b < p.B; b += nth) {
     int q, c, cu0;
-    long long cnt[4] = {0, 0, 0, 0};
-    bool split, tiles, owner_ok;
-    if (b < p.B) lane_counts(p, b, true, q, c, cu0, cnt, split, tiles, owner_ok);
+    const bool ok = lane_valid(p, b, true, q, c, cu0);
+    if (ok && p.partials_mode && owner_ranges_bad(p, b, c))
+      raise_flag(p.status, PA_FLAG_OWNER_RANGE);
+    if (lc) {
+      s_lanes.cu[b] = p.cu_seqlens[b];
+      s_lanes.ctx[b] = p.ctx_lens[b];
+      s_lanes.ok[b] = ok ? 1 : 0;
+      if (b == p.B - 1) s_lanes.cu[p.B] = p.cu_seqlens[p.B];
+    }
+  }
+  __syncthreads();
+
+  const int units = p.split_all_rows ? p.T : p.B;
+  long long total[4] = {0, 0, 0, 0};
+  for (int base = 0; base < units; base += nth) {
+    long long cnt[4];
+    RowPlan rp;
+    int r;
+    row_counts(p, lc, base + tid, r, cnt, rp);
     long long ex[4], tot[4];
     block_scan4(cnt, ex, tot);
 #pragma unroll
@@ -187,49 +245,36 @@ __device__ void build_plan(const StepParams& p) {
 
   if (!overflow) {
     long long carry[4] = {0, 0, 0, 0};
-    for (int base = 0; base < p.B; base += nth) {
-      const int b = base + tid;
-      int q = 0, c = 0, cu0 = 0;
-      long long cnt[4] = {0, 0, 0, 0};
-      bool split = false, tiles = false, owner_ok = true;
-      if (b < p.B) lane_counts(p, b, false, q, c, cu0, cnt, split, tiles, owner_ok);
+    for (int base = 0; base < units; base += nth) {
+      long long cnt[4];
+      RowPlan rp;
+      int r = 0;
+      const bool ok = row_counts(p, lc, base + tid, r, cnt, rp);
       long long ex[4], tot[4];
       block_scan4(cnt, ex, tot);
-      if (split) {
-        long long lb = carry[0] + ex[0];             // long full pairs
-        long long sb = total[0] + carry[1] + ex[1];  // short full pairs
-        long long tb = carry[2] + ex[2];             // tail pair k sits at cap - 1 - k
-        long long eb = carry[3] + ex[3];             // KV-parallel: the lane's first entry
-        for (int j = 0; j < q; ++j) {
-          const int keys = c - q + j + 1;
-          const int sl = split_len(keys);
-          const int nf = keys / sl;
-          const bool has_tail = (keys % sl) != 0;
-          const int n = nf + (has_tail ? 1 : 0);
-          const int row = cu0 + j;
-          long long& fb = sl > kSplit ? lb : sb;
-          const long long tslot = cap - 1 - tb;
-          int i0, i1;
-          owned_splits(p, b, sl, n, i0, i1);
-          if (!owner_ok) i0 = i1 = 0;
-          if (p.partials_mode) {
-            pl.row_info[row] = make_int4((int)eb, keys, n, owner_ok ? b : -1);
-            eb += n;
-          } else {
-            pl.row_info[row] = make_int4((int)fb, has_tail ? (int)tslot : -1, n, b);
-          }
-          for (int i = i0; i < min(i1, nf); ++i) pl.pairs[fb++] = make_int4(row, i, b, keys);
-          if (has_tail && n - 1 >= i0 && n - 1 < i1) {
-            pl.pairs[tslot] = make_int4(row, nf, b, keys);
-            ++tb;
-          }
+      if (ok && rp.split) {
+        const long long lb = carry[0] + ex[0];             // long full pairs
+        const long long sb = total[0] + carry[1] + ex[1];  // short full pairs
+        const long long tb = carry[2] + ex[2];             // tail pair k sits at cap - 1 - k
+        const long long eb = carry[3] + ex[3];             // KV-parallel: the row's first entry
+        const long long fb = rp.sl > kSplit ? lb : sb;
+        const bool has_tail = rp.n > rp.nf;
+        const long long tslot = cap - 1 - tb;
+        if (p.partials_mode) {
+          pl.row_info[r] = make_int4((int)eb, rp.keys, rp.n, rp.owner_ok ? rp.b : -1);
+        } else {
+          pl.row_info[r] = make_int4((int)fb, has_tail ? (int)tslot : -1, rp.n, rp.b);
         }
+        long long f = fb;
+        for (int i = rp.i0; i < min(rp.i1, rp.nf); ++i) pl.pairs[f++] = make_int4(r, i, rp.b, rp.keys);
+        if (has_tail && rp.n - 1 >= rp.i0 && rp.n - 1 < rp.i1)
+          pl.pairs[tslot] = make_int4(r, rp.nf, rp.b, rp.keys);
       }
-      if (tiles) {
+      if (ok && rp.tiles && rp.j == 0) {
         const long long t0 = carry[3] + ex[3];
         for (int t = 0; t < cnt[3]; ++t) {
-          const int last = min(q, (t + 1) * kPrefillRows) - 1;
-          pl.ptiles_tmp[t0 + t] = make_int4(b, t, c - q + last, 0);
+          const int last = min(rp.q, (t + 1) * kPrefillRows) - 1;
+          pl.ptiles_tmp[t0 + t] = make_int4(rp.b, t, rp.c - rp.q + last, 0);
         }
       }
 #pragma unroll
