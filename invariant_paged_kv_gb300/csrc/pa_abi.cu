@@ -17,6 +17,9 @@ cudaError_t launch_decode_bf16(const StepParams& p, const CUtensorMap& k, const 
 cudaError_t launch_decode_fp8(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
                               long long max_items, cudaStream_t s);
 cudaError_t launch_split_f32(const StepParams& p, long long max_items, cudaStream_t s);
+cudaError_t launch_rows_bf16(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
+                             long long max_items, cudaStream_t s);
+int rows_group_size(int g);
 cudaError_t launch_combine(const StepParams& p, cudaStream_t s);
 cudaError_t launch_prefill_tc(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
                               const CUtensorMap& v, long long max_items, cudaStream_t s);
@@ -452,6 +455,10 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
   if (fp8) p.scale_log2 *= k_scale;
   p.plan = carve(workspace, cap, B, T, H, D);
   const bool prefill_tc = !p.split_all_rows && max_q_len >= 2;
+  // row-invariant bf16 steps: prefill rows in groups sharing key tiles
+  p.group_rows = (dtype == PA_BF16 && mode == PA_MODE_ROW_INVARIANT && max_q_len >= 2)
+                     ? rows_group_size(H / Hkv)
+                     : 0;
 
   CUtensorMap tmK, tmV, tmQ;
   if (fp8) {
@@ -481,6 +488,11 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
   if (prefill_tc) {
     const long long pitems = max_prefill_tiles(B, T) * Hkv * ((H / Hkv + 1) / 2);
     if (launch_prefill_tc(p, tmQ, tmK, tmV, pitems, s) != cudaSuccess) return PA_ERR_CUDA;
+    count_launches(1);
+  }
+  if (p.group_rows) {
+    // group records never outnumber the grouped rows' (row, split) entries
+    if (launch_rows_bf16(p, tmK, tmV, items, s) != cudaSuccess) return PA_ERR_CUDA;
     count_launches(1);
   }
   if (record(events, n_events, 3, s) != PA_OK) return PA_ERR_CUDA;

@@ -69,6 +69,9 @@ __device__ __forceinline__ int pair_slot(const SplitPlan& pl, int k, int nfull) 
 
 // Query rows per tile of the tensor-core prefill path.
 constexpr int kPrefillRows = 128;
+// Consumer warps of the row-invariant prefill-row kernel; a group holds
+// kRowWarps rows per row a warp carries.
+constexpr int kRowWarps = 8;
 
 struct StepParams {
   const void* q;
@@ -98,6 +101,12 @@ struct StepParams {
   // 2 = merge: fold every row's splits, split i read from the owner whose
   // range [key_bounds[w][lane], key_bounds[w + 1][lane]) holds its first key.
   // In modes 1 and 2 row_info[row] = {first entry, key count, splits, lane}.
+  // bf16 row-invariant steps: the rows of lanes with q_len >= 2 are computed
+  // in groups of up to group_rows consecutive rows sharing key tiles (their
+  // partials at row_info[row].x + split, the group records after the full
+  // pairs: pairs[header[1] + k], header[3] of them); decode lanes as usual.
+  // 0: no grouping.
+  int group_rows;
   int partials_mode;
   const int* key_lo;
   const int* key_hi;
@@ -173,6 +182,10 @@ __device__ __forceinline__ void fence_mbar_init() {
 
 __device__ __forceinline__ void fence_proxy_async_smem() {
   asm volatile("fence.proxy.async.shared::cta;" ::: "memory");
+}
+
+__device__ __forceinline__ void mbar_arrive(uint32_t bar) {
+  asm volatile("mbarrier.arrive.shared::cta.b64 _, [%0];" ::"r"(bar) : "memory");
 }
 
 __device__ __forceinline__ void mbar_expect_tx(uint32_t bar, uint32_t bytes) {

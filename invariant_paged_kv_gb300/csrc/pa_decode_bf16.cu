@@ -21,6 +21,7 @@
 // others leave (m, l, acc) for the fixed-order combine. Every item's
 // arithmetic depends only on its own row's q and keys: which warp runs it and
 // what else is in the step do not enter.
+#include "pa_split_bf16_row.cuh"
 #include "pa_split_items.cuh"
 
 namespace pa {
@@ -39,14 +40,6 @@ struct Tile {
   static constexpr int kWarpBytes = kStages * kStageBytes;
   static constexpr int kSmemBytes = kWarps * kWarpBytes + 1024;  // + alignment slack
 };
-
-// Shared address of 16-byte chunk c16 (0 .. D/8-1) of key row `tok` inside a
-// tile written by TMA with 128-byte swizzle: chunk index XOR (row mod 8).
-template <int D>
-__device__ __forceinline__ uint32_t tile_addr(uint32_t base, int tok, int c16) {
-  const int half = c16 >> 3, chunk = c16 & 7;
-  return base + half * Tile<D>::kHalfBytes + tok * 128 + ((chunk ^ (tok & 7)) << 4);
-}
 
 template <int D, int NT, bool kOwner>
 __global__ void __launch_bounds__(kWarps * 32, 2)
@@ -137,30 +130,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     if (c_item >= n_items) break;
     const Item it = load_item(p, c_item, nfull);
 
-    // q fragments (B operand of S^T = K Q^T): k = dims, n = heads of the group
-    uint32_t qf[NT][KS][2];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      const int hl = nt * 8 + gid;  // head within the group
-      const bool hv = hl < g;
-      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
-          qbase + ((size_t)it.row * p.H + (size_t)it.kvh * g + (hv ? hl : 0)) * D);
-#pragma unroll
-      for (int kk = 0; kk < KS; ++kk) {
-        qf[nt][kk][0] = hv ? qrow[(kk * 16 + 2 * tig) >> 1] : 0u;
-        qf[nt][kk][1] = hv ? qrow[(kk * 16 + 8 + 2 * tig) >> 1] : 0u;
-      }
-    }
-
-    float m[NT][2], l[NT][2];
-    float o[KS][NT][4];
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-      m[nt][0] = m[nt][1] = -INFINITY;
-      l[nt][0] = l[nt][1] = 0.f;
-#pragma unroll
-      for (int mt = 0; mt < KS; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
-    }
+    RowAcc<D, NT> ra;
+    ra.init(p, it.row, it.kvh, gid, tig);
 
 #pragma unroll 1
     for (int ch = 0; ch < it.nchunks; ++ch) {
@@ -202,53 +173,17 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 #pragma unroll
         for (int kk = 0; kk < KS; ++kk) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4(tile_addr<D>(ks, tok, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+          ldsm_x4(bf16_tile_addr(ks, tok, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(s[nt], a0, a1, a2, a3, qf[nt][kk][0], qf[nt][kk][1]);
+          for (int nt = 0; nt < NT; ++nt)
+            mma_bf16_16816(s[nt], a0, a1, a2, a3, ra.qf[nt][kk][0], ra.qf[nt][kk][1]);
         }
       }
 
       // online softmax over this chunk; this thread holds keys gid and gid + 8
       // for heads 2 * tig and 2 * tig + 1 of each n tile
-      const bool va = gid < nvalid, vb = gid + 8 < nvalid;
-      uint32_t pb[NT][2];
-      float alpha[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        float pa[2], pc[2];
-#pragma unroll
-        for (int e = 0; e < 2; ++e) {
-          const float ta = va ? __fmul_rn(s[nt][e], p.scale_log2) : -INFINITY;
-          const float tb = vb ? __fmul_rn(s[nt][2 + e], p.scale_log2) : -INFINITY;
-          float mx = fmaxf(ta, tb);
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
-          mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
-          const float mn = fmaxf(m[nt][e], mx);
-          alpha[nt][e] = ex2_approx(m[nt][e] - mn);
-          m[nt][e] = mn;
-          pa[e] = ex2_approx(ta - mn);
-          pc[e] = ex2_approx(tb - mn);
-        }
-        pb[nt][0] = pack_bf16x2(pa[0], pa[1]);  // key gid,     heads 2tig, 2tig+1
-        pb[nt][1] = pack_bf16x2(pc[0], pc[1]);  // key gid + 8, heads 2tig, 2tig+1
-        l[nt][0] = fmaf(l[nt][0], alpha[nt][0], bf16_lo(pb[nt][0]) + bf16_lo(pb[nt][1]));
-        l[nt][1] = fmaf(l[nt][1], alpha[nt][1], bf16_hi(pb[nt][0]) + bf16_hi(pb[nt][1]));
-#pragma unroll
-        for (int mt = 0; mt < KS; ++mt) {
-          o[mt][nt][0] *= alpha[nt][0];
-          o[mt][nt][1] *= alpha[nt][1];
-          o[mt][nt][2] *= alpha[nt][0];
-          o[mt][nt][3] *= alpha[nt][1];
-        }
-      }
-      // P^T (keys x heads, accumulator layout) -> B operand (k = keys, n = heads)
       uint32_t pbt[NT][2];
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt) {
-        pbt[nt][0] = movmatrix_trans(pb[nt][0]);
-        pbt[nt][1] = movmatrix_trans(pb[nt][1]);
-      }
+      ra.softmax(s, nvalid, gid, p.scale_log2, pbt);
 
       // O^T += V^T P^T : 16 dims x 8 heads per (m tile, n tile)
       {
@@ -256,9 +191,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
 #pragma unroll
         for (int mt = 0; mt < KS; ++mt) {
           uint32_t a0, a1, a2, a3;
-          ldsm_x4_trans(tile_addr<D>(vs, tok, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
+          ldsm_x4_trans(bf16_tile_addr(vs, tok, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
 #pragma unroll
-          for (int nt = 0; nt < NT; ++nt) mma_bf16_16816(o[mt][nt], a0, a1, a2, a3, pbt[nt][0], pbt[nt][1]);
+          for (int nt = 0; nt < NT; ++nt)
+            mma_bf16_16816(ra.o[mt][nt], a0, a1, a2, a3, pbt[nt][0], pbt[nt][1]);
         }
       }
       __syncwarp();  // every lane is done reading this stage
@@ -267,62 +203,10 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     }
 
     // ---- finish the item ----
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) {
-#pragma unroll
-      for (int e = 0; e < 2; ++e) {
-        float v = l[nt][e];
-        v += __shfl_xor_sync(0xffffffffu, v, 4);
-        v += __shfl_xor_sync(0xffffffffu, v, 8);
-        v += __shfl_xor_sync(0xffffffffu, v, 16);
-        l[nt][e] = v;
-      }
-    }
-    const bool single = it.single && !kOwner;
-    const size_t head0 = (size_t)it.row * p.H + (size_t)it.kvh * g;  // first head of the group
-    if (single) {
-      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int hl = nt * 8 + 2 * tig + (r & 1);
-          if (hl < g) {
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-              const int d = mt * 16 + gid + (r >> 1) * 8;
-              out[(head0 + hl) * D + d] = __float2bfloat16_rn(finish_div(o[mt][nt][r], l[nt][r & 1]));
-            }
-          }
-        }
-    } else {
-      const size_t ph0 =
-          (size_t)(kOwner ? (long long)p.plan.row_info[it.row].x + it.t0 / split_len(it.keys)
-                          : (long long)it.pair) * p.H +
-          (size_t)it.kvh * g;
-#pragma unroll
-      for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-        for (int r = 0; r < 4; ++r) {
-          const int hl = nt * 8 + 2 * tig + (r & 1);
-          if (hl < g) {
-#pragma unroll
-            for (int mt = 0; mt < KS; ++mt) {
-              const int d = mt * 16 + gid + (r >> 1) * 8;
-              p.plan.acc[(ph0 + hl) * D + d] = o[mt][nt][r];
-            }
-          }
-        }
-      if (gid == 0) {
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-#pragma unroll
-          for (int e = 0; e < 2; ++e) {
-            const int hl = nt * 8 + 2 * tig + e;
-            if (hl < g) p.plan.ml[ph0 + hl] = make_float2(m[nt][e], l[nt][e]);
-          }
-      }
-    }
+    ra.finish(p, it.row, it.kvh, it.single && !kOwner,
+              kOwner ? (long long)p.plan.row_info[it.row].x + it.t0 / split_len(it.keys)
+                     : (long long)it.pair,
+              gid, tig);
   }
 }
 

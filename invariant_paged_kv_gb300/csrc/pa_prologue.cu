@@ -64,27 +64,33 @@ __device__ bool lane_valid(const StepParams& p, int b, bool report, int& q, int&
   return bad == 0;
 }
 
-// Exclusive block-wide scan of four counters; returns the block totals.
-__device__ void block_scan4(const long long (&v)[4], long long (&ex)[4], long long (&tot)[4]) {
-  __shared__ long long sm[4][32];
+// Counters of the plan scan (see row_counts).
+constexpr int kCounters = 5;
+
+// Exclusive block-wide scan of the plan's counters; returns the block totals.
+__device__ void block_scan(const long long (&v)[kCounters], long long (&ex)[kCounters],
+                           long long (&tot)[kCounters]) {
+  __shared__ long long sm[kCounters][32];
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5, nw = blockDim.x >> 5;
-  long long inc[4] = {v[0], v[1], v[2], v[3]};  // inclusive within the warp
+  long long inc[kCounters];  // inclusive within the warp
+#pragma unroll
+  for (int k = 0; k < kCounters; ++k) inc[k] = v[k];
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kCounters; ++k) {
       const long long x = __shfl_up_sync(0xffffffffu, inc[k], o);
       if (lane >= o) inc[k] += x;
     }
   }
   if (lane == 31) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) sm[k][warp] = inc[k];
+    for (int k = 0; k < kCounters; ++k) sm[k][warp] = inc[k];
   }
   __syncthreads();
   if (warp == 0) {
 #pragma unroll
-    for (int k = 0; k < 4; ++k) {
+    for (int k = 0; k < kCounters; ++k) {
       long long x = lane < nw ? sm[k][lane] : 0;
 #pragma unroll
       for (int o = 1; o < 32; o <<= 1) {
@@ -96,7 +102,7 @@ __device__ void block_scan4(const long long (&v)[4], long long (&ex)[4], long lo
   }
   __syncthreads();
 #pragma unroll
-  for (int k = 0; k < 4; ++k) {
+  for (int k = 0; k < kCounters; ++k) {
     ex[k] = (warp ? sm[k][warp - 1] : 0) + inc[k] - v[k];
     tot[k] = sm[k][nw - 1];
   }
@@ -143,15 +149,16 @@ __device__ int lane_of_row(const StepParams& p, const LaneCache* lc, int r) {
   return (cu[lo] <= r && r < cu[lo + 1]) ? lo : -1;
 }
 
-// What one flat row contributes to the plan. Four counters: full split pairs
-// of rows with splits longer than kSplit ("long"), full kSplit pairs
-// ("short"), tail pairs, and [3] -- prefill tiles of the row's lane (counted
-// at its first row) or, in the KV-parallel modes, the row's canonical
-// entries. In those modes the entries depend on q_len and ctx_len alone (every
-// owner and the merge lay them out alike); malformed owner ranges only empty
-// this owner's share (mode 1) or take the rows out of the merge (mode 2).
+// What one flat row contributes to the plan. Counters: full split pairs of
+// rows with splits longer than kSplit ("long"), full kSplit pairs ("short"),
+// tail pairs, [3] -- prefill tiles of the row's lane (counted at its first
+// row) or, in the KV-parallel modes and for grouped prefill rows, the row's
+// entries -- and [4], the records of the prefill-row group the row starts.
+// In the KV-parallel modes the entries depend on q_len and ctx_len alone
+// (every owner and the merge lay them out alike); malformed owner ranges only
+// empty this owner's share (mode 1) or take the rows out of the merge (mode 2).
 struct RowPlan {
-  int b, q, c, cu0, j, keys, sl, nf, n, i0, i1;
+  int b, q, c, cu0, j, keys, sl, nf, n, i0, i1, g1;
   bool split, tiles, owner_ok;
 };
 
@@ -159,8 +166,8 @@ struct RowPlan {
 // a lane (whose split path has at most its one decode row; a prefill lane
 // only adds its tiles). Returns the unit's row in r.
 __device__ bool row_counts(const StepParams& p, const LaneCache* lc, int u, int& r,
-                           long long (&cnt)[4], RowPlan& rp) {
-  cnt[0] = cnt[1] = cnt[2] = cnt[3] = 0;
+                           long long (&cnt)[kCounters], RowPlan& rp) {
+  for (int k = 0; k < kCounters; ++k) cnt[k] = 0;
   rp.split = rp.tiles = false;
   rp.owner_ok = true;
   const bool by_row = p.split_all_rows;
@@ -186,6 +193,27 @@ __device__ bool row_counts(const StepParams& p, const LaneCache* lc, int u, int&
     rp.nf = rp.keys / rp.sl;
     rp.n = rp.nf + ((rp.keys % rp.sl) != 0);
     if (p.partials_mode) cnt[3] = rp.n;  // canonical entries (no prefill tiles here)
+    if (p.group_rows && rp.q >= 2) {     // a grouped prefill row: entries only
+      cnt[3] = rp.n;
+      rp.i0 = rp.i1 = 0;                 // no pairs of its own
+      // The lane's rows with split length sl form one run (split_len grows
+      // with the key count: sl = kSplit up to kSplit * kMaxSplits keys, else
+      // sl covers (sl / 2 * kMaxSplits, sl * kMaxSplits]); groups of
+      // group_rows rows start at the run's first row. A group has one record
+      // per split of its last row: {first row, rows | split << 8, lane, keys
+      // of the first row}.
+      const long long kmin = rp.sl == kSplit ? 1 : (long long)(rp.sl / 2) * kMaxSplits + 1;
+      const long long kmax = (long long)rp.sl * kMaxSplits;
+      const long long key0 = (long long)rp.c - rp.q + 1;  // keys of the lane's row 0
+      const int js = (int)max(0LL, kmin - key0);
+      const int je = (int)min((long long)rp.q, kmax - key0 + 1);
+      if ((rp.j - js) % p.group_rows == 0) {
+        rp.g1 = min(rp.j + p.group_rows, je);
+        const int keys_last = rp.c - rp.q + rp.g1;
+        cnt[4] = (keys_last + rp.sl - 1) / rp.sl;
+      }
+      return true;
+    }
     owned_splits(p, rp.b, rp.sl, rp.n, rp.i0, rp.i1);
     if (!rp.owner_ok) rp.i0 = rp.i1 = 0;
     cnt[rp.sl > kSplit ? 0 : 1] = max(0, min(rp.i1, rp.nf) - rp.i0);
@@ -225,33 +253,35 @@ __device__ void build_plan(const StepParams& p) {
   __syncthreads();
 
   const int units = p.split_all_rows ? p.T : p.B;
-  long long total[4] = {0, 0, 0, 0};
+  long long total[kCounters] = {0, 0, 0, 0, 0};
   for (int base = 0; base < units; base += nth) {
-    long long cnt[4];
+    long long cnt[kCounters];
     RowPlan rp;
     int r;
     row_counts(p, lc, base + tid, r, cnt, rp);
-    long long ex[4], tot[4];
-    block_scan4(cnt, ex, tot);
+    long long ex[kCounters], tot[kCounters];
+    block_scan(cnt, ex, tot);
 #pragma unroll
-    for (int k = 0; k < 4; ++k) total[k] += tot[k];
+    for (int k = 0; k < kCounters; ++k) total[k] += tot[k];
   }
   const int cap = pl.capacity;
   const long long nfull = total[0] + total[1];
-  const bool overflow = nfull + total[2] > cap ||
-                        total[3] > (p.partials_mode ? pl.entry_capacity : (long long)pl.ptile_capacity);
+  const bool overflow =
+      nfull + total[2] + (p.group_rows ? total[3] : 0) > cap ||
+      (!p.group_rows &&
+       total[3] > (p.partials_mode ? pl.entry_capacity : (long long)pl.ptile_capacity));
   if (overflow && tid == 0) raise_flag(p.status, PA_FLAG_WORKSPACE);
   __syncthreads();
 
   if (!overflow) {
-    long long carry[4] = {0, 0, 0, 0};
+    long long carry[kCounters] = {0, 0, 0, 0, 0};
     for (int base = 0; base < units; base += nth) {
-      long long cnt[4];
+      long long cnt[kCounters];
       RowPlan rp;
       int r = 0;
       const bool ok = row_counts(p, lc, base + tid, r, cnt, rp);
-      long long ex[4], tot[4];
-      block_scan4(cnt, ex, tot);
+      long long ex[kCounters], tot[kCounters];
+      block_scan(cnt, ex, tot);
       if (ok && rp.split) {
         const long long lb = carry[0] + ex[0];             // long full pairs
         const long long sb = total[0] + carry[1] + ex[1];  // short full pairs
@@ -260,7 +290,14 @@ __device__ void build_plan(const StepParams& p) {
         const long long fb = rp.sl > kSplit ? lb : sb;
         const bool has_tail = rp.n > rp.nf;
         const long long tslot = cap - 1 - tb;
-        if (p.partials_mode) {
+        if (p.group_rows && rp.q >= 2) {  // its entries follow the full pairs
+          pl.row_info[r] = make_int4((int)(nfull + eb), -1, rp.n, rp.b);
+          // the records of the group it starts, after the full pairs too
+          // (never more records than grouped entries: each holds a row's split)
+          long long k = nfull + carry[4] + ex[4];
+          for (int i = 0; i < cnt[4]; ++i)
+            pl.pairs[k++] = make_int4(r, (rp.g1 - rp.j) | (i << 8), rp.b, rp.keys);
+        } else if (p.partials_mode) {
           pl.row_info[r] = make_int4((int)eb, rp.keys, rp.n, rp.owner_ok ? rp.b : -1);
         } else {
           pl.row_info[r] = make_int4((int)fb, has_tail ? (int)tslot : -1, rp.n, rp.b);
@@ -268,7 +305,7 @@ __device__ void build_plan(const StepParams& p) {
         long long f = fb;
         for (int i = rp.i0; i < min(rp.i1, rp.nf); ++i) pl.pairs[f++] = make_int4(r, i, rp.b, rp.keys);
         if (has_tail && rp.n - 1 >= rp.i0 && rp.n - 1 < rp.i1)
-          pl.pairs[tslot] = make_int4(r, rp.nf, rp.b, rp.keys);
+          pl.pairs[tslot] = make_int4(r, rp.nf, rp.b, rp.keys);  // none for grouped rows
       }
       if (ok && rp.tiles && rp.j == 0) {
         const long long t0 = carry[3] + ex[3];
@@ -278,10 +315,10 @@ __device__ void build_plan(const StepParams& p) {
         }
       }
 #pragma unroll
-      for (int k = 0; k < 4; ++k) carry[k] += tot[k];
+      for (int k = 0; k < kCounters; ++k) carry[k] += tot[k];
     }
   }
-  const int n = (overflow || p.partials_mode) ? 0 : (int)total[3];
+  const int n = (overflow || p.partials_mode || p.group_rows) ? 0 : (int)total[3];
   __syncthreads();
   // prefill tiles heaviest first (position of the tile's last row; ties by
   // list order) when there are at most blockDim of them: the order only
@@ -305,6 +342,7 @@ __device__ void build_plan(const StepParams& p) {
     pl.header[0] = overflow ? 0 : (int)(nfull + total[2]);
     pl.header[1] = overflow ? 0 : (int)nfull;
     pl.header[2] = n;
+    pl.header[3] = overflow ? 0 : (int)total[4];
   }
 }
 

@@ -106,7 +106,8 @@ def _random_cuts(lo, hi, n, seed):
 
 
 GEOMS = [wl.Geometry(32, 8, 128, 16, "bf16"), wl.Geometry(40, 8, 128, 16, "bf16"),
-         wl.Geometry(8, 8, 64, 32, "bf16"), wl.Geometry(4, 2, 64, 16, "f32"),
+         wl.Geometry(8, 8, 64, 32, "bf16"), wl.Geometry(32, 2, 128, 16, "bf16"),
+         wl.Geometry(16, 1, 64, 32, "bf16"), wl.Geometry(4, 2, 64, 16, "f32"),
          wl.Geometry(40, 8, 128, 16, "fp8"), wl.Geometry(16, 1, 64, 32, "fp8")]
 
 
