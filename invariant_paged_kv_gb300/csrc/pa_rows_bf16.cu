@@ -8,14 +8,22 @@
 // kernel's item -- a CTA takes a group of consecutive rows of one lane with
 // the same split length, one split and one kv head: a producer warp streams
 // the split's 16-key K / V tiles once (TMA, 128-byte swizzle) into an 8-stage
-// ring that 8 consumer warps read. Consumer warp w carries RPW adjacent rows
-// (RPW = 2 when the GQA group fits one mma N tile, else 1), each with exactly
-// the decode kernel's per-row code (RowAcc: the same S^T and O^T products over
-// the same 16-key chunks in the same order, the same online softmax, the same
-// finish); the rows of a warp share the K / V fragments of a chunk and give
-// the warp independent mma chains. A row never touches a chunk past its own
-// key count (it skips the rest of the group's chunks), so its bits are those
-// it would have as a decode row. Every wait is bounded (PA_FLAG_TIMEOUT).
+// ring that 8 consumer warps read.
+//
+// The decode kernel puts the g query heads of one row on the N side of its
+// mma.sync products (S^T = K Q^T, O^T = V^T P^T), one column per head, and
+// pads a short group with empty columns. Every output column of those
+// products, and every step of the online softmax (a max and a sum over keys,
+// per column), depends on its own column alone. So here the columns are
+// (row, head) pairs packed densely across rows: column k of the group is row
+// k / g, head k % g, and warp w owns columns 16 w .. 16 w + 15 (two N tiles).
+// Each column goes through exactly the decode kernel's sequence of
+// operations -- the same 16-key chunks in the same order, the same products,
+// the same max / exp2 / bf16 rounding / sum / rescale, the same finish -- so
+// its bits are those of its row computed as a decode row. A column whose row
+// has no keys left in a chunk skips the chunk's update (its max, sum and
+// rescale factor stay as they are, its p values are zero).
+// Every wait is bounded (PA_FLAG_TIMEOUT).
 #include "pa_split_bf16_row.cuh"
 
 namespace pa {
@@ -23,6 +31,8 @@ namespace pa {
 namespace {
 
 constexpr int kRW = kRowWarps;  // consumer warps
+constexpr int kNTW = 2;         // 8-column N tiles per consumer warp
+constexpr int kCols = kRW * kNTW * 8;
 constexpr int kRStages = 8;
 constexpr int kRThreads = (kRW + 1) * 32;
 
@@ -66,58 +76,90 @@ __device__ __forceinline__ bool wait_r(uint32_t bar, uint32_t parity, volatile i
   return true;
 }
 
-// One 16-key chunk for rows FIRST .. RPW-1 of the warp (the rows still inside
-// their key range; the later a row, the more keys it has): the K fragments
-// feed every row's S^T chain, the V fragments every row's O^T update.
-template <int D, int NT, int RPW, int FIRST>
-__device__ __forceinline__ void chunk_rows(RowAcc<D, NT> (&ra)[RPW], const int (&nvalid)[RPW],
-                                           uint32_t ks, uint32_t vs, int lane, int gid,
-                                           float scale_log2) {
-  constexpr int KS = D / 16;
-  // S^T = K Q^T : 16 keys x 8 heads per n tile
-  float s[RPW][NT][4];
-#pragma unroll
-  for (int i = FIRST; i < RPW; ++i)
-#pragma unroll
-    for (int nt = 0; nt < NT; ++nt) s[i][nt][0] = s[i][nt][1] = s[i][nt][2] = s[i][nt][3] = 0.f;
-  {
-    const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
-#pragma unroll
-    for (int kk = 0; kk < KS; ++kk) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4(bf16_tile_addr(ks, tok, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
-#pragma unroll
-      for (int i = FIRST; i < RPW; ++i)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_bf16_16816(s[i][nt], a0, a1, a2, a3, ra[i].qf[nt][kk][0], ra[i].qf[nt][kk][1]);
-    }
-  }
-  uint32_t pbt[RPW][NT][2];
-#pragma unroll
-  for (int i = FIRST; i < RPW; ++i) ra[i].softmax(s[i], nvalid[i], gid, scale_log2, pbt[i]);
-  // O^T += V^T P^T : 16 dims x 8 heads per (m tile, n tile)
-  {
-    const int tok = (lane & 7) + (lane >> 4) * 8;
-#pragma unroll
-    for (int mt = 0; mt < KS; ++mt) {
-      uint32_t a0, a1, a2, a3;
-      ldsm_x4_trans(bf16_tile_addr(vs, tok, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
-#pragma unroll
-      for (int i = FIRST; i < RPW; ++i)
-#pragma unroll
-        for (int nt = 0; nt < NT; ++nt)
-          mma_bf16_16816(ra[i].o[mt][nt], a0, a1, a2, a3, pbt[i][nt][0], pbt[i][nt][1]);
-    }
-  }
-}
+// The state of one warp's 16 columns for one (group, split, kv head). This
+// thread holds keys gid and gid + 8 of each chunk for columns 2 tig and
+// 2 tig + 1 of each N tile (index e), and the q fragment of column gid.
+template <int D>
+struct ColAcc {
+  static constexpr int KS = D / 16;
+  float m[kNTW][2], l[kNTW][2];
+  float o[KS][kNTW][4];
+  uint32_t qf[kNTW][KS][2];
 
-template <int D, int NT, int RPW>
+  __device__ __forceinline__ void init(const StepParams& p, const Group& gr, int kvh, int col0,
+                                       int g, int gid, int tig) {
+    const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(p.q);
+#pragma unroll
+    for (int nt = 0; nt < kNTW; ++nt) {
+      const int c = col0 + nt * 8 + gid;
+      const int j = c / g, h = c - j * g;
+      const bool cv = j < gr.nrows;
+      const uint32_t* qrow = reinterpret_cast<const uint32_t*>(
+          qbase + ((size_t)(gr.r0 + (cv ? j : 0)) * p.H + (size_t)kvh * g + (cv ? h : 0)) * D);
+#pragma unroll
+      for (int kk = 0; kk < KS; ++kk) {
+        qf[nt][kk][0] = cv ? qrow[(kk * 16 + 2 * tig) >> 1] : 0u;
+        qf[nt][kk][1] = cv ? qrow[(kk * 16 + 8 + 2 * tig) >> 1] : 0u;
+      }
+      m[nt][0] = m[nt][1] = -INFINITY;
+      l[nt][0] = l[nt][1] = 0.f;
+#pragma unroll
+      for (int mt = 0; mt < KS; ++mt) o[mt][nt][0] = o[mt][nt][1] = o[mt][nt][2] = o[mt][nt][3] = 0.f;
+    }
+  }
+
+  // One chunk: s in the accumulator layout of S^T (keys gid / gid + 8),
+  // nvalid[nt][e] keys of it real for column (nt, e) (<= 0: the column sits
+  // the chunk out). For a column that takes part, the same operations in the
+  // same order as the decode kernel's row.
+  __device__ __forceinline__ void softmax(const float (&s)[kNTW][4], const int (&nvalid)[kNTW][2],
+                                          int gid, float scale_log2,
+                                          uint32_t (&pbt)[kNTW][2]) {
+#pragma unroll
+    for (int nt = 0; nt < kNTW; ++nt) {
+      float pa[2], pc[2], alpha[2];
+#pragma unroll
+      for (int e = 0; e < 2; ++e) {
+        const bool va = gid < nvalid[nt][e], vb = gid + 8 < nvalid[nt][e];
+        const float ta = va ? __fmul_rn(s[nt][e], scale_log2) : -INFINITY;
+        const float tb = vb ? __fmul_rn(s[nt][2 + e], scale_log2) : -INFINITY;
+        float mx = fmaxf(ta, tb);
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 4));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 8));
+        mx = fmaxf(mx, __shfl_xor_sync(0xffffffffu, mx, 16));
+        const bool act = nvalid[nt][e] > 0;
+        const float mn = act ? fmaxf(m[nt][e], mx) : m[nt][e];
+        alpha[e] = act ? ex2_approx(m[nt][e] - mn) : 1.f;
+        m[nt][e] = mn;
+        pa[e] = act ? ex2_approx(ta - mn) : 0.f;
+        pc[e] = act ? ex2_approx(tb - mn) : 0.f;
+      }
+      const uint32_t pb0 = pack_bf16x2(pa[0], pa[1]);  // key gid,     columns 2tig, 2tig+1
+      const uint32_t pb1 = pack_bf16x2(pc[0], pc[1]);  // key gid + 8, columns 2tig, 2tig+1
+      // l * 1 + 0 == l: a column sitting out keeps its sum
+      l[nt][0] = fmaf(l[nt][0], alpha[0], bf16_lo(pb0) + bf16_lo(pb1));
+      l[nt][1] = fmaf(l[nt][1], alpha[1], bf16_hi(pb0) + bf16_hi(pb1));
+      if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
+#pragma unroll
+        for (int mt = 0; mt < KS; ++mt) {
+          o[mt][nt][0] *= alpha[0];
+          o[mt][nt][1] *= alpha[1];
+          o[mt][nt][2] *= alpha[0];
+          o[mt][nt][3] *= alpha[1];
+        }
+      }
+      pbt[nt][0] = movmatrix_trans(pb0);
+      pbt[nt][1] = movmatrix_trans(pb1);
+    }
+  }
+};
+
+template <int D>
 __global__ void __launch_bounds__(kRThreads, 1)
     rows_bf16_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
   using TL = RTile<D>;
-  static_assert(RPW == 1 || RPW == 2, "rows per warp");
+  constexpr int KS = D / 16;
   extern __shared__ uint8_t dsmem[];
   // zeroed[st]: warp 0 has zeroed the V rows past the group's keys in stage
   // st (a group's last, partial chunk); one phase per such use of the stage,
@@ -128,6 +170,7 @@ __global__ void __launch_bounds__(kRThreads, 1)
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
+  const int g = p.H / p.Hkv;
   const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
   if (threadIdx.x == 0) {
     for (int i = 0; i < kRStages; ++i) {
@@ -180,16 +223,24 @@ __global__ void __launch_bounds__(kRThreads, 1)
       }
       f = __shfl_sync(0xffffffffu, f, 0);
     } else {
-      // ------------------------- consumer: RPW rows -------------------------
-      RowAcc<D, NT> ra[RPW];
-      int len[RPW], my_nch[RPW];
+      // ---------------------- consumer: 16 (row, head) columns ----------------
+      const int col0 = warp * (kNTW * 8);
+      // keys of this split for the columns this thread holds in the softmax
+      // layout (<= 0: the column's row lacks the split, or no such row)
+      int len[kNTW][2];
+      int len_w = 0;
 #pragma unroll
-      for (int i = 0; i < RPW; ++i) {
-        const int j = warp * RPW + i;  // row of the group
-        len[i] = (j < gr.nrows) ? min(sl, gr.keys0 + j - t0) : 0;  // <= 0: no such split
-        my_nch[i] = len[i] > 0 ? (len[i] + kChunk - 1) / kChunk : 0;
-        if (my_nch[i] > 0) ra[i].init(p, gr.r0 + j, kvh, gid, tig);
-      }
+      for (int nt = 0; nt < kNTW; ++nt)
+#pragma unroll
+        for (int e = 0; e < 2; ++e) {
+          const int j = (col0 + nt * 8 + 2 * tig + e) / g;
+          len[nt][e] = j < gr.nrows ? min(sl, gr.keys0 + j - t0) : 0;
+          len_w = max(len_w, len[nt][e]);
+        }
+      len_w = __reduce_max_sync(0xffffffffu, len_w);
+      const int nch_w = (len_w + kChunk - 1) / kChunk;  // chunks any column of the warp needs
+      ColAcc<D> ca;
+      if (nch_w > 0) ca.init(p, gr, kvh, col0, g, gid, tig);
       bool ok = true;
       for (int ch = 0; ch < nch; ++ch, ++f) {
         const uint32_t st = f % kRStages;
@@ -221,29 +272,90 @@ __global__ void __launch_bounds__(kRThreads, 1)
           }
           zbits ^= 1u << st;
         }
-        int nvalid[RPW];
+        if (ch < nch_w) {
+          // S^T = K Q^T : 16 keys x 8 columns per N tile
+          float s[kNTW][4];
 #pragma unroll
-        for (int i = 0; i < RPW; ++i) nvalid[i] = min(kChunk, len[i] - ch * kChunk);
-        // the rows inside their key range at this chunk form a suffix of the
-        // warp's rows (my_nch grows with the row)
-        if (ch < my_nch[0]) {
-          chunk_rows<D, NT, RPW, 0>(ra, nvalid, ks, vs, lane, gid, p.scale_log2);
-        } else if (RPW == 2 && ch < my_nch[RPW - 1]) {
-          chunk_rows<D, NT, RPW, RPW - 1>(ra, nvalid, ks, vs, lane, gid, p.scale_log2);
+          for (int nt = 0; nt < kNTW; ++nt) s[nt][0] = s[nt][1] = s[nt][2] = s[nt][3] = 0.f;
+          {
+            const int tok = (lane & 7) + ((lane >> 3) & 1) * 8;
+#pragma unroll
+            for (int kk = 0; kk < KS; ++kk) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4(bf16_tile_addr(ks, tok, kk * 2 + (lane >> 4)), a0, a1, a2, a3);
+#pragma unroll
+              for (int nt = 0; nt < kNTW; ++nt)
+                mma_bf16_16816(s[nt], a0, a1, a2, a3, ca.qf[nt][kk][0], ca.qf[nt][kk][1]);
+            }
+          }
+          int nvalid[kNTW][2];
+#pragma unroll
+          for (int nt = 0; nt < kNTW; ++nt)
+#pragma unroll
+            for (int e = 0; e < 2; ++e) nvalid[nt][e] = min(kChunk, len[nt][e] - ch * kChunk);
+          uint32_t pbt[kNTW][2];
+          ca.softmax(s, nvalid, gid, p.scale_log2, pbt);
+          // O^T += V^T P^T : 16 dims x 8 columns per (m tile, N tile)
+          {
+            const int tok = (lane & 7) + (lane >> 4) * 8;
+#pragma unroll
+            for (int mt = 0; mt < KS; ++mt) {
+              uint32_t a0, a1, a2, a3;
+              ldsm_x4_trans(bf16_tile_addr(vs, tok, mt * 2 + ((lane >> 3) & 1)), a0, a1, a2, a3);
+#pragma unroll
+              for (int nt = 0; nt < kNTW; ++nt)
+                mma_bf16_16816(ca.o[mt][nt], a0, a1, a2, a3, pbt[nt][0], pbt[nt][1]);
+            }
+          }
         }
         __syncwarp();  // every lane is done reading this stage
         if (lane == 0) mbar_arrive(smem_u32(&empty[st]));
       }
-      if (ok) {
+      if (ok && nch_w > 0) {
+        // finish: l summed over the warp's key lanes, then per column either
+        // the normalised output (a row with one split) or the partial
 #pragma unroll
-        for (int i = 0; i < RPW; ++i) {
-          if (my_nch[i] > 0) {
-            const int r = gr.r0 + warp * RPW + i;
-            const int keys = gr.keys0 + warp * RPW + i;
-            const int n = (keys + sl - 1) / sl;  // this row's splits
-            ra[i].finish(p, r, kvh, n == 1, (long long)p.plan.row_info[r].x + gr.split, gid, tig);
+        for (int nt = 0; nt < kNTW; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            float v = ca.l[nt][e];
+            v += __shfl_xor_sync(0xffffffffu, v, 4);
+            v += __shfl_xor_sync(0xffffffffu, v, 8);
+            v += __shfl_xor_sync(0xffffffffu, v, 16);
+            ca.l[nt][e] = v;
           }
-        }
+#pragma unroll
+        for (int nt = 0; nt < kNTW; ++nt)
+#pragma unroll
+          for (int e = 0; e < 2; ++e) {
+            if (len[nt][e] <= 0) continue;
+            const int c = col0 + nt * 8 + 2 * tig + e;
+            const int j = c / g, h = c - j * g;
+            const int r = gr.r0 + j;
+            const int keys = gr.keys0 + j;
+            const size_t head = (size_t)r * p.H + (size_t)kvh * g + h;
+            if ((keys + sl - 1) / sl == 1) {  // one split: the output itself
+              __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out);
+#pragma unroll
+              for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi) {
+                  const int d = mt * 16 + gid + hi * 8;
+                  out[head * D + d] = __float2bfloat16_rn(finish_div(ca.o[mt][nt][hi * 2 + e], ca.l[nt][e]));
+                }
+            } else {
+              const size_t ph = ((size_t)p.plan.row_info[r].x + gr.split) * p.H +
+                                (size_t)kvh * g + h;
+#pragma unroll
+              for (int mt = 0; mt < KS; ++mt)
+#pragma unroll
+                for (int hi = 0; hi < 2; ++hi) {
+                  const int d = mt * 16 + gid + hi * 8;
+                  p.plan.acc[ph * D + d] = ca.o[mt][nt][hi * 2 + e];
+                }
+              if (gid == 0) p.plan.ml[ph] = make_float2(ca.m[nt][e], ca.l[nt][e]);
+            }
+          }
       }
     }
     if (s_abort) break;
@@ -258,10 +370,10 @@ __global__ void __launch_bounds__(kRThreads, 1)
   }
 }
 
-template <int D, int NT, int RPW>
+template <int D>
 cudaError_t launch_r(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v, int grid,
                      cudaStream_t s) {
-  auto kern = rows_bf16_kernel<D, NT, RPW>;
+  auto kern = rows_bf16_kernel<D>;
   static unsigned long long done = 0;
   cudaError_t e = smem_opt_in(kern, RTile<D>::kSmemBytes, &done);
   if (e != cudaSuccess) return e;
@@ -273,9 +385,10 @@ cudaError_t launch_r(const StepParams& p, const CUtensorMap& k, const CUtensorMa
 
 int num_sms();
 
-// Rows per group for a GQA group of g heads: two rows per consumer warp when
-// the group fits one mma N tile (g <= 8), else one.
-int rows_group_size(int g) { return kRW * (g <= 8 ? 2 : 1); }
+// Rows per group for a GQA group of g heads: as many rows as fill the CTA's
+// kCols (row, head) columns; 0 (no grouping: the rows take the decode path)
+// when one row's heads do not fit.
+int rows_group_size(int g) { return g >= 1 && g <= kCols ? kCols / g : 0; }
 
 // max_items: an upper bound on (group, split, kv head) items of the step.
 cudaError_t launch_rows_bf16(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
@@ -284,9 +397,8 @@ cudaError_t launch_rows_bf16(const StepParams& p, const CUtensorMap& k, const CU
   int grid = (int)(max_items < cap ? max_items : cap);
   if (grid < 1) grid = 1;
   const int g = p.H / p.Hkv;
-  if (p.group_rows != rows_group_size(g)) return cudaErrorInvalidValue;
-  if (p.D == 128) return g <= 8 ? launch_r<128, 1, 2>(p, k, v, grid, s) : launch_r<128, 2, 1>(p, k, v, grid, s);
-  return g <= 8 ? launch_r<64, 1, 2>(p, k, v, grid, s) : launch_r<64, 2, 1>(p, k, v, grid, s);
+  if (p.group_rows != rows_group_size(g) || p.group_rows < 1) return cudaErrorInvalidValue;
+  return p.D == 128 ? launch_r<128>(p, k, v, grid, s) : launch_r<64>(p, k, v, grid, s);
 }
 
 }  // namespace pa

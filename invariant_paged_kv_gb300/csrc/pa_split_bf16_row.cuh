@@ -80,12 +80,15 @@ struct RowAcc {
       const uint32_t pb1 = pack_bf16x2(pc[0], pc[1]);  // key gid + 8, heads 2tig, 2tig+1
       l[nt][0] = fmaf(l[nt][0], alpha[0], bf16_lo(pb0) + bf16_lo(pb1));
       l[nt][1] = fmaf(l[nt][1], alpha[1], bf16_hi(pb0) + bf16_hi(pb1));
+      // o * 1 == o exactly: the rescale is skipped when no head's max moved
+      if (!__all_sync(0xffffffffu, alpha[0] == 1.f && alpha[1] == 1.f)) {
 #pragma unroll
-      for (int mt = 0; mt < KS; ++mt) {
-        o[mt][nt][0] *= alpha[0];
-        o[mt][nt][1] *= alpha[1];
-        o[mt][nt][2] *= alpha[0];
-        o[mt][nt][3] *= alpha[1];
+        for (int mt = 0; mt < KS; ++mt) {
+          o[mt][nt][0] *= alpha[0];
+          o[mt][nt][1] *= alpha[1];
+          o[mt][nt][2] *= alpha[0];
+          o[mt][nt][3] *= alpha[1];
+        }
       }
       pbt[nt][0] = movmatrix_trans(pb0);
       pbt[nt][1] = movmatrix_trans(pb1);
