@@ -41,6 +41,7 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILES = {
     False: (os.path.join(ROOT, "profiles", "decode_bf16_long_tail.md"),
             ["invariant_paged_kv_gb300/csrc/pa_decode_bf16.cu",
+             "invariant_paged_kv_gb300/csrc/pa_split_bf16_row.cuh",
              "invariant_paged_kv_gb300/csrc/pa_split_items.cuh",
              "invariant_paged_kv_gb300/csrc/pa_common.cuh"]),
     True: (os.path.join(ROOT, "profiles", "decode_fp8_long_tail.md"),

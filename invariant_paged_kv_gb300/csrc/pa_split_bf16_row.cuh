@@ -1,7 +1,7 @@
-// The per-row arithmetic of the bf16 split kernels, shared by the decode-row
-// kernel (one row per warp) and the prefill-row kernel of the row-invariant
-// mode (rows of one lane sharing key tiles): both call these functions, so a
-// row's bits are the same whichever of the two computes it.
+// The per-row arithmetic of the bf16 decode split kernel (one row per warp).
+// The prefill-row kernel of the row-invariant mode repeats it column by
+// column, operation for operation, so a row's bits are the same whichever of
+// the two computes it.
 //
 // A row's state for one (split, kv head): the g query heads of the group on
 // the N side of mma.sync (n tile nt holds heads 8 nt .. 8 nt + 7), this thread
