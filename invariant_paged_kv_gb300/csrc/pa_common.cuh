@@ -34,9 +34,11 @@ constexpr long long kWaitCycles = 2000000000LL;
 // Split plan, built on the device by the prologue kernel from cu_seqlens_q and
 // ctx_lens, stored in the workspace:
 //   header[0] = number of (row, split) pairs, header[1] = number of full pairs,
-//   header[2] = number of prefill q tiles
+//   header[2] = number of prefill q tiles, header[3] = number of prefill-row
+//   group records, header[4..5] = the split kernels' item counter (64-bit,
+//   zeroed with the plan)
 //   (full pairs of rows with longer splits come first, then full 512-key
-//   pairs, then tails: roughly largest first, for the snake-order schedule)
+//   pairs, then tails: roughly largest first, the order items are taken in)
 //   (pair k < header[1] sits at pairs[k]; tail pair k >= header[1] at
 //   pairs[capacity - 1 - (k - header[1])], see pair_slot)
 //   row_info[r] = {first full pair, tail pair or -1, number of splits, lane or -1}
@@ -60,6 +62,12 @@ struct SplitPlan {
   int ptile_capacity;  // prefill tiles the workspace holds
   long long entry_capacity;  // KV-parallel modes: entries the partial buffer holds
 };
+
+// The split kernels' item counter: each warp takes its next (pair, kv head)
+// item from it, in list order.
+__device__ __forceinline__ unsigned long long* item_counter(const SplitPlan& pl) {
+  return reinterpret_cast<unsigned long long*>(pl.header + 4);
+}
 
 // Slot of the k-th pair in work order: full pairs from the front of the
 // list, tail pairs from its back.

@@ -3,7 +3,10 @@
 // paged.py: fixed KV split per context length, no atomics).
 //
 // Work item = (row, split, kv head); splits follow split_len (512 keys for
-// rows up to 8192 keys, longer for longer rows). One warp owns an item: it streams the
+// rows up to 65,536 keys, longer for longer rows). Warps take items from a
+// counter in list order (largest first), so a warp that finishes early takes
+// more; the counter only decides who computes an item -- no partial result
+// is ever accumulated atomically. One warp owns an item: it streams the
 // split's keys in 16-key chunks through a private 3-stage ring of swizzled
 // shared-memory tiles filled by TMA (one 64-element box per half row), and
 // computes, for the g = H / Hkv query heads that read this kv head,
@@ -49,6 +52,7 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   constexpr int KS = D / 16;  // 16-wide steps along D
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kStages];
+  __shared__ long long s_items[kWarps][kItemSlots];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -66,15 +70,15 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   }
   __syncwarp();
 
-  const int g = p.H / p.Hkv;
   const long long n_items = (long long)p.plan.header[0] * p.Hkv;
   const int nfull = p.plan.header[1];
-  const long long gw = (long long)blockIdx.x * kWarps + warp;
-  const long long nw = (long long)gridDim.x * kWarps;
+  static_assert(kStages < kItemSlots, "item slots");
+  long long* const wq = s_items[warp];
 
   // ---- producer cursor: runs up to kStages chunks ahead of the consumer ----
   long long p_k = 0;
-  long long p_item = item_at(0, gw, nw);
+  long long p_item = take_item(p, lane);
+  if (lane == 0) wq[0] = p_item;
   int p_chunk = 0, p_w0 = 0;
   Item pi;
   int p_blk = 0;
@@ -111,7 +115,8 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     if (++p_chunk == pi.nchunks) {
       p_chunk = 0;
       p_w0 = 0;
-      p_item = item_at(++p_k, gw, nw);
+      p_item = take_item(p, lane);
+      if (lane == 0) wq[++p_k & (kItemSlots - 1)] = p_item;
       if (p_item < n_items) {
         pi = load_item(p, p_item, nfull);
         p_blk = load_blocks(p, pi, 0, lane);
@@ -122,11 +127,11 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
   for (int s = 0; s < kStages; ++s) produce();
 
   uint32_t consumed = 0;
-  const __nv_bfloat16* qbase = static_cast<const __nv_bfloat16*>(p.q);
 
 #pragma unroll 1
   for (long long c_k = 0;; ++c_k) {
-    const long long c_item = item_at(c_k, gw, nw);
+    __syncwarp();
+    const long long c_item = wq[c_k & (kItemSlots - 1)];
     if (c_item >= n_items) break;
     const Item it = load_item(p, c_item, nfull);
 

@@ -3,7 +3,8 @@
 // K/V dequantised on read; fp8 KV needs per-tensor scales).
 //
 // Same work decomposition and schedule as the bf16 split kernel -- item =
-// (row, split, kv head), one warp per item, chunks of keys through a private
+// (row, split, kv head) taken from the item counter in list order, one warp
+// per item, chunks of keys through a private
 // ring of TMA-filled shared-memory stages, online softmax in ascending key
 // order -- with three differences:
 //  * a chunk is 32 keys of 1-byte codes (the bytes of a 16-key bf16 chunk):
@@ -59,6 +60,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   constexpr int SEG = D / 64;  // 16-byte K runs a thread reads per key row
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kStages];
+  __shared__ long long s_items[kWarps][kItemSlots];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -79,12 +81,13 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   const int g = p.H / p.Hkv;
   const long long n_items = (long long)p.plan.header[0] * p.Hkv;
   const int nfull = p.plan.header[1];
-  const long long gw = (long long)blockIdx.x * kWarps + warp;
-  const long long nw = (long long)gridDim.x * kWarps;
+  static_assert(kStages < kItemSlots, "item slots");
+  long long* const wq = s_items[warp];
 
   // ---- producer cursor: runs up to kStages chunks ahead of the consumer ----
   long long p_k = 0;
-  long long p_item = item_at(0, gw, nw);
+  long long p_item = take_item(p, lane);
+  if (lane == 0) wq[0] = p_item;
   int p_chunk = 0, p_w0 = 0;
   Item pi;
   int p_blk = 0;
@@ -126,7 +129,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     if (++p_chunk == nchunks_of(pi)) {
       p_chunk = 0;
       p_w0 = 0;
-      p_item = item_at(++p_k, gw, nw);
+      p_item = take_item(p, lane);
+      if (lane == 0) wq[++p_k & (kItemSlots - 1)] = p_item;
       if (p_item < n_items) {
         pi = load_item(p, p_item, nfull);
         p_blk = load_blocks(p, pi, 0, lane);
@@ -141,7 +145,8 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 
 #pragma unroll 1
   for (long long c_k = 0;; ++c_k) {
-    const long long c_item = item_at(c_k, gw, nw);
+    __syncwarp();
+    const long long c_item = wq[c_k & (kItemSlots - 1)];
     if (c_item >= n_items) break;
     const Item it = load_item(p, c_item, nfull);
 

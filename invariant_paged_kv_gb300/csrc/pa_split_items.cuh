@@ -12,13 +12,21 @@ struct Item {
   int pair, kvh, row, lane, keys, t0, len, nchunks, single;
 };
 
-// k-th item of warp gw among nw warps: passes over the item list alternate
-// direction (snake order), so with items sorted by size every warp gets a
-// near-equal share of the work. Which warp runs an item never changes its
-// arithmetic.
-__device__ __forceinline__ long long item_at(long long k, long long gw, long long nw) {
-  return k * nw + ((k & 1) ? (nw - 1 - gw) : gw);
+// The next item for the calling warp: a warp that finishes early takes more
+// items, so all warps end within about one item of each other (items go out
+// in list order, largest first). The counter only hands out indices: an
+// item's arithmetic and where its result goes depend on the item alone,
+// never on which warp runs it or when.
+__device__ __forceinline__ long long take_item(const StepParams& p, int lane) {
+  unsigned long long v = 0;
+  if (lane == 0) v = atomicAdd(item_counter(p.plan), 1ull);
+  return (long long)__shfl_sync(0xffffffffu, v, 0);
 }
+
+// Items a warp's producer has taken and its consumer has not finished: the
+// producer runs at most kStages chunks ahead, so at most kStages items beyond
+// the consumer's current one; slot k & (kItemSlots - 1) holds the warp's k-th.
+constexpr int kItemSlots = 4;
 
 __device__ __forceinline__ Item load_item(const StepParams& p, long long item, int nfull) {
   Item it;
