@@ -35,8 +35,9 @@ constexpr long long kWaitCycles = 2000000000LL;
 // ctx_lens, stored in the workspace:
 //   header[0] = number of (row, split) pairs, header[1] = number of full pairs,
 //   header[2] = number of prefill q tiles, header[3] = number of prefill-row
-//   group records, header[4..5] = the split kernels' item counter (64-bit,
-//   zeroed with the plan)
+//   group records, header[4 + 2 c .. 5 + 2 c] = item counter c (64-bit,
+//   zeroed with the plan): c = 0 the split kernels, 1 the tensor-core
+//   prefill, 2 the prefill-row kernel
 //   (full pairs of rows with longer splits come first, then full 512-key
 //   pairs, then tails: roughly largest first, the order items are taken in)
 //   (pair k < header[1] sits at pairs[k]; tail pair k >= header[1] at
@@ -63,10 +64,11 @@ struct SplitPlan {
   long long entry_capacity;  // KV-parallel modes: entries the partial buffer holds
 };
 
-// The split kernels' item counter: each warp takes its next (pair, kv head)
-// item from it, in list order.
-__device__ __forceinline__ unsigned long long* item_counter(const SplitPlan& pl) {
-  return reinterpret_cast<unsigned long long*>(pl.header + 4);
+// Item counters: each worker (a warp of the split kernels, a CTA of the
+// prefill kernels) takes its next item from one, in list order.
+constexpr int kCounterSplit = 0, kCounterPrefill = 1, kCounterRows = 2, kItemCounters = 3;
+__device__ __forceinline__ unsigned long long* item_counter(const SplitPlan& pl, int c) {
+  return reinterpret_cast<unsigned long long*>(pl.header + 4 + 2 * c);
 }
 
 // Slot of the k-th pair in work order: full pairs from the front of the

@@ -128,6 +128,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
+  // items are taken from the prefill item counter in list order (heaviest
+  // tiles first): thread 0 takes item n + 1 during item n into slot
+  // (n + 1) & 1, and the end-of-item barrier publishes it
+  __shared__ long long s_item[2];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
@@ -156,6 +160,7 @@ __global__ void __launch_bounds__(kThreads, 1)
       mbar_init(smem_u32(&bars.o[h][1]), 1);
     }
     s_abort = 0;
+    s_item[0] = (long long)atomicAdd(item_counter(p.plan, kCounterPrefill), 1ull);
     fence_mbar_init();
   }
   if (warp == 9 && lane == 0) {
@@ -183,8 +188,12 @@ __global__ void __launch_bounds__(kThreads, 1)
   // key tiles done by each head slot
   uint32_t n_item = 0, n_kv = 0, n_t[2] = {0, 0};
 
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const ItemInfo it = item_info(p, item, g);
+  for (;;) {
+    const long long item = s_item[n_item & 1];
+    if (item >= n_items) break;
+    if (threadIdx.x == 0)
+      s_item[(n_item + 1) & 1] = (long long)atomicAdd(item_counter(p.plan, kCounterPrefill), 1ull);
+    const ItemInfo it = item_info(p, (int)item, g);
     const int nh = 1 + it.has_b;
 
     if (warp == 9) {

@@ -343,7 +343,7 @@ __device__ void build_plan(const StepParams& p) {
     pl.header[1] = overflow ? 0 : (int)nfull;
     pl.header[2] = n;
     pl.header[3] = overflow ? 0 : (int)total[4];
-    *item_counter(pl) = 0ull;
+    for (int c = 0; c < kItemCounters; ++c) *item_counter(pl, c) = 0ull;
   }
 }
 

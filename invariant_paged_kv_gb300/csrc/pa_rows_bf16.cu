@@ -167,6 +167,15 @@ __global__ void __launch_bounds__(kRThreads, 1)
   // waiter never meets the barrier more than one phase away
   __shared__ __align__(8) uint64_t full[kRStages], empty[kRStages], zeroed[kRStages];
   __shared__ volatile int s_abort;
+  // The producer takes items from the prefill-row item counter in list order
+  // and writes the CTA's k-th into s_q[k % kQueue] before it starts the
+  // item's first chunk; consumers read it once that chunk's full barrier has
+  // completed (release by the producer's arrive, acquire by the wait). An
+  // index past the end goes out the same way with a plain arrive and no
+  // copy: the consumers' stop token. The producer runs at most kRStages
+  // chunks -- so at most kRStages items -- ahead.
+  constexpr int kQueue = 2 * kRStages;
+  __shared__ long long s_q[kQueue];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int gid = lane >> 2, tig = lane & 3;
@@ -185,26 +194,41 @@ __global__ void __launch_bounds__(kRThreads, 1)
   }
   __syncthreads();
 
-  const int n_items = p.plan.header[3] * p.Hkv;
+  const long long n_items = (long long)p.plan.header[3] * p.Hkv;
   uint32_t f = 0;      // running chunk counter, identical in every role
   uint32_t zbits = 0;  // consumers: parity of zeroed[st] uses, bit st
 
-  for (int item = blockIdx.x; item < n_items; item += gridDim.x) {
-    const Group gr = group_at(p, item / p.Hkv);
-    const int kvh = item % p.Hkv;
-    const int sl = split_len(gr.keys0);
-    const int t0 = gr.split * sl;
-    const int len_max = min(sl, gr.keys0 + gr.nrows - 1 - t0);  // the last row's share
-    const int nch = (len_max + kChunk - 1) / kChunk;
-
-    if (warp == kRW) {
-      // ------------------------------ producer ------------------------------
-      if (lane == 0) {
+  if (warp == kRW) {
+    // -------------------------------- producer --------------------------------
+    if (lane == 0) {
+      bool ok = true;
+      for (long long k = 0; ok; ++k) {
+        const long long item = (long long)atomicAdd(item_counter(p.plan, kCounterRows), 1ull);
+        const bool stop = item >= n_items;
+        Group gr{};
+        int kvh = 0, t0 = 0, nch = 1;
+        if (!stop) {
+          gr = group_at(p, (int)(item / p.Hkv));
+          kvh = (int)(item % p.Hkv);
+          const int sl = split_len(gr.keys0);
+          t0 = gr.split * sl;
+          const int len_max = min(sl, gr.keys0 + gr.nrows - 1 - t0);  // the last row's share
+          nch = (len_max + kChunk - 1) / kChunk;
+        }
         for (int ch = 0; ch < nch; ++ch, ++f) {
           const uint32_t st = f % kRStages;
           if (f >= kRStages &&
-              !wait_r(smem_u32(&empty[st]), ((f / kRStages) - 1) & 1, &s_abort, p.status))
+              !wait_r(smem_u32(&empty[st]), ((f / kRStages) - 1) & 1, &s_abort, p.status)) {
+            ok = false;
             break;
+          }
+          if (ch == 0) s_q[k % kQueue] = item;
+          if (stop) {
+            mbar_arrive(smem_u32(&full[st]));
+            ++f;
+            ok = false;  // done
+            break;
+          }
           const int key = t0 + ch * kChunk;
           int blk = p.block_tables[(size_t)gr.lane * p.max_blocks + key / p.bs];
           if (blk < 0 || blk >= p.NB) {
@@ -221,10 +245,23 @@ __global__ void __launch_bounds__(kRThreads, 1)
           }
         }
       }
-      f = __shfl_sync(0xffffffffu, f, 0);
-    } else {
-      // ---------------------- consumer: 16 (row, head) columns ----------------
-      const int col0 = warp * (kNTW * 8);
+    }
+  } else {
+    // ---------------------- consumer: 16 (row, head) columns ----------------
+    const int col0 = warp * (kNTW * 8);
+    for (long long k = 0;; ++k) {
+      // the stage of the item's first chunk (or of the stop token)
+      if (!__all_sync(0xffffffffu, wait_r(smem_u32(&full[f % kRStages]), (f / kRStages) & 1,
+                                          &s_abort, p.status)))
+        break;
+      const long long item = s_q[k % kQueue];
+      if (item >= n_items) break;
+      const Group gr = group_at(p, (int)(item / p.Hkv));
+      const int kvh = (int)(item % p.Hkv);
+      const int sl = split_len(gr.keys0);
+      const int t0 = gr.split * sl;
+      const int len_max = min(sl, gr.keys0 + gr.nrows - 1 - t0);  // the last row's share
+      const int nch = (len_max + kChunk - 1) / kChunk;
       // keys of this split for the columns this thread holds in the softmax
       // layout (<= 0: the column's row lacks the split, or no such row)
       int len[kNTW][2];
@@ -244,8 +281,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
       bool ok = true;
       for (int ch = 0; ch < nch; ++ch, ++f) {
         const uint32_t st = f % kRStages;
-        if (!__all_sync(0xffffffffu, wait_r(smem_u32(&full[st]), (f / kRStages) & 1, &s_abort,
-                                            p.status))) {
+        if (ch > 0 && !__all_sync(0xffffffffu, wait_r(smem_u32(&full[st]), (f / kRStages) & 1,
+                                                      &s_abort, p.status))) {
           ok = false;
           break;
         }
@@ -357,8 +394,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
             }
           }
       }
+      if (!ok) break;
     }
-    if (s_abort) break;
   }
   // copies this CTA started land before it leaves
   if (warp == kRW && lane == 0) {

@@ -19,7 +19,7 @@ struct Item {
 // never on which warp runs it or when.
 __device__ __forceinline__ long long take_item(const StepParams& p, int lane) {
   unsigned long long v = 0;
-  if (lane == 0) v = atomicAdd(item_counter(p.plan), 1ull);
+  if (lane == 0) v = atomicAdd(item_counter(p.plan, kCounterSplit), 1ull);
   return (long long)__shfl_sync(0xffffffffu, v, 0);
 }
 
