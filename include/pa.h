@@ -195,7 +195,11 @@ size_t pa_attention_workspace_bytes_ex(int32_t B, int32_t T, int32_t max_q_len,
  *   scale            softmax scale applied to q.k (fp32, finite and > 0)
  *   workspace        device scratch of workspace_bytes >= the value
  *                    pa_attention_workspace_bytes returns for this step,
- *                    256-byte aligned; contents on entry are irrelevant
+ *                    256-byte aligned; contents on entry are irrelevant.
+ *                    The call's kernels own it until its work on `stream`
+ *                    completes (the split plan, the kernels' item counters
+ *                    and the split partials live there): calls whose work
+ *                    may overlap on the GPU need separate workspaces
  * Lanes with q_len == 1 take the split-KV decode path: a row with K keys is
  * split into ranges [S i, S (i + 1)) with S = 512 * 2^j for the smallest j
  * that gives at most 128 ranges (512-key ranges up to K = 65536), each range
