@@ -12,7 +12,10 @@ and each layer's keys (~5.5 GB) are far larger than L2, so no flush is
 needed between steps.
 
 The K timed steps are replayed from one CUDA graph (captured untimed, with
-the same calls and phase events); --no-graph launches them eagerly.
+the same calls); --no-graph launches them eagerly. Phase events (the kernels'
+own times, from which the roofline comes) are recorded on every tenth timed
+step and the last one. The end-to-end leg copies every step's inputs in and
+outputs out, on copy streams that overlap other layers' attention.
 
 Prints ONE JSON line (rank 0). Under torchrun each rank runs its own
 independent step (seed offset by rank; no collective on the data path):
@@ -385,8 +388,13 @@ def run_ours(args, rank, world, local_rank):
     # a serving step is fixed, so engines replay it) and the graph is replayed
     # once in the timed region; --no-graph launches them eagerly instead.
     K = args.steps
-    ev = [[[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(layers)]
-          for _ in range(K)]
+    # Phase events (the kernels' own times) on every tenth step of the timed
+    # region, and on its last step: each recorded event costs the stream a
+    # few microseconds, so recording them on every step would understate the
+    # step throughput by ~2%.
+    timed_steps = [k for k in range(K) if k % 10 == 9 or k == K - 1]
+    ev = {k: [[torch.cuda.Event(enable_timing=True) for _ in range(5)] for _ in range(layers)]
+          for k in timed_steps}
     t_start, t_end = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     clocks = ClockSampler(local_rank) if not args.no_clocks else None
     graph = None
@@ -395,7 +403,7 @@ def run_ours(args, rank, world, local_rank):
         launches0 = pa.kernel_launches()
         with torch.cuda.graph(graph):
             for k in range(K):
-                one_step(events=ev[k])
+                one_step(events=ev.get(k))
         launches = pa.kernel_launches() - launches0
         graph.replay()  # untimed
         torch.cuda.synchronize()
@@ -408,7 +416,7 @@ def run_ours(args, rank, world, local_rank):
     t_start.record(stream)
     if graph is None:
         for k in range(K):
-            one_step(events=ev[k])
+            one_step(events=ev.get(k))
     else:
         graph.replay()
     t_end.record(stream)
@@ -420,13 +428,13 @@ def run_ours(args, rank, world, local_rank):
     flags = pa.read_status(status)
     if flags:
         raise RuntimeError(f"device status flags {flags:#x}")
-    decode_ms = [e[1].elapsed_time(e[2]) for st in ev for e in st]
-    prefill_ms = [e[2].elapsed_time(e[3]) for st in ev for e in st]
+    decode_ms = [e[1].elapsed_time(e[2]) for st in ev.values() for e in st]
+    prefill_ms = [e[2].elapsed_time(e[3]) for st in ev.values() for e in st]
     phase_ms = {
-        "prologue": statistics.mean(e[0].elapsed_time(e[1]) for st in ev for e in st),
+        "prologue": statistics.mean(e[0].elapsed_time(e[1]) for st in ev.values() for e in st),
         "decode": statistics.mean(decode_ms),
         "prefill": statistics.mean(prefill_ms),
-        "combine": statistics.mean(e[3].elapsed_time(e[4]) for st in ev for e in st),
+        "combine": statistics.mean(e[3].elapsed_time(e[4]) for st in ev.values() for e in st),
     }
     ms_max = max_over_ranks(ms, world, dev)
 
@@ -436,57 +444,100 @@ def run_ours(args, rank, world, local_rank):
     rows_per_s = step.T * world / (ms_max * 1e-3)
 
     # ---- end to end: per-step inputs from pinned host memory, result back ----
+    # Every step copies all of its inputs (q, new K/V rows of every layer and
+    # the step descriptors) from pinned host memory and every layer's output
+    # back, inside the timed region. The copies run on two copy streams, one
+    # per direction, and overlap the attention of other layers: device-side
+    # inputs and outputs are double-buffered by step parity, and events order
+    # each copy after the compute that frees its buffer (step k + 1's inputs
+    # arrive while step k computes; layer l's output leaves while layer l + 1
+    # computes), as a serving engine pipelines them.
     e2e = None
     if not args.no_e2e:
         pin = lambda x: x.cpu().pin_memory()
         h_q = [pin(x) for x in tens["q"]]
         h_kn = [pin(x) for x in tens["k_new"]]
         h_vn = [pin(x) for x in tens["v_new"]]
-        h_bt, h_cu = pin(bt), pin(cu)
-        h_ctx, h_sl = pin(ctx), pin(slots)
+        h_desc = [pin(bt), pin(cu), pin(ctx), pin(slots)]
         h_out = [torch.empty(o.shape, dtype=o.dtype, pin_memory=True) for o in outs]
-        d_q = [torch.empty_like(x) for x in tens["q"]]
-        d_kn = [torch.empty_like(x) for x in tens["k_new"]]
-        d_vn = [torch.empty_like(x) for x in tens["v_new"]]
-        d_bt, d_cu, d_ctx, d_sl = (torch.empty_like(bt), torch.empty_like(cu),
-                                   torch.empty_like(ctx), torch.empty_like(slots))
-        h2d = sum(x.numel() * x.element_size() for x in h_q + h_kn + h_vn + [h_bt, h_cu, h_ctx, h_sl])
+        d_in = [{"q": [torch.empty_like(x) for x in tens["q"]],
+                 "kn": [torch.empty_like(x) for x in tens["k_new"]],
+                 "vn": [torch.empty_like(x) for x in tens["v_new"]],
+                 "desc": [torch.empty_like(x) for x in (bt, cu, ctx, slots)]} for _ in range(2)]
+        d_out = [[torch.empty_like(o) for o in outs] for _ in range(2)]
+        h2d = sum(x.numel() * x.element_size() for x in h_q + h_kn + h_vn + h_desc)
         d2h = sum(x.numel() * x.element_size() for x in h_out)
+        hs, ds = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+        ev_desc = [torch.cuda.Event() for _ in range(2)]
+        ev_in = [[torch.cuda.Event() for _ in range(layers)] for _ in range(2)]
+        ev_comp = [[torch.cuda.Event() for _ in range(layers)] for _ in range(2)]
+        ev_out = [[torch.cuda.Event() for _ in range(layers)] for _ in range(2)]
 
-        def e2e_step():
-            for src, dst in zip(h_q + h_kn + h_vn + [h_bt, h_cu, h_ctx, h_sl],
-                                d_q + d_kn + d_vn + [d_bt, d_cu, d_ctx, d_sl]):
-                dst.copy_(src, non_blocking=True)
-            one_step(q=d_q, kn=d_kn, vn=d_vn, dbt=d_bt, dcu=d_cu, dctx=d_ctx, dslots=d_sl)
-            for src, dst in zip(outs, h_out):
-                dst.copy_(src, non_blocking=True)
+        def e2e_steps(n):
+            hs.wait_stream(stream)
+            ds.wait_stream(stream)
+            for k in range(n):
+                b = k & 1
+                B, O = d_in[b], d_out[b]
+                with torch.cuda.stream(hs):
+                    if k >= 2:  # buffer set b was last read by step k - 2
+                        hs.wait_event(ev_comp[b][layers - 1])
+                    for src, dst in zip(h_desc, B["desc"]):
+                        dst.copy_(src, non_blocking=True)
+                    ev_desc[b].record(hs)
+                    for l in range(layers):
+                        for src, dst in ((h_q[l], B["q"][l]), (h_kn[l], B["kn"][l]),
+                                         (h_vn[l], B["vn"][l])):
+                            dst.copy_(src, non_blocking=True)
+                        ev_in[b][l].record(hs)
+                dbt, dcu, dctx, dsl = B["desc"]
+                for l in range(layers):
+                    stream.wait_event(ev_desc[b])
+                    stream.wait_event(ev_in[b][l])
+                    if k >= 2:  # step k - 2's output of this layer has left
+                        stream.wait_event(ev_out[b][l])
+                    pa.attention(B["q"][l], tens["k_cache"][l], tens["v_cache"][l], dbt, dcu, dctx,
+                                 O[l], max_q_len=step.max_q_len, max_ctx_len=step.max_ctx_len,
+                                 scale=scale, workspace=ws, slot_mapping=dsl,
+                                 k_new=B["kn"][l], v_new=B["vn"][l], status=status,
+                                 mode=args.mode, k_scale=wl.FP8_K_SCALE, v_scale=wl.FP8_V_SCALE)
+                    ev_comp[b][l].record(stream)
+                    with torch.cuda.stream(ds):
+                        ds.wait_event(ev_comp[b][l])
+                        h_out[l].copy_(O[l], non_blocking=True)
+                        ev_out[b][l].record(ds)
+            stream.wait_stream(hs)
+            stream.wait_stream(ds)
 
-        for _ in range(2):
-            e2e_step()
+        e2e_steps(2)
         e2e_graph = None
         if not args.no_graph:
             e2e_graph = torch.cuda.CUDAGraph()
             with torch.cuda.graph(e2e_graph):
-                for _ in range(K):
-                    e2e_step()
+                e2e_steps(K)
             e2e_graph.replay()
         barrier()
         a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
         a.record(stream)
         if e2e_graph is None:
-            for _ in range(K):
-                e2e_step()
+            e2e_steps(K)
         else:
             e2e_graph.replay()
         b.record(stream)
         barrier()
         e2e_ms = max_over_ranks(a.elapsed_time(b) / K, world, dev)
+        # the pipelined copies must not change a bit: same inputs, same outputs
+        for l in range(layers):
+            if not torch.equal(h_out[l], outs[l].cpu()):
+                raise RuntimeError(f"end-to-end output of layer {l} differs from the "
+                                   "device-resident run")
         e2e = {"value": round(weak_scaling_value(step_bytes, world, e2e_ms), 1), "unit": "GB/s",
                "ms_per_step": round(e2e_ms, 4), "h2d_bytes_per_step": int(h2d),
                "d2h_bytes_per_step": int(d2h),
-               "what": "pinned host -> device copies of q, new K/V rows and step descriptors "
-                       "of every layer, the layers' pa_attention calls, device -> host copy "
-                       "of every layer's output"}
+               "what": "every step: pinned host -> device copies of q, new K/V rows and step "
+                       "descriptors of every layer, the layers' pa_attention calls, device -> "
+                       "host copy of every layer's output; copies on two copy streams "
+                       "overlapping other layers' attention (double-buffered device buffers)"}
 
     peak, peak_kind = measured_hbm_peak()
     dec_ms = statistics.mean(decode_ms)
