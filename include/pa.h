@@ -19,13 +19,15 @@
  *     no per-call state. All work is enqueued on `stream` (a cudaStream_t;
  *     NULL = the legacy default stream). Results are valid once the stream
  *     reaches that point. Only pa_read_status synchronises.
- *   - Element type `dtype` applies to q, caches, new rows and out alike.
+ *   - Element type `dtype` applies to q, caches, new rows and out alike,
+ *     except PA_FP8_E4M3: caches hold e4m3 codes (1 byte) under per-tensor
+ *     scales while q, new rows and out are bf16.
  *   - ctx_lens[b] counts every key lane b attends AFTER this step's write, its
  *     own new rows included; row j (0-based) of a lane with q_len rows sits at
  *     absolute position ctx_lens[b] - q_len + j and attends keys 0..position.
  *   - Query head h reads kv head h / (H / Hkv) (blocked GQA map).
  *   - Supported: D in {64, 128}; block_size in {16, 32}; H % Hkv == 0 and
- *     1 <= H / Hkv <= 16; dtype PA_F32 or PA_BF16.
+ *     1 <= H / Hkv <= 16; dtype PA_F32, PA_BF16 or PA_FP8_E4M3.
  *
  * Errors
  *   - Problems visible on the host (NULL pointers, unsupported geometry,
