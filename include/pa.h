@@ -178,7 +178,9 @@ size_t pa_attention_workspace_bytes_ex(int32_t B, int32_t T, int32_t max_q_len,
  *  PagedAttention protocol -- write new K/V, return [T, H, D] -- and the
  *  paged-attention kernel contract: q, k/v cache blocks, block tables,
  *  cu_seqlens_q, ctx_lens, slot mapping; fixed KV split per context length,
- *  no atomics.)
+ *  no atomics. Read here as: no result accumulated atomically. The kernels
+ *  take their work items from atomic counters in the workspace, which
+ *  decides only which warp or CTA computes an item, never its arithmetic.)
  *
  *   q                [T, H, D]
  *   k_cache, v_cache [num_blocks, block_size, Hkv, D]
