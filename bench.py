@@ -44,6 +44,7 @@ FALLBACK_HBM_GBS = 6800.0
 PROFILES = {
     False: (os.path.join(ROOT, "profiles", "decode_bf16_long_tail.md"),
             ["invariant_paged_kv_gb300/csrc/pa_decode_bf16.cu",
+             "invariant_paged_kv_gb300/csrc/pa_decode_bf16.cuh",
              "invariant_paged_kv_gb300/csrc/pa_split_bf16_row.cuh",
              "invariant_paged_kv_gb300/csrc/pa_split_items.cuh",
              "invariant_paged_kv_gb300/csrc/pa_common.cuh"]),
@@ -547,8 +548,16 @@ def run_ours(args, rank, world, local_rank):
     achieved = nbytes["decode_kernel"] / (dec_ms * 1e-3) / 1e9
     fp8 = g.dtype == "fp8"
     traffic, sha = committed_traffic(fp8)
+    # bf16 steps with prefill chunks in the batch-invariant mode run the decode
+    # and the tensor-core prefill in one launch on disjoint SMs: both rooflines
+    # are then taken over that launch's time
+    mixed = bool(wl.prefill_flops(step)) and args.mode == "batch" and g.dtype == "bf16"
+    if mixed:
+        traffic = None  # the committed decode capture is of the decode-only kernel
     roofline = {"bound": "hbm",
-                "kernel": ("decode_fp8_kernel (split-KV decode partials, e4m3 codes)" if fp8
+                "kernel": ("mixed_kernel (split-KV decode and tcgen05 prefill on disjoint SMs, "
+                           "one launch)" if mixed else
+                           "decode_fp8_kernel (split-KV decode partials, e4m3 codes)" if fp8
                            else "decode_bf16_kernel (split-KV decode partials)"),
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
                 "peak_kind": peak_kind, "frac": round(achieved / peak, 4),
@@ -557,11 +566,13 @@ def run_ours(args, rank, world, local_rank):
 
     prefill = None
     pf = wl.prefill_flops(step)
-    if pf and args.mode == "batch" and g.dtype == "bf16":  # the tensor-core prefill ran
-        pf_ms = statistics.mean(prefill_ms)
+    if mixed:  # the tensor-core prefill ran, in the same launch as the decode
+        pf_ms = dec_ms
         tpeak, tkind = measured_bf16_peak(sustained=True)
         ach = pf / (pf_ms * 1e-3) / 1e12
-        prefill = {"bound": "tensor", "kernel": "prefill_tc_kernel (tcgen05, bf16 -> fp32)",
+        prefill = {"bound": "tensor",
+                   "kernel": "mixed_kernel, prefill role (tcgen05, bf16 -> fp32; shares the "
+                             "launch and its SMs with the decode role)",
                    "achieved": round(ach, 1), "peak": tpeak, "unit": "TFLOP/s",
                    "peak_kind": tkind, "frac": round(ach / tpeak, 4),
                    "flops_per_launch": pf, "avg_launch_ms": round(pf_ms, 4)}

@@ -21,8 +21,8 @@ cudaError_t launch_rows_bf16(const StepParams& p, const CUtensorMap& k, const CU
                              long long max_items, cudaStream_t s);
 int rows_group_size(int g);
 cudaError_t launch_combine(const StepParams& p, cudaStream_t s);
-cudaError_t launch_prefill_tc(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
-                              const CUtensorMap& v, long long max_items, cudaStream_t s);
+cudaError_t launch_mixed(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                         const CUtensorMap& v, cudaStream_t s);
 
 void decode_gemm_plan(int N, int K, int* S, int* chunks_per_split);
 cudaError_t launch_decode_gemm(void* y, float* part, int T_pad, int N, int K, int S, int cps,
@@ -454,6 +454,7 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
   p.out_scale = p.v_scale;
   if (fp8) p.scale_log2 *= k_scale;
   p.plan = carve(workspace, cap, B, T, H, D);
+  p.sm_count = num_sms();
   const bool prefill_tc = !p.split_all_rows && max_q_len >= 2;
   // row-invariant bf16 steps: prefill rows in groups sharing key tiles
   p.group_rows = (dtype == PA_BF16 && mode == PA_MODE_ROW_INVARIANT && max_q_len >= 2)
@@ -479,17 +480,16 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
   if (launch_prologue(p, true, with_write, s) != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
   if (record(events, n_events, 1, s) != PA_OK) return PA_ERR_CUDA;
-  cudaError_t e = fp8 ? launch_decode_fp8(p, tmK, tmV, items, s)
-                      : dtype == PA_BF16 ? launch_decode_bf16(p, tmK, tmV, items, s)
-                                         : launch_split_f32(p, items, s);
+  // steps with prefill chunks on the tensor cores run decode and prefill in
+  // one launch on disjoint SMs (the phase events then see it all as the
+  // split phase)
+  cudaError_t e = prefill_tc ? launch_mixed(p, tmQ, tmK, tmV, s)
+                  : fp8      ? launch_decode_fp8(p, tmK, tmV, items, s)
+                  : dtype == PA_BF16 ? launch_decode_bf16(p, tmK, tmV, items, s)
+                                     : launch_split_f32(p, items, s);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
   if (record(events, n_events, 2, s) != PA_OK) return PA_ERR_CUDA;
-  if (prefill_tc) {
-    const long long pitems = max_prefill_tiles(B, T) * Hkv * ((H / Hkv + 1) / 2);
-    if (launch_prefill_tc(p, tmQ, tmK, tmV, pitems, s) != cudaSuccess) return PA_ERR_CUDA;
-    count_launches(1);
-  }
   if (p.group_rows) {
     // group records never outnumber the grouped rows' (row, split) entries
     if (launch_rows_bf16(p, tmK, tmV, items, s) != cudaSuccess) return PA_ERR_CUDA;

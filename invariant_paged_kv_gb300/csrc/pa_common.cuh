@@ -37,7 +37,8 @@ constexpr long long kWaitCycles = 2000000000LL;
 //   header[2] = number of prefill q tiles, header[3] = number of prefill-row
 //   group records, header[4 + 2 c .. 5 + 2 c] = item counter c (64-bit,
 //   zeroed with the plan): c = 0 the split kernels, 1 the tensor-core
-//   prefill, 2 the prefill-row kernel
+//   prefill, 2 the prefill-row kernel; header[kHeaderSplitKeys],
+//   header[kHeaderPrefillWork] (64-bit) = the step's work totals
 //   (full pairs of rows with longer splits come first, then full 512-key
 //   pairs, then tails: roughly largest first, the order items are taken in)
 //   (pair k < header[1] sits at pairs[k]; tail pair k >= header[1] at
@@ -67,6 +68,16 @@ struct SplitPlan {
 // Item counters: each worker (a warp of the split kernels, a CTA of the
 // prefill kernels) takes its next item from one, in list order.
 constexpr int kCounterSplit = 0, kCounterPrefill = 1, kCounterRows = 2, kItemCounters = 3;
+// 64-bit work totals of the step, for the mixed-step kernel's role split:
+// keys of the rows on the split path, and the (row, key) pairs the prefill
+// tiles' rows attend
+constexpr int kHeaderSplitKeys = 4 + 2 * kItemCounters;
+constexpr int kHeaderPrefillWork = kHeaderSplitKeys + 2;
+// prefill-role CTAs of the mixed-step kernel, chosen by the plan builder
+constexpr int kHeaderPrefillCtas = kHeaderPrefillWork + 2;
+__device__ __forceinline__ long long* header_total(const SplitPlan& pl, int at) {
+  return reinterpret_cast<long long*>(pl.header + at);
+}
 __device__ __forceinline__ unsigned long long* item_counter(const SplitPlan& pl, int c) {
   return reinterpret_cast<unsigned long long*>(pl.header + 4 + 2 * c);
 }
@@ -117,6 +128,7 @@ struct StepParams {
   // pairs: pairs[header[1] + k], header[3] of them); decode lanes as usual.
   // 0: no grouping.
   int group_rows;
+  int sm_count;  // SMs of the device (the mixed-step kernel's grid)
   int partials_mode;
   const int* key_lo;
   const int* key_hi;

@@ -1,0 +1,62 @@
+// Steps that mix decode rows and prefill chunks (bf16 caches, the
+// batch-invariant mode): the split-KV decode work is bound by HBM bandwidth
+// and the tensor-core prefill by the tensor pipe, and on their own they run
+// one after the other. Here one launch runs both on disjoint SMs: every CTA
+// (one per SM: the prefill's shared memory admits one) takes one role -- the
+// prefill CTA of pa_prefill_tc.cuh, or 8 independent decode warps of
+// pa_decode_bf16.cuh -- so the two kinds of work overlap. Each role takes its
+// items from its own counter, and an item's arithmetic is the same whichever
+// CTA computes it, so every output bit is the one the two kernels give on
+// their own.
+//
+// The number of prefill CTAs, which balances the two roles' times, comes
+// from the plan builder (prefill_role_ctas); it decides only where work runs,
+// never its result.
+#include "pa_decode_bf16.cuh"
+#include "pa_prefill_tc.cuh"
+
+namespace pa {
+
+namespace {
+
+constexpr int kDecWarps = 8;  // decode warps of a decode-role CTA
+
+template <int D, int NT>
+__global__ void __launch_bounds__(pftc::kThreads, 1)
+    mixed_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmQ,
+                 const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
+  extern __shared__ uint8_t dsmem[];
+  if ((int)blockIdx.x < p.plan.header[kHeaderPrefillCtas]) {
+    pftc::prefill_tc_cta<D>(p, &tmQ, &tmK, &tmV, dsmem);
+  } else if (threadIdx.x < kDecWarps * 32) {
+    decode_bf16_warps<D, NT, false, kDecWarps>(p, &tmK, &tmV, dsmem);
+  }
+}
+
+template <int D, int NT>
+cudaError_t launch_m(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                     const CUtensorMap& v, int grid, cudaStream_t s) {
+  constexpr int a = pftc::PfLayout<D>::kSmemBytes, b = DecTile<D>::smem_bytes(kDecWarps);
+  constexpr int smem = a > b ? a : b;
+  auto kern = mixed_kernel<D, NT>;
+  static unsigned long long done = 0;
+  cudaError_t e = smem_opt_in(kern, smem, &done);
+  if (e != cudaSuccess) return e;
+  kern<<<grid, pftc::kThreads, smem, s>>>(p, q, k, v);
+  return cudaGetLastError();
+}
+
+}  // namespace
+
+int num_sms();
+
+// One CTA per SM.
+cudaError_t launch_mixed(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
+                         const CUtensorMap& v, cudaStream_t s) {
+  const int grid = p.sm_count;
+  const int g = p.H / p.Hkv;
+  if (p.D == 128) return g <= 8 ? launch_m<128, 1>(p, q, k, v, grid, s) : launch_m<128, 2>(p, q, k, v, grid, s);
+  return g <= 8 ? launch_m<64, 1>(p, q, k, v, grid, s) : launch_m<64, 2>(p, q, k, v, grid, s);
+}
+
+}  // namespace pa

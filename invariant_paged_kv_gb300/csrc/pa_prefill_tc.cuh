@@ -30,11 +30,17 @@
 // other. Every wait is bounded (timeout -> PA_FLAG_TIMEOUT). No parity wait
 // ever meets a barrier more than one phase away from the awaited one, ahead
 // or behind (the P V barriers alternate by tile parity for that reason).
+//
+// The work is written as the code of one CTA (prefill_tc_cta): it runs as the
+// prefill role of the mixed-step kernel (pa_mixed.cu), which gives every CTA
+// this role when a step has no decode rows.
+#pragma once
+
 #include "pa_tcgen05.cuh"
 
 namespace pa {
+namespace pftc {
 
-namespace {
 
 constexpr int kRows = 128;  // query rows per item (M)
 constexpr int kKeys = 128;  // keys per tile (N of S, K of PV)
@@ -116,15 +122,13 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
   return __all_sync(0xffffffffu, wait_or_abort_1(bar, parity, abort_flag, status));
 }
 
-// 320 threads put three warps on two of the four SM sub-partitions, whose
-// register files hold 16384 each: 168 registers per thread is the ceiling.
+// The work of one CTA of kThreads threads (see the roles above); dsmem
+// holds PfLayout<D>::kSmemBytes bytes.
 template <int D>
-__global__ void __launch_bounds__(kThreads, 1)
-    prefill_tc_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmQ,
-                      const __grid_constant__ CUtensorMap tmK,
-                      const __grid_constant__ CUtensorMap tmV) {
+__device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtensorMap* tmQ,
+                                               const CUtensorMap* tmK, const CUtensorMap* tmV,
+                                               uint8_t* dsmem) {
   using L = PfLayout<D>;
-  extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) Bars bars;
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
@@ -164,9 +168,9 @@ __global__ void __launch_bounds__(kThreads, 1)
     fence_mbar_init();
   }
   if (warp == 9 && lane == 0) {
-    prefetch_tensormap(&tmQ);
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
+    prefetch_tensormap(tmQ);
+    prefetch_tensormap(tmK);
+    prefetch_tensormap(tmV);
   }
   if (warp == 8) tmem_alloc(smem_u32(&s_tmem), kTmemCols);
   tc_fence_before();
@@ -205,7 +209,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         for (int hb = 0; hb < nh; ++hb)
 #pragma unroll
           for (int h = 0; h < L::kHalves; ++h)
-            tma_load_3d(sQ + hb * L::kQBytes + h * L::kHalfBytes, &tmQ, h * 64, it.head0 + hb,
+            tma_load_3d(sQ + hb * L::kQBytes + h * L::kHalfBytes, tmQ, h * 64, it.head0 + hb,
                         it.cu0 + it.tile * kRows, bq);
       }
       for (int kt = 0; kt < it.nkt; ++kt) {
@@ -229,7 +233,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < nchunk) {
 #pragma unroll
           for (int h = 0; h < L::kHalves; ++h)
-            tma_load_3d(sK0 + st * L::kKBytes + h * L::kKHalfBytes + lane * kChunk * 128, &tmK,
+            tma_load_3d(sK0 + st * L::kKBytes + h * L::kKHalfBytes + lane * kChunk * 128, tmK,
                         h * 64, it.kvh, tok, bkf[st]);
         }
         if (use >= 1 && !wait_or_abort(bve[st], (use - 1) & 1, &s_abort, p.status)) break;
@@ -238,7 +242,7 @@ __global__ void __launch_bounds__(kThreads, 1)
         if (lane < nchunk) {
 #pragma unroll
           for (int h = 0; h < L::kHalves; ++h)
-            tma_load_3d(sV0 + st * L::kVBytes + h * L::kKHalfBytes + lane * kChunk * 128, &tmV,
+            tma_load_3d(sV0 + st * L::kVBytes + h * L::kKHalfBytes + lane * kChunk * 128, tmV,
                         h * 64, it.kvh, tok, bvf[st]);
         }
       }
@@ -480,28 +484,5 @@ __global__ void __launch_bounds__(kThreads, 1)
   }
 }
 
-template <int D>
-cudaError_t launch_d(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
-                     const CUtensorMap& v, int grid, cudaStream_t s) {
-  auto kern = prefill_tc_kernel<D>;
-  static unsigned long long done = 0;
-  cudaError_t e = smem_opt_in(kern, PfLayout<D>::kSmemBytes, &done);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kThreads, PfLayout<D>::kSmemBytes, s>>>(p, q, k, v);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
-int num_sms();
-
-// max_items: an upper bound on (q tile, kv head, head pair) items of the step.
-cudaError_t launch_prefill_tc(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
-                              const CUtensorMap& v, long long max_items, cudaStream_t s) {
-  long long cap = num_sms();
-  int grid = (int)(max_items < cap ? max_items : cap);
-  if (grid < 1) grid = 1;
-  return p.D == 128 ? launch_d<128>(p, q, k, v, grid, s) : launch_d<64>(p, q, k, v, grid, s);
-}
-
+}  // namespace pftc
 }  // namespace pa

@@ -223,6 +223,43 @@ __device__ bool row_counts(const StepParams& p, const LaneCache* lc, int u, int&
   return true;
 }
 
+// Prefill-role CTAs of the mixed-step kernel out of nctas (one per SM): the
+// split that balances the two roles' times, from the step's work totals and
+// per-SM rates measured on this part with the two roles running side by side
+// -- the decode role streams ~66 GB/s per SM up to ~6760 GB/s in all, the
+// prefill role runs ~4.0 TFLOP/s per SM. fp32 (the part's fp64 rate is low);
+// it decides only where work runs, never its result.
+__device__ int prefill_role_ctas(const StepParams& p, long long split_keys, long long pf_work,
+                                 int pf_tiles, int nctas) {
+  const int g = p.H / p.Hkv;
+  const long long pf_items = (long long)pf_tiles * p.Hkv * ((g + 1) / 2);
+  if (pf_work <= 0 || pf_items <= 0 || nctas <= 1) return 0;
+  if (split_keys <= 0) return nctas;
+  const float kDecPerSm = 66e9f, kDecMax = 6760e9f, kPfPerSm = 4.0e12f;
+  const float a = 4.f * p.D * p.H * (float)pf_work / kPfPerSm;               // prefill SM-seconds
+  const float b = (float)split_keys * p.Hkv * p.D * 2.f * p.elem_bytes;      // decode bytes
+  auto t = [&](int m) {  // the later of the two roles with m prefill CTAs
+    return fmaxf(b / fminf(kDecMax, kDecPerSm * (nctas - m)), a / m);
+  };
+  // the two times cross where a / m = b / (kDecPerSm (nctas - m)) while the
+  // decode role is below its cap, or where a / m = b / kDecMax once it is
+  // not; the nearest integers around both crossings are the candidates
+  const float m1 = nctas * a / (a + b / kDecPerSm), m2 = a * kDecMax / b;
+  int best = 1;
+  float best_t = t(1);
+  const float cand[2] = {m1, m2};
+  for (int c = 0; c < 2; ++c)
+    for (int d = -1; d <= 1; ++d) {
+      const int m = min(nctas - 1, max(1, (int)cand[c] + d));
+      const float tm = t(m);
+      if (tm < best_t) {
+        best_t = tm;
+        best = m;
+      }
+    }
+  return (int)(best < pf_items ? best : pf_items);
+}
+
 // The plan is built over units (blockDim at a time, two passes): pass 1
 // counts and scans, pass 2 scans again and writes -- long full pairs from the
 // front of the list, short full pairs after all long ones, tail pairs from the
@@ -254,11 +291,30 @@ __device__ void build_plan(const StepParams& p) {
 
   const int units = p.split_all_rows ? p.T : p.B;
   long long total[kCounters] = {0, 0, 0, 0, 0};
+  // work totals for the mixed-step kernel's role split (steps with prefill
+  // tiles only): keys of the split-path rows, (row, key) pairs of the prefill
+  // rows -- rows j = 0 .. q-1 of a lane attend c - q + j + 1 keys
+  __shared__ long long s_mix[2];
+  const bool mixed = !p.split_all_rows && p.max_q_len >= 2;
+  if (tid < 2) s_mix[tid] = 0;
+  __syncthreads();
   for (int base = 0; base < units; base += nth) {
     long long cnt[kCounters];
     RowPlan rp;
     int r;
-    row_counts(p, lc, base + tid, r, cnt, rp);
+    const bool ok0 = row_counts(p, lc, base + tid, r, cnt, rp);
+    if (mixed) {
+      long long w[2] = {ok0 && rp.split ? (long long)rp.keys : 0, 0};
+      if (ok0 && rp.tiles && rp.j == 0)
+        w[1] = (long long)rp.q * (rp.c - rp.q) + (long long)rp.q * (rp.q + 1) / 2;
+#pragma unroll
+      for (int k = 0; k < 2; ++k) {
+#pragma unroll
+        for (int o = 16; o >= 1; o >>= 1) w[k] += __shfl_xor_sync(0xffffffffu, w[k], o);
+        if ((tid & 31) == 0 && w[k]) atomicAdd(reinterpret_cast<unsigned long long*>(&s_mix[k]),
+                                               (unsigned long long)w[k]);
+      }
+    }
     long long ex[kCounters], tot[kCounters];
     block_scan(cnt, ex, tot);
 #pragma unroll
@@ -344,6 +400,10 @@ __device__ void build_plan(const StepParams& p) {
     pl.header[2] = n;
     pl.header[3] = overflow ? 0 : (int)total[4];
     for (int c = 0; c < kItemCounters; ++c) *item_counter(pl, c) = 0ull;
+    *header_total(pl, kHeaderSplitKeys) = overflow ? 0 : s_mix[0];
+    *header_total(pl, kHeaderPrefillWork) = overflow ? 0 : s_mix[1];
+    pl.header[kHeaderPrefillCtas] =
+        (overflow || !mixed) ? 0 : prefill_role_ctas(p, s_mix[0], s_mix[1], n, p.sm_count);
   }
 }
 
