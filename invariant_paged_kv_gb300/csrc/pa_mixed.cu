@@ -48,8 +48,6 @@ cudaError_t launch_m(const StepParams& p, const CUtensorMap& q, const CUtensorMa
 
 }  // namespace
 
-int num_sms();
-
 // One CTA per SM.
 cudaError_t launch_mixed(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
                          const CUtensorMap& v, cudaStream_t s) {

@@ -250,7 +250,9 @@ __device__ int prefill_role_ctas(const StepParams& p, long long split_keys, long
   const float cand[2] = {m1, m2};
   for (int c = 0; c < 2; ++c)
     for (int d = -1; d <= 1; ++d) {
-      const int m = min(nctas - 1, max(1, (int)cand[c] + d));
+      // (the crossing can lie far outside [1, nctas - 1]: clamp before the
+      // conversion to int)
+      const int m = min(nctas - 1, max(1, (int)fminf(fmaxf(cand[c], 0.f), (float)nctas) + d));
       const float tm = t(m);
       if (tm < best_t) {
         best_t = tm;
