@@ -17,12 +17,12 @@ cudaError_t launch_decode_bf16(const StepParams& p, const CUtensorMap& k, const 
 cudaError_t launch_decode_fp8(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
                               long long max_items, cudaStream_t s);
 cudaError_t launch_split_f32(const StepParams& p, long long max_items, cudaStream_t s);
-cudaError_t launch_rows_bf16(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
-                             long long max_items, cudaStream_t s);
 int rows_group_size(int g);
 cudaError_t launch_combine(const StepParams& p, cudaStream_t s);
 cudaError_t launch_mixed(const StepParams& p, const CUtensorMap& q, const CUtensorMap& k,
                          const CUtensorMap& v, cudaStream_t s);
+cudaError_t launch_row_mixed(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
+                             cudaStream_t s);
 
 void decode_gemm_plan(int N, int K, int* S, int* chunks_per_split);
 cudaError_t launch_decode_gemm(void* y, float* part, int T_pad, int N, int K, int S, int cps,
@@ -483,18 +483,14 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
   // steps with prefill chunks on the tensor cores run decode and prefill in
   // one launch on disjoint SMs (the phase events then see it all as the
   // split phase)
-  cudaError_t e = prefill_tc ? launch_mixed(p, tmQ, tmK, tmV, s)
-                  : fp8      ? launch_decode_fp8(p, tmK, tmV, items, s)
+  cudaError_t e = prefill_tc    ? launch_mixed(p, tmQ, tmK, tmV, s)
+                  : p.group_rows ? launch_row_mixed(p, tmK, tmV, s)
+                  : fp8          ? launch_decode_fp8(p, tmK, tmV, items, s)
                   : dtype == PA_BF16 ? launch_decode_bf16(p, tmK, tmV, items, s)
                                      : launch_split_f32(p, items, s);
   if (e != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
   if (record(events, n_events, 2, s) != PA_OK) return PA_ERR_CUDA;
-  if (p.group_rows) {
-    // group records never outnumber the grouped rows' (row, split) entries
-    if (launch_rows_bf16(p, tmK, tmV, items, s) != cudaSuccess) return PA_ERR_CUDA;
-    count_launches(1);
-  }
   if (record(events, n_events, 3, s) != PA_OK) return PA_ERR_CUDA;
   if (launch_combine(p, s) != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);

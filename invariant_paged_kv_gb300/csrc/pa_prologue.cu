@@ -223,19 +223,19 @@ __device__ bool row_counts(const StepParams& p, const LaneCache* lc, int u, int&
   return true;
 }
 
-// Prefill-role CTAs of the mixed-step kernel out of nctas (one per SM): the
-// split that balances the two roles' times, from the step's work totals and
-// per-SM rates measured on this part with the two roles running side by side
-// -- the decode role streams ~66 GB/s per SM up to ~6760 GB/s in all, the
-// prefill role runs ~4.0 TFLOP/s per SM. fp32 (the part's fp64 rate is low);
-// it decides only where work runs, never its result.
+// Prefill-role CTAs of a mixed kernel out of nctas (one per SM): the split
+// that balances the two roles' times, from the step's work totals and per-SM
+// rates measured on this part with the roles running side by side -- the
+// decode role streams ~66 GB/s per SM up to ~6760 GB/s in all; the prefill
+// role runs pf_rate flop/s per SM (~4.0 TFLOP/s for the tensor-core prefill,
+// ~1.0 TFLOP/s for the row-invariant mode's prefill rows on mma.sync). fp32
+// (the part's fp64 rate is low); it decides only where work runs, never its
+// result.
 __device__ int prefill_role_ctas(const StepParams& p, long long split_keys, long long pf_work,
-                                 int pf_tiles, int nctas) {
-  const int g = p.H / p.Hkv;
-  const long long pf_items = (long long)pf_tiles * p.Hkv * ((g + 1) / 2);
+                                 long long pf_items, float pf_rate, int nctas) {
   if (pf_work <= 0 || pf_items <= 0 || nctas <= 1) return 0;
   if (split_keys <= 0) return nctas;
-  const float kDecPerSm = 66e9f, kDecMax = 6760e9f, kPfPerSm = 4.0e12f;
+  const float kDecPerSm = 66e9f, kDecMax = 6760e9f, kPfPerSm = pf_rate;
   const float a = 4.f * p.D * p.H * (float)pf_work / kPfPerSm;               // prefill SM-seconds
   const float b = (float)split_keys * p.Hkv * p.D * 2.f * p.elem_bytes;      // decode bytes
   auto t = [&](int m) {  // the later of the two roles with m prefill CTAs
@@ -293,11 +293,11 @@ __device__ void build_plan(const StepParams& p) {
 
   const int units = p.split_all_rows ? p.T : p.B;
   long long total[kCounters] = {0, 0, 0, 0, 0};
-  // work totals for the mixed-step kernel's role split (steps with prefill
-  // tiles only): keys of the split-path rows, (row, key) pairs of the prefill
-  // rows -- rows j = 0 .. q-1 of a lane attend c - q + j + 1 keys
+  // work totals for the mixed kernels' role split (steps with prefill rows
+  // only): keys of the split-path decode rows, (row, key) pairs of the
+  // prefill rows -- rows j = 0 .. q-1 of a lane attend c - q + j + 1 keys
   __shared__ long long s_mix[2];
-  const bool mixed = !p.split_all_rows && p.max_q_len >= 2;
+  const bool mixed = (!p.split_all_rows || p.group_rows) && p.max_q_len >= 2;
   if (tid < 2) s_mix[tid] = 0;
   __syncthreads();
   for (int base = 0; base < units; base += nth) {
@@ -306,7 +306,9 @@ __device__ void build_plan(const StepParams& p) {
     int r;
     const bool ok0 = row_counts(p, lc, base + tid, r, cnt, rp);
     if (mixed) {
-      long long w[2] = {ok0 && rp.split ? (long long)rp.keys : 0, 0};
+      const bool grouped = ok0 && p.group_rows && rp.q >= 2;  // a prefill row, row mode
+      long long w[2] = {ok0 && rp.split && !grouped ? (long long)rp.keys : 0,
+                        grouped ? (long long)rp.keys : 0};
       if (ok0 && rp.tiles && rp.j == 0)
         w[1] = (long long)rp.q * (rp.c - rp.q) + (long long)rp.q * (rp.q + 1) / 2;
 #pragma unroll
@@ -404,8 +406,14 @@ __device__ void build_plan(const StepParams& p) {
     for (int c = 0; c < kItemCounters; ++c) *item_counter(pl, c) = 0ull;
     *header_total(pl, kHeaderSplitKeys) = overflow ? 0 : s_mix[0];
     *header_total(pl, kHeaderPrefillWork) = overflow ? 0 : s_mix[1];
+    const int g = p.H / p.Hkv;
     pl.header[kHeaderPrefillCtas] =
-        (overflow || !mixed) ? 0 : prefill_role_ctas(p, s_mix[0], s_mix[1], n, p.sm_count);
+        (overflow || !mixed) ? 0
+        : p.group_rows ? prefill_role_ctas(p, s_mix[0], s_mix[1], total[4] * p.Hkv, 1.0e12f,
+                                           p.sm_count)
+                       : prefill_role_ctas(p, s_mix[0], s_mix[1],
+                                           (long long)n * p.Hkv * ((g + 1) / 2), 4.0e12f,
+                                           p.sm_count);
   }
 }
 

@@ -24,11 +24,17 @@
 // has no keys left in a chunk skips the chunk's update (its max, sum and
 // rescale factor stay as they are, its p values are zero).
 // Every wait is bounded (PA_FLAG_TIMEOUT).
+//
+// The work is written as the code of one CTA (rows_bf16_cta): it runs as the
+// prefill-row role of the row-mode mixed kernel (pa_mixed.cu), which gives
+// every CTA this role when a step has no decode rows.
+#pragma once
+
 #include "pa_split_bf16_row.cuh"
 
 namespace pa {
+namespace rows {
 
-namespace {
 
 constexpr int kRW = kRowWarps;  // consumer warps
 constexpr int kNTW = 2;         // 8-column N tiles per consumer warp
@@ -154,13 +160,13 @@ struct ColAcc {
   }
 };
 
+// The work of one CTA of kRThreads threads (see above); dsmem holds
+// RTile<D>::kSmemBytes bytes.
 template <int D>
-__global__ void __launch_bounds__(kRThreads, 1)
-    rows_bf16_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
-                     const __grid_constant__ CUtensorMap tmV) {
+__device__ __forceinline__ void rows_bf16_cta(const StepParams& p, const CUtensorMap* tmK,
+                                              const CUtensorMap* tmV, uint8_t* dsmem) {
   using TL = RTile<D>;
   constexpr int KS = D / 16;
-  extern __shared__ uint8_t dsmem[];
   // zeroed[st]: warp 0 has zeroed the V rows past the group's keys in stage
   // st (a group's last, partial chunk); one phase per such use of the stage,
   // and the stage is reused only after every consumer released it, so a
@@ -189,8 +195,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
     }
     s_abort = 0;
     fence_mbar_init();
-    prefetch_tensormap(&tmK);
-    prefetch_tensormap(&tmV);
+    prefetch_tensormap(tmK);
+    prefetch_tensormap(tmV);
   }
   __syncthreads();
 
@@ -240,8 +246,8 @@ __global__ void __launch_bounds__(kRThreads, 1)
           mbar_expect_tx(smem_u32(&full[st]), TL::kStageBytes);
 #pragma unroll
           for (int h = 0; h < TL::kHalves; ++h) {
-            tma_load_3d(ks + h * TL::kHalfBytes, &tmK, h * 64, kvh, tok, smem_u32(&full[st]));
-            tma_load_3d(vs + h * TL::kHalfBytes, &tmV, h * 64, kvh, tok, smem_u32(&full[st]));
+            tma_load_3d(ks + h * TL::kHalfBytes, tmK, h * 64, kvh, tok, smem_u32(&full[st]));
+            tma_load_3d(vs + h * TL::kHalfBytes, tmV, h * 64, kvh, tok, smem_u32(&full[st]));
           }
         }
       }
@@ -407,35 +413,5 @@ __global__ void __launch_bounds__(kRThreads, 1)
   }
 }
 
-template <int D>
-cudaError_t launch_r(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v, int grid,
-                     cudaStream_t s) {
-  auto kern = rows_bf16_kernel<D>;
-  static unsigned long long done = 0;
-  cudaError_t e = smem_opt_in(kern, RTile<D>::kSmemBytes, &done);
-  if (e != cudaSuccess) return e;
-  kern<<<grid, kRThreads, RTile<D>::kSmemBytes, s>>>(p, k, v);
-  return cudaGetLastError();
-}
-
-}  // namespace
-
-int num_sms();
-
-// Rows per group for a GQA group of g heads: as many rows as fill the CTA's
-// kCols (row, head) columns; 0 (no grouping: the rows take the decode path)
-// when one row's heads do not fit.
-int rows_group_size(int g) { return g >= 1 && g <= kCols ? kCols / g : 0; }
-
-// max_items: an upper bound on (group, split, kv head) items of the step.
-cudaError_t launch_rows_bf16(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
-                             long long max_items, cudaStream_t s) {
-  long long cap = num_sms();
-  int grid = (int)(max_items < cap ? max_items : cap);
-  if (grid < 1) grid = 1;
-  const int g = p.H / p.Hkv;
-  if (p.group_rows != rows_group_size(g) || p.group_rows < 1) return cudaErrorInvalidValue;
-  return p.D == 128 ? launch_r<128>(p, k, v, grid, s) : launch_r<64>(p, k, v, grid, s);
-}
-
+}  // namespace rows
 }  // namespace pa
