@@ -19,14 +19,13 @@ namespace pa {
 
 namespace {
 
-constexpr int kWarps = 8;   // heads per CTA (one warp per (row, head))
-constexpr int kAhead = 8;   // splits loaded ahead of the fold
+constexpr int kWarps = 8;  // heads per CTA (one warp per (row, head))
 
 // One warp folds the splits of one (row, head); lane l owns dims 4l .. 4l+3
 // (D = 128) or 2l .. 2l+1 (D = 64). The loads of kAhead splits are issued
 // before their fold so the memory system sees many requests at once; the fold
-// itself runs strictly in split order.
-template <int D>
+// itself runs strictly in split order, so kAhead changes no bit.
+template <int D, int kAhead>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p) {
   constexpr int VPL = D / 32;  // values per lane
   using Vec = typename std::conditional<VPL == 4, float4, float2>::type;
@@ -112,13 +111,26 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p
 
 }  // namespace
 
+// Load depth per warp against resident warps: decode rows with long split
+// lists go faster with 8 splits in flight; when prefill rows take the split
+// path (the row-invariant mode), most folded rows have a few splits and a
+// depth of 2 goes faster: 32 registers a thread admit 8 CTAs per SM where
+// depth 8 admits 3.
 cudaError_t launch_combine(const StepParams& p, cudaStream_t s) {
   if (p.T <= 0) return cudaSuccess;
   dim3 grid(p.T, (p.H + kWarps - 1) / kWarps);
-  if (p.D == 128)
-    combine_kernel<128><<<grid, kWarps * 32, 0, s>>>(p);
-  else
-    combine_kernel<64><<<grid, kWarps * 32, 0, s>>>(p);
+  const bool shallow = p.split_all_rows && p.max_q_len >= 2;
+  if (p.D == 128) {
+    if (shallow)
+      combine_kernel<128, 2><<<grid, kWarps * 32, 0, s>>>(p);
+    else
+      combine_kernel<128, 8><<<grid, kWarps * 32, 0, s>>>(p);
+  } else {
+    if (shallow)
+      combine_kernel<64, 2><<<grid, kWarps * 32, 0, s>>>(p);
+    else
+      combine_kernel<64, 8><<<grid, kWarps * 32, 0, s>>>(p);
+  }
   return cudaGetLastError();
 }
 
