@@ -40,6 +40,7 @@ sys.path.insert(0, ROOT)
 
 METRIC = "decode-attention KV GB/s (% of GB300 HBM peak) and tokens/s per ragged step"
 FALLBACK_HBM_GBS = 6800.0
+NOMINAL_HBM_GBS = 8000.0  # GB300 HBM3e data-sheet rate (~8 TB/s)
 # committed ncu summaries of the decode kernels and the sources they were taken on
 PROFILES = {
     False: (os.path.join(ROOT, "profiles", "decode_bf16_long_tail.md"),
@@ -596,6 +597,7 @@ def run_ours(args, rank, world, local_rank):
         "config": workload_config(step, layers, name, args),
         "rows_per_s": round(rows_per_s, 1),
         "frac_of_hbm_peak": round(value / peak, 4),
+        "frac_of_nominal_hbm": round(value / NOMINAL_HBM_GBS, 4),
         "bytes_per_step": step_bytes,
         "phase_ms_per_layer": {k: round(v, 4) for k, v in phase_ms.items()},
         "roofline": roofline, "prefill_roofline": prefill, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
@@ -814,6 +816,7 @@ def run_gemm(args, rank, world, local_rank):
                    "l2": "no flush: the 2.5 GB weight exceeds the 129 MB L2",
                    "small": bool(args.small), "cuda_graph": not args.no_graph},
         "frac_of_hbm_peak": round(value / peak, 4),
+        "frac_of_nominal_hbm": round(value / NOMINAL_HBM_GBS, 4),
         "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
         "clocks": clk,
     }
