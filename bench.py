@@ -549,15 +549,22 @@ def run_ours(args, rank, world, local_rank):
     achieved = nbytes["decode_kernel"] / (dec_ms * 1e-3) / 1e9
     fp8 = g.dtype == "fp8"
     traffic, sha = committed_traffic(fp8)
-    # bf16 steps with prefill chunks in the batch-invariant mode run the decode
-    # and the tensor-core prefill in one launch on disjoint SMs: both rooflines
-    # are then taken over that launch's time
-    mixed = bool(wl.prefill_flops(step)) and args.mode == "batch" and g.dtype == "bf16"
-    if mixed:
-        traffic = None  # the committed decode capture is of the decode-only kernel
+    # bf16 steps with prefill chunks run the decode and the prefill in one
+    # launch on disjoint SMs (the tcgen05 prefill in the batch-invariant mode,
+    # the prefill-row role in the row-invariant mode): both rooflines are then
+    # taken over that launch's time
+    has_pf = bool(wl.prefill_flops(step)) and g.dtype == "bf16"
+    mixed = has_pf and args.mode == "batch"
+    row_mixed = has_pf and args.mode == "row"
+    # the committed DRAM counters are of the decode-only kernel on the
+    # full-size long-tail step; other workloads have none
+    if mixed or row_mixed or args.workload != "long_tail" or args.small:
+        traffic = None
     roofline = {"bound": "hbm",
                 "kernel": ("mixed_kernel (split-KV decode and tcgen05 prefill on disjoint SMs, "
                            "one launch)" if mixed else
+                           "row_mixed_kernel (split-KV decode and the prefill-row role on "
+                           "disjoint SMs, one launch)" if row_mixed else
                            "decode_fp8_kernel (split-KV decode partials, e4m3 codes)" if fp8
                            else "decode_bf16_kernel (split-KV decode partials)"),
                 "achieved": round(achieved, 1), "peak": peak, "unit": "GB/s",
@@ -577,6 +584,15 @@ def run_ours(args, rank, world, local_rank):
                    "achieved": round(ach, 1), "peak": tpeak, "unit": "TFLOP/s",
                    "peak_kind": tkind, "frac": round(ach / tpeak, 4),
                    "flops_per_launch": pf, "avg_launch_ms": round(pf_ms, 4)}
+    elif row_mixed:  # prefill rows on mma.sync, in the same launch as the decode
+        tpeak, tkind = measured_bf16_peak(sustained=True)
+        ach = pf / (dec_ms * 1e-3) / 1e12
+        prefill = {"bound": "tensor",
+                   "kernel": "row_mixed_kernel, prefill-row role (mma.sync, bf16 -> fp32; "
+                             "shares the launch and its SMs with the decode role)",
+                   "achieved": round(ach, 1), "peak": tpeak, "unit": "TFLOP/s",
+                   "peak_kind": tkind, "frac": round(ach / tpeak, 4),
+                   "flops_per_launch": pf, "avg_launch_ms": round(dec_ms, 4)}
 
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
