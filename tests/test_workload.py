@@ -81,9 +81,40 @@ def _check_step(step):
         assert np.all(row[n:] == -1)
 
 
-@pytest.mark.parametrize("make", [wl.tiny_f32, wl.decode_batch, wl.mixed_step])
+def _long_tail_small_pool(sample):
+    return wl.long_tail(sample, pool_bytes_per_layer=1e8)  # pool = the used blocks
+
+
+@pytest.mark.parametrize("make", [wl.tiny_f32, wl.decode_batch, wl.mixed_step,
+                                  _long_tail_small_pool])
 def test_configs_well_formed(make):
     _check_step(make(0))
+
+
+def test_mixed_step_recipe():
+    """Decode lanes first (q_len 1, ctx in [16, 16384]), then 8 chunks of 512
+    new rows after U{0..4096} earlier keys."""
+    for sample in range(3):
+        s = wl.mixed_step(sample)
+        assert list(s.q_lens[:120]) == [1] * 120 and list(s.q_lens[120:]) == [512] * 8
+        assert s.ctx_lens[:120].min() >= 16 and s.ctx_lens[:120].max() <= 16384
+        offs = s.ctx_lens[120:] - 512
+        assert offs.min() >= 0 and offs.max() <= 4096
+
+
+def test_length_distributions_follow_the_recipe():
+    """Seeded lognormal medians (decode_batch 2048, mixed decode rows 3000) and
+    the long tail's 90/10 split, over several samples."""
+    dec = np.concatenate([wl.decode_batch(k).ctx_lens for k in range(5)])
+    assert 1600 <= np.median(dec) <= 2600
+    mix = np.concatenate([wl.mixed_step(k).ctx_lens[:120] for k in range(5)])
+    assert 2400 <= np.median(mix) <= 3700
+    for k in range(3):
+        c = wl.long_tail(k, pool_bytes_per_layer=1e8).ctx_lens
+        short, long_ = c[c < 16384], c[c >= 16384]
+        assert len(short) == 230 and len(long_) == 26
+        assert short.min() >= 1024 and short.max() <= 4096
+        assert long_.min() >= 16384 and long_.max() <= 40960
 
 
 def test_config_shapes():
