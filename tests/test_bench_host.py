@@ -74,3 +74,16 @@ def test_committed_profiles_name_existing_sources():
         assert os.path.isfile(summary), summary
         for rel in sources:
             assert os.path.isfile(os.path.join(bench.ROOT, rel)), rel
+
+
+def test_reference_arm_runs_on_rank_zero_only():
+    """Under torchrun the reference arm (the oracle on the host cores) runs on
+    rank 0 alone; every other rank exits 0 at once and prints nothing."""
+    import subprocess
+    env = dict(os.environ, RANK="1", WORLD_SIZE="2", LOCAL_RANK="1",
+               MASTER_ADDR="127.0.0.1", MASTER_PORT="29999")
+    r = subprocess.run([sys.executable, os.path.join(bench.ROOT, "bench.py"), "--impl",
+                        "reference", "--gpus", "2", "--steps", "1", "--warmup", "3"],
+                       env=env, capture_output=True, text=True, timeout=120)
+    assert r.returncode == 0, r.stderr
+    assert r.stdout.strip() == ""
