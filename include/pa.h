@@ -238,11 +238,13 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
  *   events    array of n_events cudaEvent_t handles (may be NULL / 0). They
  *             are recorded on `stream` in this order, as far as n_events
  *             reaches: [0] before the first launch, [1] after the write +
- *             plan prologue, [2] after the split kernel, [3] after the
- *             prefill kernel (no launch between [2] and [3] when no row
- *             takes the prefill path), [4] after the combine. When `stream`
- *             is being captured into a CUDA graph the events become
- *             event-record nodes of the graph (recorded at each replay).
+ *             plan prologue, [2] after the work launch (the split kernel, or
+ *             on steps with prefill rows the launch that runs the split work
+ *             and the prefill side by side), [3] at the same point (the
+ *             prefill has no launch of its own), [4] after the combine.
+ *             When `stream` is being captured into a CUDA graph the events
+ *             become event-record nodes of the graph (recorded at each
+ *             replay).
  */
 pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cache,
                           const int32_t* block_tables, int32_t max_blocks_per_seq,
