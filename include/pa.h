@@ -208,7 +208,8 @@ size_t pa_attention_workspace_bytes_ex(int32_t B, int32_t T, int32_t max_q_len,
  * split into ranges [S i, S (i + 1)) with S = 512 * 2^j for the smallest j
  * that gives at most 128 ranges (512-key ranges up to K = 65536), each range
  * reduced in ascending key order, and the ranges folded left to right in
- * fp32. Lanes with q_len >= 2 take the prefill path. Which path a row
+ * fp32. In bf16 steps lanes with q_len >= 2 take the tensor-core prefill
+ * path; fp32 steps take the split path for every row. Which path a row
  * takes, its split points and its reduction order depend only on its own
  * lane.
  */
