@@ -25,6 +25,10 @@ binary32, so widening is a 16-bit shift); fp32 data as float32. With the
 under one scale per tensor: the write quantises the new rows and the gather
 reads codes back as decode(code) * scale (oracle/e4m3.py).
 
+``attend_row_terms`` adds, for the tests' rounding-error bound, plain sums over
+a row's softmax weights (weighted magnitudes of V and of the scores' terms);
+they are pinned like the rest and do not enter the output.
+
 Readings where the pages leave a step open (listed with their reasons in the
 design notes of this repository):
   * ``ctx_lens`` counts the keys after this step's write, so a lane with
@@ -164,6 +168,42 @@ def row_weights(q_row, K, position: int, scale: float, h: int) -> np.ndarray:
     return softmax_weights(scale * (K[:n, kv, :] @ q_row[h]))
 
 
+def attend_row_terms(q_row, K, V, position: int, scale: float) -> dict:
+    """Sums over one row's softmax weights that size a rounding-error bound
+    for a computed version of ``attend_row`` (the weights are ``row_weights``;
+    nothing here changes what attention computes).
+
+    For head h, its kv head k, the row's weights w_i over its visible keys
+    and c_i = sum_d |q[h, d]| |K[i, k, d]| (the size of key i's score before
+    scaling), all float64:
+        wv[h, d]   = sum_i w_i |V[i, k, d]|
+        w2v2[h, d] = sum_i w_i^2 V[i, k, d]^2
+        w2v[h, d]  = sum_i w_i^2 |V[i, k, d]|
+        wcv[h, d]  = sum_i w_i c_i |V[i, k, d]|
+        w2[h]      = sum_i w_i^2
+        wc[h]      = sum_i w_i c_i
+        cmax[h]    = max_i c_i
+    """
+    H, D = q_row.shape
+    Hkv = K.shape[1]
+    n = visible_keys(position)
+    t = {name: np.empty((H, D)) for name in ("wv", "w2v2", "w2v", "wcv")}
+    t.update({name: np.empty(H) for name in ("w2", "wc", "cmax")})
+    for h in range(H):
+        kv = kv_head_of(h, H, Hkv)
+        w = row_weights(q_row, K, position, scale, h)
+        v = V[:n, kv, :]
+        c = np.abs(K[:n, kv, :]) @ np.abs(q_row[h])
+        t["wv"][h] = w @ np.abs(v)
+        t["w2v2"][h] = (w * w) @ (v * v)
+        t["w2v"][h] = (w * w) @ np.abs(v)
+        t["wcv"][h] = (w * c) @ np.abs(v)
+        t["w2"][h] = np.sum(w * w)
+        t["wc"][h] = np.sum(w * c)
+        t["cmax"][h] = np.max(c)
+    return t
+
+
 def widen_kv(x, dtype: str, kv_scale: float) -> np.ndarray:
     """Exact float64 values of cache elements: e4m3 codes times their
     tensor's scale for 'fp8', ``widen`` otherwise."""
@@ -175,14 +215,16 @@ def widen_kv(x, dtype: str, kv_scale: float) -> np.ndarray:
 def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens,
               scale: float, dtype: str, block_size: int,
               slot_mapping=None, k_new=None, v_new=None, rows=None,
-              k_scale: float = 1.0, v_scale: float = 1.0):
+              k_scale: float = 1.0, v_scale: float = 1.0, terms: bool = False):
     """Reference output of one flat ragged step, float64 ``[T, H, D]``.
 
     When new rows are given they are written first (the step writes, then
     attends); with dtype 'fp8' they are quantised under ``k_scale`` /
     ``v_scale`` on the way in. ``rows`` optionally restricts the work to a
     subset of flat rows (others are left NaN), for sampled checks of large
-    steps. Returns (out, k_cache_after, v_cache_after).
+    steps. Returns (out, k_cache_after, v_cache_after), and with ``terms``
+    a fourth item: ``attend_row_terms`` of every computed row, stacked into
+    ``[T, H, D]`` / ``[T, H]`` arrays (NaN elsewhere).
     """
     if k_new is not None:
         if dtype == "fp8":
@@ -198,6 +240,10 @@ def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens,
     B = ctx.shape[0]
     want = None if rows is None else set(int(r) for r in rows)
     out = np.full((T, H, D), np.nan, dtype=np.float64)
+    tt = None
+    if terms:
+        tt = {name: np.full((T, H, D), np.nan) for name in ("wv", "w2v2", "w2v", "wcv")}
+        tt.update({name: np.full((T, H), np.nan) for name in ("w2", "wc", "cmax")})
     for b in range(B):
         q_len = int(cu[b + 1] - cu[b])
         if q_len == 0:
@@ -212,29 +258,18 @@ def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens,
                 continue
             position = int(ctx[b]) - q_len + j
             out[r] = attend_row(widen(q[r], q_dtype), K, V, position, scale)
+            if terms:
+                for name, val in attend_row_terms(widen(q[r], q_dtype), K, V, position,
+                                                  scale).items():
+                    tt[name][r] = val
+    if terms:
+        return out, k_cache, v_cache, tt
     return out, k_cache, v_cache
 
 
 # ---------------------------------------------------------------------------
 # partials and their ordered fold (KV-parallel page owners)
 # ---------------------------------------------------------------------------
-
-def split_length(keys: int, base: int = 512, max_splits: int = 128) -> int:
-    """Keys per split of a row with ``keys`` keys: base * 2^j for the smallest
-    j that leaves at most ``max_splits`` splits (a function of the row's own
-    key count only: "Numerics envelopes", The hierarchy, invariance.batch, no
-    split count that scales with batch or occupancy)."""
-    s = base
-    while -(-keys // s) > max_splits:
-        s *= 2
-    return s
-
-
-def split_starts(keys: int):
-    """First key of every split of a row with ``keys`` keys."""
-    s = split_length(keys)
-    return list(range(0, keys, s))
-
 
 def row_partial(q_row, K, V, lo: int, hi: int, scale: float, h: int):
     """Unnormalised softmax partial of head h over keys [lo, hi), float64:

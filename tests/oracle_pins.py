@@ -24,12 +24,12 @@ What pins what:
                              float8_e4m3fn cast (inside the finite range)
   * fp8 brute force       -> fp8 paged oracle == codes read by torch, scaled,
                              scipy softmax on the unpaged sequence
-  * split length          -> its defining property (fewest splits <= 128 with
-                             the shortest length 512 * 2^j) and named values
   * fold of partials      -> any key partition folds back to the row's
                              attention (1e-12); one partial folds to acc / l
   * decode linear         -> explicit triple loops on small shapes; identity
-                             weights return x
+                             weights return x; the |x| |w| sums likewise
+  * bound terms           -> explicit loops over scipy's softmax weights; a
+                             single key and a zero query give closed forms
 """
 import json
 import math
@@ -432,22 +432,6 @@ def check_fp8_brute_force():
     return None
 
 
-def check_split_length():
-    cases = {1: 512, 512: 512, 65536: 512, 65537: 1024, 131072: 1024, 131073: 2048,
-             10 ** 6: 8192}
-    for keys, want in cases.items():
-        if pa.split_length(keys) != want:
-            return f"split_length({keys}) = {pa.split_length(keys)}, want {want}"
-    for keys in (1, 7, 513, 40000, 70000, 300000, 2 ** 21 + 3):
-        s = pa.split_length(keys)
-        if -(-keys // s) > 128 or (s > 512 and -(-keys // (s // 2)) <= 128):
-            return f"split_length({keys}) = {s} is not the smallest length with <= 128 splits"
-        st = pa.split_starts(keys)
-        if st[0] != 0 or any(b - a != s for a, b in zip(st, st[1:])) or st[-1] >= keys:
-            return f"split_starts({keys}) do not tile the row"
-    return None
-
-
 def check_fold_partials():
     """Folding the partials of any partition of a row's keys, in key order,
     gives the row's attention (a partition-independence identity of softmax)."""
@@ -498,12 +482,85 @@ def check_decode_gemm_brute_force():
     return None
 
 
+def check_decode_gemm_abs_sum():
+    """sum_k |x[t, k] w[n, k]| (the size the decode-GEMM rounding bound
+    scales with) against explicit loops over torch's own bf16 widening."""
+    g = torch.Generator().manual_seed(78)
+    for T, N, K in ((1, 1, 1), (3, 5, 7), (4, 8, 16)):
+        x = torch.randn(T, K, generator=g).to(torch.bfloat16)
+        w = torch.randn(N, K, generator=g).to(torch.bfloat16)
+        got = dg.abs_sum(to_store(x), to_store(w))
+        xf, wf = as_f64(x), as_f64(w)
+        if got.shape != (T, N):
+            return "abs_sum has the wrong shape"
+        for t in range(T):
+            for n in range(N):
+                acc = 0.0
+                for k in range(K):
+                    acc += abs(xf[t, k] * wf[n, k])
+                if abs(got[t, n] - acc) > 1e-12 * max(1.0, acc):
+                    return f"abs_sum [{T}x{K}]x[{N}x{K}] differs from loops at ({t},{n})"
+    return None
+
+
+def check_row_terms():
+    """The bound terms of one row against explicit loops over scipy's softmax
+    weights, and their closed forms for a single key and a zero query."""
+    rng = np.random.default_rng(57)
+    H, Hkv, D, L = 6, 3, 8, 11
+    q = rng.standard_normal((H, D))
+    K = rng.standard_normal((L, Hkv, D))
+    V = rng.standard_normal((L, Hkv, D))
+    scale, pos = 0.4, 7
+    got = pa.attend_row_terms(q, K, V, pos, scale)
+    for h in range(H):
+        kv = h // (H // Hkv)
+        n = pos + 1
+        w = scipy.special.softmax(scale * np.array([sum(q[h, d] * K[i, kv, d] for d in range(D))
+                                                     for i in range(n)]))
+        c = [sum(abs(q[h, d]) * abs(K[i, kv, d]) for d in range(D)) for i in range(n)]
+        want = {"w2": sum(w[i] ** 2 for i in range(n)), "wc": sum(w[i] * c[i] for i in range(n)),
+                "cmax": max(c)}
+        for name, val in want.items():
+            if abs(got[name][h] - val) > 1e-12 * max(1.0, abs(val)):
+                return f"row terms: {name}[{h}] = {got[name][h]}, loops give {val}"
+        for d in range(D):
+            v = [V[i, kv, d] for i in range(n)]
+            want = {"wv": sum(w[i] * abs(v[i]) for i in range(n)),
+                    "w2v2": sum(w[i] ** 2 * v[i] ** 2 for i in range(n)),
+                    "w2v": sum(w[i] ** 2 * abs(v[i]) for i in range(n)),
+                    "wcv": sum(w[i] * c[i] * abs(v[i]) for i in range(n))}
+            for name, val in want.items():
+                if abs(got[name][h, d] - val) > 1e-12 * max(1.0, abs(val)):
+                    return f"row terms: {name}[{h},{d}] = {got[name][h, d]}, loops give {val}"
+    # one key: w = 1
+    one = pa.attend_row_terms(q, K, V, 0, scale)
+    v0 = np.abs(V[0])[[h // (H // Hkv) for h in range(H)]]
+    c0 = np.array([np.abs(q[h]) @ np.abs(K[0, h // (H // Hkv)]) for h in range(H)])
+    if not (np.allclose(one["wv"], v0, rtol=1e-15, atol=0) and
+            np.allclose(one["w2v2"], v0 ** 2, rtol=1e-15, atol=0) and
+            np.allclose(one["w2"], 1.0, rtol=1e-15, atol=0) and
+            np.allclose(one["cmax"], c0, rtol=1e-15, atol=0) and
+            np.allclose(one["wcv"], c0[:, None] * v0, rtol=1e-14, atol=0)):
+        return "row terms of a single key are not |v0|, v0^2, 1, c0, c0 |v0|"
+    # zero query: every weight is 1 / n and every c_i is 0
+    z = pa.attend_row_terms(np.zeros((H, D)), K, V, pos, scale)
+    n = pos + 1
+    vv = V[:n][:, [h // (H // Hkv) for h in range(H)], :]
+    if not (np.allclose(z["w2"], 1.0 / n, rtol=1e-14, atol=0) and
+            np.allclose(z["wv"], np.abs(vv).mean(axis=0), rtol=1e-13, atol=0) and
+            np.allclose(z["w2v2"], (vv ** 2).sum(axis=0) / n ** 2, rtol=1e-13, atol=0) and
+            not np.any(z["wc"]) and not np.any(z["wcv"]) and not np.any(z["cmax"])):
+        return "row terms of a zero query are not the uniform-weight closed forms"
+    return None
+
+
 ALL_CHECKS = [check_single_key, check_zero_query_mean, check_position_code,
               check_constant_v_per_head, check_one_hot, check_brute_force,
               check_block_permutation, check_weights_sum, check_write_bytes,
               check_kv_bytes_golden, check_e4m3_values_golden, check_e4m3_nearest,
-              check_e4m3_scaled_quantize, check_fp8_brute_force, check_split_length,
-              check_fold_partials, check_decode_gemm_brute_force]
+              check_e4m3_scaled_quantize, check_fp8_brute_force, check_fold_partials,
+              check_decode_gemm_brute_force, check_decode_gemm_abs_sum, check_row_terms]
 
 
 def failures():

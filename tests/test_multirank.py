@@ -68,11 +68,11 @@ def test_single_rank_identity():
 def _canonical(step):
     """(row, split) -> entry in the canonical partial layout: rows in flat
     order, each row's splits in order."""
-    import oracle.paged_attention as opa
+    import split_rule
     idx, e = {}, 0
     pos = step.row_positions()
     for r in range(step.T):
-        for i, _ in enumerate(opa.split_starts(int(pos[r]) + 1)):
+        for i, _ in enumerate(split_rule.split_starts(int(pos[r]) + 1)):
             idx[(r, i)] = e
             e += 1
     return idx, e
@@ -87,6 +87,7 @@ def _kvp_rank(rank, world, port, out):
     import torch.distributed as dist
 
     import oracle.paged_attention as opa
+    import split_rule
     from helpers import to_store
     from invariant_paged_kv_gb300 import kv_parallel, workload as wl
     os.environ.update(MASTER_ADDR="127.0.0.1", MASTER_PORT=str(port))
@@ -116,8 +117,8 @@ def _kvp_rank(rank, world, port, out):
             for r in range(step.T):
                 b, p = int(lane_of[r]), int(pos[r])
                 K, V = seq(b)
-                starts = opa.split_starts(p + 1)
-                sl = opa.split_length(p + 1)
+                starts = split_rule.split_starts(p + 1)
+                sl = split_rule.split_length(p + 1)
                 for i, k0 in enumerate(starts):
                     if not (bounds[rank, b] <= k0 < bounds[rank + 1, b]):
                         continue  # another owner's split
@@ -133,7 +134,7 @@ def _kvp_rank(rank, world, port, out):
                 b, p = int(lane_of[r]), int(pos[r])
                 for h in range(H):
                     parts = []
-                    for i, k0 in enumerate(opa.split_starts(p + 1)):
+                    for i, k0 in enumerate(split_rule.split_starts(p + 1)):
                         w = max(x for x in range(W) if bounds[x, b] <= k0)
                         e = views[w, idx[(r, i)], h]
                         parts.append((float(e[0]), float(e[1]), e[2:].numpy()))
@@ -169,3 +170,23 @@ def test_kv_parallel_exchange_two_gloo_ranks():
     assert b0 == b1              # every rank merges to the same bits
     assert e0 <= 1e-12 and e1 <= 1e-12
     assert split0 >= 2           # lanes really were shared between the owners
+
+
+def test_split_rule_named_values():
+    """The tests' copy of the library's split rule: named values of the rule
+    pa_attention documents, its defining property, and agreement with the
+    host copy the KV-parallel owner bounds use."""
+    import sys
+    sys.path.insert(0, ROOT)
+    import split_rule
+    from invariant_paged_kv_gb300 import kv_parallel
+    cases = {1: 512, 512: 512, 65536: 512, 65537: 1024, 131072: 1024, 131073: 2048,
+             10 ** 6: 8192}
+    for keys, want in cases.items():
+        assert split_rule.split_length(keys) == want
+    for keys in (1, 7, 513, 40000, 70000, 300000, 2 ** 21 + 3):
+        s = split_rule.split_length(keys)
+        assert -(-keys // s) <= 128 and (s == 512 or -(-keys // (s // 2)) > 128)
+        st = split_rule.split_starts(keys)
+        assert st[0] == 0 and st[-1] < keys and all(b - a == s for a, b in zip(st, st[1:]))
+        assert kv_parallel.split_len(keys) == s

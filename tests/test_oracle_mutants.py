@@ -147,17 +147,46 @@ def _fold_drops_first(parts):
     return _orig_fold(parts[1:] if len(parts) > 1 else parts)
 
 
-def _split_length_off(keys, base=512, max_splits=128):
-    s = base
-    while -(-keys // s) >= max_splits:
-        s *= 2
-    return s
+_orig_terms = pa.attend_row_terms
+
+
+def _terms_w_not_squared(q_row, K, V, position, scale):
+    t = _orig_terms(q_row, K, V, position, scale)
+    t["w2v2"] = t["wv"] ** 2  # (sum w |v|)^2 in place of sum w^2 v^2
+    return t
+
+
+def _terms_signed_q(q_row, K, V, position, scale):
+    H, D = q_row.shape
+    t = _orig_terms(q_row, K, V, position, scale)
+    n = position + 1
+    for h in range(H):
+        kv = h // (H // K.shape[1])
+        t["cmax"][h] = np.max(np.abs(K[:n, kv, :] @ q_row[h]))
+    return t
+
+
+def _terms_drop_last_key(q_row, K, V, position, scale):
+    t = _orig_terms(q_row, K, V, max(position - 1, 0), scale)
+    return t
+
+
+TERMS_MUTANTS = {
+    "bound terms square the weighted mean instead of weighting squares": _terms_w_not_squared,
+    "bound terms take |q.k| for sum |q||k|": _terms_signed_q,
+    "bound terms drop the last key": _terms_drop_last_key,
+}
+
+
+@pytest.mark.parametrize("name", sorted(TERMS_MUTANTS))
+def test_terms_mutant_is_caught(name, monkeypatch):
+    monkeypatch.setattr(pa, "attend_row_terms", TERMS_MUTANTS[name])
+    assert oracle_pins.failures(), f"no pin caught the mutant '{name}'"
 
 
 FOLD_MUTANTS = {
     "fold forgets to rescale": ("fold_partials", _fold_unordered_max),
     "fold drops the first partial": ("fold_partials", _fold_drops_first),
-    "split length off by one split": ("split_length", _split_length_off),
 }
 
 
@@ -172,6 +201,10 @@ def _linear_drops_last_k(x_bits, w_bits):
     return _orig_linear(np.asarray(x_bits)[:, :-1], np.asarray(w_bits)[:, :-1])
 
 
+def _abs_sum_signed(x_bits, w_bits):
+    return np.abs(dg.widen_bf16(x_bits) @ dg.widen_bf16(w_bits).T)
+
+
 def _linear_wrong_widening(x_bits, w_bits):
     x = (np.asarray(x_bits).astype(np.uint32) << np.uint32(15)).view(np.float32).astype(np.float64)
     return x @ dg.widen_bf16(w_bits).T
@@ -181,6 +214,7 @@ GEMM_MUTANTS = {
     "gemm pairs x and w along reversed k": ("linear", _linear_k_reversed),
     "gemm drops the last k": ("linear", _linear_drops_last_k),
     "gemm widens x with the wrong shift": ("linear", _linear_wrong_widening),
+    "abs sum takes |sum| instead of sum of |x w|": ("abs_sum", _abs_sum_signed),
 }
 
 
