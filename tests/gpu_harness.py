@@ -4,6 +4,7 @@ import numpy as np
 import torch
 
 import oracle.paged_attention as opa
+import parity_bound as pb
 from helpers import to_store
 from invariant_paged_kv_gb300 import pa, workload as wl
 
@@ -57,8 +58,9 @@ SCALES = dict(k_scale=wl.FP8_K_SCALE, v_scale=wl.FP8_V_SCALE)
 
 
 def oracle_attention(step: wl.Step, t_cpu: dict, layer=0, write=True, rows=None, scale=None,
-                     caches=None):
-    """Oracle output (float64) plus the caches after the write, from CPU copies."""
+                     caches=None, terms=False):
+    """Oracle output (float64) plus the caches after the write, from CPU copies
+    (and, with ``terms``, the rows' bound terms as a fourth item)."""
     g = step.geom
     kc = caches[0] if caches is not None else to_store(t_cpu["k_cache"][layer])
     vc = caches[1] if caches is not None else to_store(t_cpu["v_cache"][layer])
@@ -69,7 +71,7 @@ def oracle_attention(step: wl.Step, t_cpu: dict, layer=0, write=True, rows=None,
     return opa.attention(to_store(t_cpu["q"][layer]), kc, vc, step.block_tables,
                          step.cu_seqlens_q, step.ctx_lens,
                          opa.default_scale(g.D) if scale is None else scale, g.dtype,
-                         g.block_size, rows=rows, **SCALES, **kw)
+                         g.block_size, rows=rows, terms=terms, **SCALES, **kw)
 
 
 def to_cpu(t: dict) -> dict:
@@ -86,6 +88,33 @@ def max_abs(gpu_out: torch.Tensor, ref: np.ndarray, rows=None) -> float:
 
 
 TOL = {"f32": 1e-5, "bf16": 2e-2, "fp8": 2e-2}
+
+# (test, stats) of every parity comparison in this session, printed at the end
+PARITY_LOG = []
+
+
+def check_parity(gpu_out, ref: np.ndarray, terms: dict, positions, geom: wl.Geometry,
+                 label: str, scale=None) -> dict:
+    """Compare GPU rows with the oracle's: the acceptance bar (max-abs TOL) and
+    the derived per-element rounding bound of parity_bound (every element
+    within its bound, no per-row slope). ref / terms / positions are the
+    same rows as gpu_out, in order."""
+    got = gpu_out.detach().cpu().to(torch.float64).numpy() if torch.is_tensor(gpu_out) \
+        else np.asarray(gpu_out, dtype=np.float64)
+    assert not np.isnan(got).any(), "GPU output has NaN"
+    assert not np.isnan(ref).any(), "oracle output has NaN on compared rows"
+    sc = opa.default_scale(geom.D) if scale is None else scale
+    st = pb.compare(got, ref, terms, positions, geom.D, sc, geom.dtype)
+    st["rows"] = int(ref.shape[0])
+    PARITY_LOG.append((label, geom.dtype, st))
+    assert st["max_abs"] <= TOL[geom.dtype], (label, st)
+    assert st["ratio"] <= 1.0, f"{label}: an element exceeds its rounding bound: {st}"
+    assert st["slope_ratio"] <= 1.0, f"{label}: a row's errors have a slope: {st}"
+    return st
+
+
+def rows_of(terms: dict, idx) -> dict:
+    return {k: v[idx] for k, v in terms.items()}
 
 
 def compact_lanes(step: wl.Step, t: dict, lanes, layer=0):

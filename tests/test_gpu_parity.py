@@ -4,8 +4,8 @@ import pytest
 import torch
 
 import oracle.paged_attention as opa
-from gpu_harness import (TOL, compact_lanes, device_step, max_abs, oracle_attention,
-                         run_attention, to_cpu, workspace_for)
+from gpu_harness import (TOL, check_parity, compact_lanes, device_step, max_abs,
+                         oracle_attention, rows_of, run_attention, to_cpu, workspace_for)
 from helpers import to_store
 from invariant_paged_kv_gb300 import build, pa, workload as wl
 
@@ -96,29 +96,34 @@ def test_write_kv_flags_out_of_range_slot():
 # attention
 # ---------------------------------------------------------------------------
 
-def _check_step(step, seed, rows=None, poison=True, layers=1, mode="batch"):
+def _check_step(step, seed, rows=None, poison=True, layers=1, mode="batch", label=None):
     """Run the step through the C ABI (invariance ``mode``) and compare with the oracle.
 
     The oracle sees a compact copy of the lanes that own the checked rows
     (all rows when ``rows`` is None): their blocks, before the step's write.
+    Every checked element must meet the fixed bar and its derived rounding
+    bound (gpu_harness.check_parity).
     """
     t = wl.make_tensors(step, seed, "cuda", layers=layers, poison=poison)
     lane_of = step.row_lane()
     lanes = range(step.B) if rows is None else sorted(set(int(lane_of[r]) for r in rows))
+    label = label or f"{step.geom} {mode} seed {seed}"
     worst = 0.0
     for layer in range(layers):
         sub, sub_t, sub_rows, blk = compact_lanes(step, t, lanes, layer)
         out, flags = run_attention(step, t, layer=layer, mode=mode)
         assert flags == 0, flags
-        ref, kc, vc = oracle_attention(sub, sub_t)
+        want = rows if rows is not None else list(range(step.T))
+        pos = {int(r): i for i, r in enumerate(sub_rows)}
+        idx = [pos[int(r)] for r in want]
+        ref, kc, vc, terms = oracle_attention(sub, sub_t, rows=idx, terms=True)
         # the write inside the call is bit-exact on every block the lanes use
         assert np.array_equal(_bytes(t["k_cache"][layer].index_select(0, blk)), kc.view(np.uint8))
         assert np.array_equal(_bytes(t["v_cache"][layer].index_select(0, blk)), vc.view(np.uint8))
-        want = rows if rows is not None else list(range(step.T))
-        pos = {int(r): i for i, r in enumerate(sub_rows)}
         got = out[torch.tensor(want, dtype=torch.long, device=out.device)]
-        worst = max(worst, max_abs(got, ref[[pos[int(r)] for r in want]]))
-    assert worst <= TOL[step.geom.dtype], worst
+        st = check_parity(got, ref[idx], rows_of(terms, idx), sub.row_positions()[idx],
+                          step.geom, f"{label} layer {layer}")
+        worst = max(worst, st["max_abs"])
     return worst
 
 
@@ -189,13 +194,23 @@ def test_prefill_chunks_e4m3(D, bs):
     _check_step(_ragged(geom, q, ctx, 23), 213)
 
 
+def _long_tail_rows(step, n_short=10):
+    """Every long row (16k-40k keys) of the long-tail step and a seeded
+    sample of the short ones."""
+    longs = [int(x) for x in np.nonzero(step.ctx_lens >= 16384)[0]]
+    shorts = np.nonzero(step.ctx_lens < 16384)[0]
+    rng = np.random.default_rng(55)
+    return sorted(longs + [int(x) for x in rng.choice(shorts, n_short, replace=False)])
+
+
 def test_long_tail_e4m3_sampled():
-    """Long-context heavy tail over e4m3 caches (one layer), sampled rows."""
+    """Long-context heavy tail over e4m3 caches (one layer): every long row
+    and a sample of short ones, unreferenced cache bytes poisoned."""
     free, _ = torch.cuda.mem_get_info()
-    step = wl.long_tail(0, pool_bytes_per_layer=min(15e9, 0.4 * free), dtype="fp8")
-    order = np.argsort(step.ctx_lens)
-    rows = [int(x) for x in order[:3]] + [int(x) for x in order[-3:]] + [100, 200]
-    _check_step(step, 5100, rows=rows, poison=False)
+    step = wl.long_tail(0, pool_bytes_per_layer=min(15e9, 0.3 * free), dtype="fp8")
+    rows = _long_tail_rows(step)
+    assert sum(step.ctx_lens[r] >= 16384 for r in rows) == 26
+    _check_step(step, 5100, rows=rows, poison=True, label="long_tail e4m3 (26 long + 10 short)")
 
 
 def test_mixed_small_full():
@@ -220,13 +235,14 @@ def test_mixed_step_sampled(mode):
 
 
 def test_long_tail_sampled():
-    """Long-context heavy tail at full size (one layer of the 4), sampled rows."""
+    """Long-context heavy tail at full size (one layer of the 4): every long
+    row and a sample of short ones, unreferenced cache bytes poisoned."""
     free, _ = torch.cuda.mem_get_info()
-    pool = min(15e9, 0.4 * free)
+    pool = min(15e9, 0.3 * free)
     step = wl.long_tail(0, pool_bytes_per_layer=pool)
-    order = np.argsort(step.ctx_lens)
-    rows = [int(x) for x in order[:3]] + [int(x) for x in order[-3:]] + [100, 200]
-    _check_step(step, 5000, rows=rows, poison=False)
+    rows = _long_tail_rows(step)
+    assert sum(step.ctx_lens[r] >= 16384 for r in rows) == 26
+    _check_step(step, 5000, rows=rows, poison=True, label="long_tail bf16 (26 long + 10 short)")
 
 
 def test_empty_step_is_noop():
@@ -254,8 +270,9 @@ def test_device_flags_bad_lane_and_block():
     assert flags & pa.FLAGS["CTX_RANGE"]
     assert flags & pa.FLAGS["BLOCK_RANGE"]
     # the untouched lane is still right
-    ref, _, _ = oracle_attention(step, to_cpu(t), write=False, rows=[2])
-    assert max_abs(out, ref, [2]) <= TOL["bf16"]
+    ref, _, _, terms = oracle_attention(step, to_cpu(t), write=False, rows=[2], terms=True)
+    check_parity(out[2:3], ref[2:3], rows_of(terms, [2]), step.row_positions()[[2]], geom,
+                 "flagged step, untouched lane")
 
 
 def test_workspace_too_small_is_flagged():

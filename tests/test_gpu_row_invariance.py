@@ -16,7 +16,7 @@ import pytest
 import torch
 
 import oracle.paged_attention as opa
-from gpu_harness import SCALES, max_abs, run_attention
+from gpu_harness import SCALES, check_parity, run_attention
 from helpers import to_store
 from invariant_paged_kv_gb300 import build, pa, workload as wl
 
@@ -137,10 +137,10 @@ def test_row_bits_independent_of_chunking(geom):
     bt = blocks[None, :].astype(np.int32)
     for p in rows:
         q1 = to_store(seq["q"][p:p + 1].cpu())
-        o, _, _ = opa.attention(q1, kc, vc, bt, np.array([0, 1], np.int32),
-                                np.array([p + 1], np.int32), opa.default_scale(geom.D),
-                                geom.dtype, geom.block_size, **SCALES)
-        assert max_abs(ref[p:p + 1], o) <= (1e-5 if geom.dtype == "f32" else 2e-2), p
+        o, _, _, terms = opa.attention(q1, kc, vc, bt, np.array([0, 1], np.int32),
+                                       np.array([p + 1], np.int32), opa.default_scale(geom.D),
+                                       geom.dtype, geom.block_size, terms=True, **SCALES)
+        check_parity(ref[p:p + 1], o, terms, [p], geom, f"row mode {geom} position {p}")
 
 
 def test_row_bits_across_split_length_change():
