@@ -8,11 +8,17 @@
 // device-wide synchronisation cudaMalloc / cudaFree may imply. Such a caller
 // still passes its inputs and outputs; only the scratch is built in.
 //
-// The array below is a file-scope __device__ object: every GPU that loads
-// the library holds PA_STATIC_SCRATCH_BYTES of it until the process exits. In
-// host code its name is only a host-side stand-in, never a device address, so
-// the host looks the address up with cudaGetSymbolAddress, once per device,
-// with that device current, and passes the looked-up pointer on.
+// The array below is a file-scope __device__ object. It lives in this
+// file's own device module, which CUDA loads on a device when the module is
+// first used there (lazy module loading is the default): here, at the
+// cudaGetSymbolAddress of the first call on that device. That is when the
+// device memory for the array is taken; the device then holds
+// PA_STATIC_SCRATCH_BYTES of it until the process exits. In host code the
+// array's name is only a host-side stand-in, never a device address, so the
+// host looks the address up with cudaGetSymbolAddress, once per device, with
+// that device current, and passes the looked-up pointer on. The address
+// belongs to the device's context of that moment: after a cudaDeviceReset
+// the entry point must not be called again in the same process.
 #include <mutex>
 
 #include "pa_common.cuh"
@@ -50,7 +56,10 @@ extern "C" pa_status pa_attention_static_scratch(
     int32_t T, int32_t H, int32_t Hkv, int32_t D, int32_t block_size, int32_t num_blocks,
     int32_t max_q_len, int32_t max_ctx_len, int64_t total_ctx, float scale, pa_dtype dtype,
     int32_t* status, void* stream) {
-  // Size check first, on the host, before any CUDA call.
+  // Argument and size checks first, on the host, before any CUDA call:
+  // negative sizes are the caller's error, as in pa_attention.
+  if (B < 0 || T < 0 || max_q_len < 0 || max_ctx_len < 0 || num_blocks <= 0)
+    return PA_ERR_INVALID_ARG;
   const size_t need = pa_attention_workspace_bytes(B, T, max_q_len, max_ctx_len, total_ctx, H,
                                                    Hkv, D, block_size, dtype);
   if (need == 0) return PA_ERR_UNSUPPORTED;

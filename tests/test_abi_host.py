@@ -17,8 +17,8 @@ def lib():
     return pa.load()
 
 
-def declared_functions():
-    src = open(os.path.join(ROOT, "include", "pa.h")).read()
+def declared_functions(header="pa.h"):
+    src = open(os.path.join(ROOT, "include", header)).read()
     src = re.sub(r"/\*.*?\*/", "", src, flags=re.S)
     return sorted(set(re.findall(r"\b(pa_\w+)\s*\(", src)))
 
@@ -35,6 +35,10 @@ def test_every_declared_symbol_is_exported(lib):
         assert hasattr(lib, name), name
     # the binding wraps exactly the declared boundary
     assert set(declared_functions()) == set(pa.EXPORTS)
+    # and the test hooks of the separate header
+    for name in declared_functions("pa_test.h"):
+        assert hasattr(lib, name), name
+    assert set(declared_functions("pa_test.h")) == set(pa.TEST_EXPORTS)
 
 
 def test_status_strings(lib):
@@ -209,3 +213,21 @@ def test_decode_gemm_refusals_before_cuda(lib):
     assert lib.pa_decode_gemm_splits(248320, 5120) == 1
     assert lib.pa_decode_gemm_workspace_bytes(64, 248320, 5120) == 0
     assert lib.pa_decode_gemm_workspace_bytes(64, 1024, 5120) >= 20 * 64 * 1024 * 4
+
+
+def test_static_scratch_refusals_before_cuda(lib):
+    """Negative sizes are refused as pa_attention refuses them (invalid
+    argument), a step beyond the built-in array as a workspace error, and
+    unsupported geometry as unsupported -- all before any CUDA call."""
+    f = lib.pa_attention_static_scratch
+
+    def call(B=4, T=4, H=8, Hkv=2, D=128, bs=16, NB=64, mq=1, mc=40, tot=69):
+        return f(None, None, None, None, 3, None, None, None, None, None, None, B, T, H, Hkv,
+                 D, bs, NB, mq, mc, tot, 0.088, 1, None, None)
+    assert call(B=-1) == 1
+    assert call(T=-1) == 1
+    assert call(mq=-1) == 1
+    assert call(mc=-1) == 1
+    assert call(NB=0) == 1
+    assert call(D=96) == 2
+    assert call(B=256, T=256, H=64, Hkv=8, mc=40960, tot=10 ** 7) == 3
