@@ -148,6 +148,12 @@ pa_status pa_write_kv_scaled(const void* k_new, const void* v_new, void* k_cache
 
 /*
  * pa_attention_workspace_bytes -- device scratch pa_attention needs.
+ * ("P3: native paged-KV continuous-batching sampler", Design, paged.py: the
+ *  paged-attention kernel contract's fixed KV split per context length --
+ *  the split partials of that split are what this scratch holds -- and
+ *  PagedKVCache.ensure_capacity, all-or-nothing: the caller sizes and owns
+ *  the memory before the step runs, so a step never fails half-done for
+ *  want of it.)
  *
  * The split-KV path stores fp32 partial results (m, l, acc[D]) per
  * (query row, split, head). The bound uses host-known scalars: B lanes, T
@@ -368,22 +374,31 @@ pa_status pa_decode_gemm(const void* x, const void* w, void* y, int32_t T_pad, i
  * that cannot take the device-wide synchronisation cudaMalloc / cudaFree may
  * cause. This entry point takes the same inputs and outputs as pa_attention
  * but no workspace: its split-KV scratch is one array of
- * PA_STATIC_SCRATCH_BYTES compiled into the library, which every GPU that
- * loads the library holds until the process exits. It calls no cudaMalloc,
- * cudaFree or other allocating routine.
+ * PA_STATIC_SCRATCH_BYTES compiled into the library. It calls no cudaMalloc,
+ * cudaFree or other allocating routine (see Set-up for when the array's own
+ * memory is taken).
  *
  *   total_ctx  sum of ctx_lens over the lanes (negative if unknown), used
  *              with B, T, max_q_len and max_ctx_len to bound the scratch the
  *              step needs, exactly as pa_attention_workspace_bytes does.
- * Returns PA_ERR_WORKSPACE, before any CUDA call, when that bound exceeds
- * PA_STATIC_SCRATCH_BYTES; PA_ERR_UNSUPPORTED for unsupported geometry.
- * Set-up: the first call on each device looks up the array's device address
- * (cudaGetSymbolAddress, with that device current) and keeps it; make that
- * first call before any stream capture. Every call on a device shares the
- * one array and it keeps the last call's contents (nothing in it needs to
- * start at zero); calls whose work overlaps on the GPU -- on different
- * streams, or from different threads -- race on it and must be serialised by
- * the caller.
+ * Returns PA_ERR_INVALID_ARG for negative sizes (as pa_attention does) and
+ * PA_ERR_WORKSPACE when that bound exceeds PA_STATIC_SCRATCH_BYTES, both
+ * before any CUDA call; PA_ERR_UNSUPPORTED for unsupported geometry.
+ * Set-up: the first call on each device, with that device current, looks up
+ * the array's device address (cudaGetSymbolAddress) and keeps it. That
+ * lookup is also when CUDA loads the library part holding the array and
+ * takes its PA_STATIC_SCRATCH_BYTES of device memory (lazy module loading,
+ * CUDA's default): a caller whose memory pool will claim all free device
+ * memory, or that captures streams into graphs, makes one set-up call first
+ * -- a call with B = T = 0 (any supported geometry, num_blocks >= 1, a
+ * positive scale) does only the set-up and returns PA_OK. From then on the device holds the array until the process exits,
+ * and calls allocate nothing. The kept address belongs to the device's
+ * context at set-up: do not call again after a cudaDeviceReset of that
+ * device. Every call on a device shares the one array and it keeps the last
+ * call's contents (nothing in it needs to start at zero: each call rewrites
+ * the plan and partials it reads); calls whose work overlaps on the GPU --
+ * on different streams, or from different threads -- race on it and must be
+ * serialised by the caller.
  */
 #define PA_STATIC_SCRATCH_BYTES (32u * 1024u * 1024u)
 
@@ -400,10 +415,21 @@ pa_status pa_attention_static_scratch(const void* q, const void* k_cache, const 
 /*
  * pa_read_status -- wait for `stream`, copy the device status word to
  * *flags_out and, if clear != 0, reset it to zero. The only synchronising call.
+ * ("P3: native paged-KV continuous-batching sampler", Review (adversarial
+ *  pass): an out-of-vocabulary prompt id became a device-side assert that
+ *  wedged the engine, and greedy NaN logits passed silently; both now fail
+ *  loudly before any sequence advances. Read here as: a bad index seen only
+ *  on the device never traps a kernel -- it sets a PA_FLAG_* bit that the
+ *  caller reads here, after the step, and acts on.)
  */
 pa_status pa_read_status(int32_t* status, void* stream, int32_t* flags_out, int32_t clear);
 
-/* Human-readable name of a pa_status value (static storage). */
+/* Human-readable name of a pa_status value (static storage).
+ * (Host-visible refusals are returned at entry, before any launch: "P3:
+ *  native paged-KV continuous-batching sampler", Review (adversarial pass),
+ *  bad requests refused at add_request instead of wedging the engine;
+ *  "Numerics envelopes", Precedence: refuse a choice that would void the
+ *  contract rather than keep it silently.) */
 const char* pa_status_string(pa_status s);
 
 /* Kernels this process has launched through the library so far. */
