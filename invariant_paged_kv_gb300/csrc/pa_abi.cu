@@ -8,6 +8,7 @@
 #include <mutex>
 
 #include "pa_common.cuh"
+#include "pa_test.h"
 
 namespace pa {
 
@@ -30,6 +31,16 @@ cudaError_t launch_decode_gemm(void* y, float* part, int T_pad, int N, int K, in
                                cudaStream_t s);
 
 static std::atomic<long long> g_launches{0};
+
+// Test hooks (include/pa_test.h): the wait limit every step's kernels get,
+// and the split item whose first copy is never issued (-1: none).
+static std::atomic<long long> g_wait_cycles{kWaitCycles};
+static std::atomic<long long> g_skip_item{-1};
+
+void apply_test_hooks(StepParams& p) {
+  p.wait_cycles = g_wait_cycles.load(std::memory_order_relaxed);
+  p.skip_item = g_skip_item.load(std::memory_order_relaxed);
+}
 
 void count_launches(int n) { g_launches.fetch_add(n, std::memory_order_relaxed); }
 
@@ -340,6 +351,7 @@ pa_status pa_write_kv_scaled(const void* k_new, const void* v_new, void* k_cache
     return PA_ERR_INVALID_ARG;
   StepParams p;
   std::memset(&p, 0, sizeof(p));
+  apply_test_hooks(p);
   p.k_cache = k_cache;
   p.v_cache = v_cache;
   p.k_new = k_new;
@@ -423,6 +435,7 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
 
   StepParams p;
   std::memset(&p, 0, sizeof(p));
+  apply_test_hooks(p);
   p.q = q;
   p.out = out;
   p.k_cache = k_cache;
@@ -557,6 +570,7 @@ pa_status pa_attention_partials(const void* q, const void* k_cache, const void* 
 
   StepParams p;
   std::memset(&p, 0, sizeof(p));
+  apply_test_hooks(p);
   p.q = q;
   p.k_cache = k_cache;
   p.v_cache = v_cache;
@@ -636,6 +650,7 @@ pa_status pa_merge_partials(const void* partials, size_t partials_bytes, int32_t
 
   StepParams p;
   std::memset(&p, 0, sizeof(p));
+  apply_test_hooks(p);
   p.out = out;
   p.cu_seqlens = cu_seqlens_q;
   p.ctx_lens = ctx_lens;
@@ -713,3 +728,12 @@ pa_status pa_read_status(int32_t* status, void* stream, int32_t* flags_out, int3
 }
 
 }  // extern "C"
+
+extern "C" void pa_test_set_wait_cycles(int64_t cycles) {
+  pa::g_wait_cycles.store(cycles > 0 ? (long long)cycles : pa::kWaitCycles,
+                          std::memory_order_relaxed);
+}
+
+extern "C" void pa_test_skip_split_item(int64_t item) {
+  pa::g_skip_item.store(item >= 0 ? (long long)item : -1LL, std::memory_order_relaxed);
+}

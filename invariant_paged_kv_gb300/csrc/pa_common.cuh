@@ -27,7 +27,8 @@ __host__ __device__ __forceinline__ int split_len(int keys) {
 }
 // Keys per pipeline stage of the split kernels (one mma M tile).
 constexpr int kChunk = 16;
-// Bounded waits give up after this many SM clock cycles (about 1 s).
+// Bounded waits give up after this many SM clock cycles (about 1 s) unless
+// a step carries another limit (StepParams::wait_cycles).
 constexpr long long kWaitCycles = 2000000000LL;
 
 // ---------------------------------------------------------------------------
@@ -130,6 +131,14 @@ struct StepParams {
   int group_rows;
   int sm_count;  // SMs of the device (the mixed-step kernel's grid)
   int partials_mode;
+  // every bounded wait of the step's kernels gives up after this many SM
+  // clock cycles (kWaitCycles unless a test shortened it)
+  long long wait_cycles;
+  // test hook, -1 normally: the split kernel's producer issues no copy for
+  // the first chunk of this item, so the consumer's bounded wait on it runs
+  // out (PA_FLAG_TIMEOUT) -- how the tests make a wait expire without any
+  // fault
+  long long skip_item;
   const int* key_lo;
   const int* key_hi;
   const int* key_bounds;        // [owners + 1][B]
@@ -227,13 +236,14 @@ __device__ __forceinline__ bool mbar_try_wait(uint32_t bar, uint32_t parity) {
   return ok != 0;
 }
 
-// Wait for the phase with the given parity to complete, for at most
-// kWaitCycles SM cycles. Returns false on timeout.
-__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity) {
+// Wait for the phase with the given parity to complete, for at most `limit`
+// SM cycles. Returns false on timeout.
+__device__ __forceinline__ bool mbar_wait_bounded(uint32_t bar, uint32_t parity,
+                                                  long long limit) {
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
-    if (clock64() - t0 > kWaitCycles) return false;
+    if (clock64() - t0 > limit) return false;
   }
   return true;
 }

@@ -102,7 +102,9 @@ __device__ __forceinline__ void decode_bf16_warps(const StepParams& p, const CUt
       p_blk = load_blocks(p, pi, p_w0, lane);
     }
     int blk = __shfl_sync(0xffffffffu, p_blk, off / p.bs - p_w0);
-    if (lane == 0) {
+    // (test hook: no copy for the first chunk of item skip_item, so its
+    // consumer's bounded wait runs out; -1 on every ordinary step)
+    if (lane == 0 && !(p_chunk == 0 && p_item == p.skip_item)) {
       if (blk < 0 || blk >= p.NB) {
         raise_flag(p.status, PA_FLAG_BLOCK_RANGE);
         blk = 0;
@@ -150,12 +152,12 @@ __device__ __forceinline__ void decode_bf16_warps(const StepParams& p, const CUt
       const uint32_t parity = (consumed / kStages) & 1u;
       // every lane waits (so every lane sees the landed bytes); the verdict is
       // made warp-uniform before anyone acts on it
-      const bool landed = __all_sync(0xffffffffu, mbar_wait_bounded(bar[stage], parity));
+      const bool landed = __all_sync(0xffffffffu, mbar_wait_bounded(bar[stage], parity, p.wait_cycles));
       if (!landed) {
         if (lane == 0) raise_flag(p.status, PA_FLAG_TIMEOUT);
         // let copies already in flight land before the warp leaves
         for (uint32_t c = consumed + 1; c < issued; ++c)
-          mbar_wait_bounded(bar[c % kStages], (c / kStages) & 1u);
+          mbar_wait_bounded(bar[c % kStages], (c / kStages) & 1u, p.wait_cycles);
         return;
       }
       const uint32_t ks = wbase + stage * TL::kStageBytes;

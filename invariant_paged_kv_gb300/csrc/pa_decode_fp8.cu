@@ -204,11 +204,11 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
     for (int ch = 0; ch < nchunks_of(it); ++ch) {
       const int stage = consumed % kStages;
       const uint32_t parity = (consumed / kStages) & 1u;
-      const bool landed = __all_sync(0xffffffffu, mbar_wait_bounded(bar[stage], parity));
+      const bool landed = __all_sync(0xffffffffu, mbar_wait_bounded(bar[stage], parity, p.wait_cycles));
       if (!landed) {
         if (lane == 0) raise_flag(p.status, PA_FLAG_TIMEOUT);
         for (uint32_t c = consumed + 1; c < issued; ++c)
-          mbar_wait_bounded(bar[c % kStages], (c / kStages) & 1u);
+          mbar_wait_bounded(bar[c % kStages], (c / kStages) & 1u, p.wait_cycles);
         return;
       }
       const uint32_t ks = wbase + stage * TL::kStageBytes;

@@ -101,13 +101,14 @@ __device__ __forceinline__ ItemInfo item_info(const StepParams& p, int item, int
 
 // Wait with the CTA-wide abort flag: returns false (and sets the flag) on timeout.
 __device__ __forceinline__ bool wait_or_abort_1(uint32_t bar, uint32_t parity,
-                                                volatile int* abort_flag, int* status) {
+                                                volatile int* abort_flag, int* status,
+                                                long long limit) {
   if (*abort_flag) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       raise_flag(status, PA_FLAG_TIMEOUT);
       return false;
@@ -118,8 +119,9 @@ __device__ __forceinline__ bool wait_or_abort_1(uint32_t bar, uint32_t parity,
 
 // Every lane of the warp waits; the verdict is made warp-uniform.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
-                                              volatile int* abort_flag, int* status) {
-  return __all_sync(0xffffffffu, wait_or_abort_1(bar, parity, abort_flag, status));
+                                              volatile int* abort_flag, int* status,
+                                              long long limit) {
+  return __all_sync(0xffffffffu, wait_or_abort_1(bar, parity, abort_flag, status, limit));
 }
 
 // The work of one CTA of kThreads threads (see the roles above); dsmem
@@ -227,7 +229,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         const uint32_t bytes = (uint32_t)nchunk * L::kHalves * kChunk * 128;
         // lane c (< nchunk) copies chunk c: the boxes go out in parallel
         const int tok = blk * p.bs + (key0 + lane * kChunk) % p.bs;
-        if (use >= 1 && !wait_or_abort(bke[st], (use - 1) & 1, &s_abort, p.status)) break;
+        if (use >= 1 && !wait_or_abort(bke[st], (use - 1) & 1, &s_abort, p.status, p.wait_cycles)) break;
         if (lane == 0) mbar_expect_tx(bkf[st], bytes);
         __syncwarp();
         if (lane < nchunk) {
@@ -236,7 +238,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
             tma_load_3d(sK0 + st * L::kKBytes + h * L::kKHalfBytes + lane * kChunk * 128, tmK,
                         h * 64, it.kvh, tok, bkf[st]);
         }
-        if (use >= 1 && !wait_or_abort(bve[st], (use - 1) & 1, &s_abort, p.status)) break;
+        if (use >= 1 && !wait_or_abort(bve[st], (use - 1) & 1, &s_abort, p.status, p.wait_cycles)) break;
         if (lane == 0) mbar_expect_tx(bvf[st], bytes);
         __syncwarp();
         if (lane < nchunk) {
@@ -270,8 +272,8 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
       // first S of the item, once Q is in TMEM and K tile 0 has landed
       {
         const uint32_t f = n_kv, st = f % kStages;
-        ok = wait_or_abort(bkf[st], (f / kStages) & 1, &s_abort, p.status) &&
-             wait_or_abort(bq, n_item & 1, &s_abort, p.status);
+        ok = wait_or_abort(bkf[st], (f / kStages) & 1, &s_abort, p.status, p.wait_cycles) &&
+             wait_or_abort(bq, n_item & 1, &s_abort, p.status, p.wait_cycles);
         for (int hb = 0; ok && hb < nh; ++hb) {
           tc_fence_after();
           issue_s(hb, 0);
@@ -283,7 +285,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         const uint32_t f = n_kv + kt, st = f % kStages;
         const bool next = kt + 1 < it.nkt;
         const uint32_t f1 = f + 1, st1 = f1 % kStages;
-        if (!wait_or_abort(bvf[st], (f / kStages) & 1, &s_abort, p.status)) break;
+        if (!wait_or_abort(bvf[st], (f / kStages) & 1, &s_abort, p.status, p.wait_cycles)) break;
         const int key0 = kt * kKeys;
         if (key0 + kKeys > it.ctx) {
           // keys past the lane's end: zero their V rows (stale bytes must not
@@ -302,7 +304,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         for (int hb = 0; hb < nh; ++hb) {
           const uint32_t th = n_t[hb] + kt;
           // P V of tile kt, once this head's softmax has written P
-          if (!wait_or_abort(bP(hb), th & 1, &s_abort, p.status)) { ok = false; break; }
+          if (!wait_or_abort(bP(hb), th & 1, &s_abort, p.status, p.wait_cycles)) { ok = false; break; }
           tc_fence_after();
           if (lane == 0) {
 #pragma unroll
@@ -317,11 +319,11 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
           if (next) {
             // S of tile kt + 1 needs its K tile, and it overwrites P of tile
             // kt: wait for that P V
-            if (hb == 0 && !wait_or_abort(bkf[st1], (f1 / kStages) & 1, &s_abort, p.status)) {
+            if (hb == 0 && !wait_or_abort(bkf[st1], (f1 / kStages) & 1, &s_abort, p.status, p.wait_cycles)) {
               ok = false;
               break;
             }
-            if (!wait_or_abort(bO(hb, th), (th >> 1) & 1, &s_abort, p.status)) { ok = false; break; }
+            if (!wait_or_abort(bO(hb, th), (th >> 1) & 1, &s_abort, p.status, p.wait_cycles)) { ok = false; break; }
             tc_fence_after();
             issue_s(hb, kt + 1);
           }
@@ -346,7 +348,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
 #pragma unroll 1
       for (int kt = 0; kt < it.nkt; ++kt) {
         const uint32_t th = n_t[hb] + kt;
-        if (!wait_or_abort(bS(hb), th & 1, &s_abort, p.status)) { ok = false; break; }
+        if (!wait_or_abort(bS(hb), th & 1, &s_abort, p.status, p.wait_cycles)) { ok = false; break; }
         tc_fence_after();
         uint32_t sv[kKeys];
 #pragma unroll
@@ -424,7 +426,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         // than one phase away from any wait on it even when tiles without a
         // rescale skip the wait.
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!wait_or_abort(bO(hb, th - 1), ((th - 1) >> 1) & 1, &s_abort, p.status)) {
+          if (!wait_or_abort(bO(hb, th - 1), ((th - 1) >> 1) & 1, &s_abort, p.status, p.wait_cycles)) {
             ok = false;
             break;
           }
@@ -444,7 +446,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         mbar_arrive(bP(hb));
       }
       const uint32_t last = n_t[hb] + it.nkt - 1;
-      if (ok && wait_or_abort(bO(hb, last), (last >> 1) & 1, &s_abort, p.status)) {
+      if (ok && wait_or_abort(bO(hb, last), (last >> 1) & 1, &s_abort, p.status, p.wait_cycles)) {
         tc_fence_after();
         const bool valid = r < it.nrows;
         const float inv_l = 1.f / l;  // one division per row; out = O * (1 / l)

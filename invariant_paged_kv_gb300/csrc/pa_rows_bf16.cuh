@@ -67,13 +67,13 @@ __device__ __forceinline__ Group group_at(const StepParams& p, int k) {
 }
 
 __device__ __forceinline__ bool wait_r(uint32_t bar, uint32_t parity, volatile int* abort_flag,
-                                       int* status) {
+                                       int* status, long long limit) {
   if (*abort_flag) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
   while (!mbar_try_wait(bar, parity)) {
     if (*abort_flag) return false;
-    if (clock64() - t0 > kWaitCycles) {
+    if (clock64() - t0 > limit) {
       *abort_flag = 1;
       raise_flag(status, PA_FLAG_TIMEOUT);
       return false;
@@ -224,7 +224,7 @@ __device__ __forceinline__ void rows_bf16_cta(const StepParams& p, const CUtenso
         for (int ch = 0; ch < nch; ++ch, ++f) {
           const uint32_t st = f % kRStages;
           if (f >= kRStages &&
-              !wait_r(smem_u32(&empty[st]), ((f / kRStages) - 1) & 1, &s_abort, p.status)) {
+              !wait_r(smem_u32(&empty[st]), ((f / kRStages) - 1) & 1, &s_abort, p.status, p.wait_cycles)) {
             ok = false;
             break;
           }
@@ -258,7 +258,7 @@ __device__ __forceinline__ void rows_bf16_cta(const StepParams& p, const CUtenso
     for (long long k = 0;; ++k) {
       // the stage of the item's first chunk (or of the stop token)
       if (!__all_sync(0xffffffffu, wait_r(smem_u32(&full[f % kRStages]), (f / kRStages) & 1,
-                                          &s_abort, p.status)))
+                                          &s_abort, p.status, p.wait_cycles)))
         break;
       const long long item = s_q[k % kQueue];
       if (item >= n_items) break;
@@ -288,7 +288,7 @@ __device__ __forceinline__ void rows_bf16_cta(const StepParams& p, const CUtenso
       for (int ch = 0; ch < nch; ++ch, ++f) {
         const uint32_t st = f % kRStages;
         if (ch > 0 && !__all_sync(0xffffffffu, wait_r(smem_u32(&full[st]), (f / kRStages) & 1,
-                                                      &s_abort, p.status))) {
+                                                      &s_abort, p.status, p.wait_cycles))) {
           ok = false;
           break;
         }
@@ -309,7 +309,7 @@ __device__ __forceinline__ void rows_bf16_cta(const StepParams& p, const CUtenso
             __syncwarp();
             if (lane == 0) mbar_arrive(smem_u32(&zeroed[st]));
           } else if (!__all_sync(0xffffffffu, wait_r(smem_u32(&zeroed[st]), (zbits >> st) & 1,
-                                                     &s_abort, p.status))) {
+                                                     &s_abort, p.status, p.wait_cycles))) {
             ok = false;
             break;
           }
@@ -408,7 +408,7 @@ __device__ __forceinline__ void rows_bf16_cta(const StepParams& p, const CUtenso
     for (uint32_t j = f > kRStages ? f - kRStages : 0; j < f; ++j) {
       const long long t0 = clock64();
       while (!mbar_try_wait(smem_u32(&full[j % kRStages]), (j / kRStages) & 1))
-        if (clock64() - t0 > kWaitCycles) break;
+        if (clock64() - t0 > p.wait_cycles) break;
     }
   }
 }

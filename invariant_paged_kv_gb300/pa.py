@@ -34,6 +34,8 @@ EXPORTS = ("pa_write_kv", "pa_write_kv_scaled", "pa_attention_workspace_bytes",
            "pa_partials_bytes", "pa_partials_workspace_bytes", "pa_attention_partials",
            "pa_merge_partials", "pa_decode_gemm_splits", "pa_decode_gemm_workspace_bytes",
            "pa_decode_gemm")
+# test hooks declared in include/pa_test.h (not part of the attention boundary)
+TEST_EXPORTS = ("pa_test_set_wait_cycles", "pa_test_skip_split_item")
 
 
 class PaError(RuntimeError):
@@ -104,6 +106,10 @@ def load() -> ctypes.CDLL:
     L.pa_decode_gemm_workspace_bytes.restype = sz
     L.pa_decode_gemm.argtypes = [vp, vp, vp, i32, i32, i32, vp, sz, vp, vp]
     L.pa_decode_gemm.restype = ctypes.c_int
+    L.pa_test_set_wait_cycles.argtypes = [i64]
+    L.pa_test_set_wait_cycles.restype = None
+    L.pa_test_skip_split_item.argtypes = [i64]
+    L.pa_test_skip_split_item.restype = None
     _lib = L
     return L
 
