@@ -225,7 +225,7 @@ class OraclePool:
 # ---------------------------------------------------------------------------
 
 class ClockSampler:
-    QUERY = ("index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
+    QUERY = ("timestamp,index,clocks.sm,clocks.max.sm,power.draw,clocks_event_reasons.active,"
              "clocks_event_reasons.hw_slowdown,clocks_event_reasons.hw_thermal_slowdown,"
              "clocks_event_reasons.sw_thermal_slowdown,clocks_event_reasons.sw_power_cap")
 
@@ -233,16 +233,21 @@ class ClockSampler:
         self.dev = device_index
         self.proc = None
         self.path = os.path.join("/tmp", f"pa_clocks_{os.getpid()}.csv")
+        self.window = None
 
     def start(self):
         try:
             self.f = open(self.path, "w")
             self.proc = subprocess.Popen(
                 ["nvidia-smi", f"--id={self.dev}", f"--query-gpu={self.QUERY}",
-                 "--format=csv,noheader,nounits", "-lms", "100"],
+                 "--format=csv,noheader,nounits", "-lms", "20"],
                 stdout=self.f, stderr=subprocess.DEVNULL)
         except (OSError, FileNotFoundError):
             self.proc = None
+
+    def mark(self, t0, t1):
+        """Host wall-clock window (time.time()) of the timed region."""
+        self.window = (t0, t1)
 
     def stop(self):
         if self.proc is None:
@@ -253,25 +258,32 @@ class ClockSampler:
         except subprocess.TimeoutExpired:
             self.proc.kill()
         self.f.close()
-        sm, mx, reasons = [], [], set()
+        import datetime
+        rows = []
         names = ["hw_slowdown", "hw_thermal_slowdown", "sw_thermal_slowdown", "sw_power_cap"]
         for line in open(self.path):
             parts = [x.strip() for x in line.split(",")]
-            if len(parts) < 9:
+            if len(parts) < 10:
                 continue
             try:
-                sm.append(float(parts[1]))
-                mx.append(float(parts[2]))
+                ts = datetime.datetime.strptime(parts[0], "%Y/%m/%d %H:%M:%S.%f").timestamp()
+                rows.append((ts, float(parts[2]), float(parts[3]),
+                             {n for n, v in zip(names, parts[6:10]) if v.lower() in ("active", "1")}))
             except ValueError:
                 continue
-            for n, v in zip(names, parts[5:9]):
-                if v.lower() in ("active", "1"):
-                    reasons.add(n)
         os.unlink(self.path)
-        if not sm:
+        if not rows:
             return None
-        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(mx),
-                "samples": len(sm), "reasons": sorted(reasons)}
+        inside = rows
+        if self.window:
+            # samples stamped inside the timed region (with one sample period of slack)
+            a, b = self.window
+            inside = [r for r in rows if a - 0.02 <= r[0] <= b + 0.02] or rows
+        sm = [r[1] for r in inside]
+        reasons = set().union(*[r[3] for r in inside])
+        return {"sm_mhz": statistics.median(sm), "sm_max_mhz": max(r[2] for r in inside),
+                "samples": len(inside), "samples_total": len(rows),
+                "reasons": sorted(reasons)}
 
 
 # ---------------------------------------------------------------------------
@@ -334,6 +346,67 @@ def committed_traffic(fp8=False):
         return float(vals["traffic_bytes_per_launch_full"]), sha
     except (KeyError, ValueError):
         return None, sha
+
+
+def _time_append(pa, k_new, v_new, kc, vc, slots, status, stream, reps=50):
+    """Mean ms of one pa_write_kv launch: reps launches captured in a CUDA
+    graph, replayed once between events (after a warm replay)."""
+    import torch
+
+    from invariant_paged_kv_gb300 import workload as wl
+    kw = dict(k_scale=wl.FP8_K_SCALE, v_scale=wl.FP8_V_SCALE)
+    pa.write_kv(k_new, v_new, kc, vc, slots, status, **kw)
+    g = torch.cuda.CUDAGraph()
+    with torch.cuda.graph(g):
+        for _ in range(reps):
+            pa.write_kv(k_new, v_new, kc, vc, slots, status, **kw)
+    g.replay()
+    torch.cuda.synchronize()
+    a, b = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
+    a.record(stream)
+    g.replay()
+    b.record(stream)
+    torch.cuda.synchronize()
+    return a.elapsed_time(b) / reps
+
+
+def measure_append(step, tens, slots, status, stream, dev):
+    """The KV append (K1) on its own: pa_write_kv of the step's new rows of
+    layer 0 into its caches (the same bytes the step's prologue writes), and of
+    65,536 rows into a 256 MiB pool where bandwidth, not launch latency,
+    decides. Algorithmic bytes: each new K and V row read once and written
+    once, plus its 8-byte slot (2 T Hkv D elem 2 + 8 T)."""
+    import torch
+
+    from invariant_paged_kv_gb300 import pa
+    g = step.geom
+    peak, kind = measured_hbm_peak()
+    elem = g.elem_bytes
+    out = {"bound": "hbm", "kernel": "prologue_kernel (write only: pa_write_kv)",
+           "peak": peak, "peak_kind": kind, "unit": "GB/s"}
+
+    def entry(T, ms):
+        nbytes = 2 * T * g.Hkv * g.D * (g.q_bytes + elem) + 8 * T
+        ach = nbytes / (ms * 1e-3) / 1e9
+        return {"rows": int(T), "algorithmic_bytes": int(nbytes), "avg_launch_ms": round(ms, 5),
+                "achieved": round(ach, 1), "frac": round(ach / peak, 4)}
+
+    ms = _time_append(pa, tens["k_new"][0], tens["v_new"][0], tens["k_cache"][0],
+                      tens["v_cache"][0], slots, status, stream)
+    out["step_rows"] = entry(step.T, ms)
+    T = 65536
+    gen = torch.Generator(device=dev).manual_seed(77)
+    kc = torch.zeros(T // g.block_size, g.block_size, g.Hkv, g.D, dtype=tens["k_cache"][0].dtype,
+                     device=dev)
+    vc = torch.zeros_like(kc)
+    kn = torch.randn(T, g.Hkv, g.D, generator=gen, device=dev).to(tens["k_new"][0].dtype)
+    vn = torch.randn(T, g.Hkv, g.D, generator=gen, device=dev).to(kn.dtype)
+    perm = torch.randperm(T, generator=gen, device=dev).to(torch.int64)
+    ms = _time_append(pa, kn, vn, kc, vc, perm, status, stream, reps=20)
+    out["large"] = entry(T, ms)
+    out["large"]["what"] = "65,536 rows scattered to a seeded permutation of a 65,536-slot pool"
+    del kc, vc, kn, vn
+    return out
 
 
 def run_ours(args, rank, world, local_rank):
@@ -415,6 +488,7 @@ def run_ours(args, rank, world, local_rank):
         time.sleep(0.3)
     if graph is None:
         launches0 = pa.kernel_launches()
+    host_t0 = time.time()
     t_start.record(stream)
     if graph is None:
         for k in range(K):
@@ -423,6 +497,9 @@ def run_ours(args, rank, world, local_rank):
         graph.replay()
     t_end.record(stream)
     barrier()
+    host_t1 = time.time()
+    if clocks:
+        clocks.mark(host_t0, host_t1)
     clk = clocks.stop() if clocks else None
     if graph is None:
         launches = pa.kernel_launches() - launches0
@@ -444,6 +521,11 @@ def run_ours(args, rank, world, local_rank):
     step_bytes = nbytes["total"] * layers
     value = weak_scaling_value(step_bytes, world, ms_max)
     rows_per_s = step.T * world / (ms_max * 1e-3)
+    # tokens/s as T / (write + attention kernel time): a step's T rows pass
+    # through every layer, each layer's time the sum of its kernels' event times
+    kernel_ms_per_layer = phase_ms["prologue"] + phase_ms["decode"] + phase_ms["combine"]
+    tokens_per_s = step.T * world / (layers * kernel_ms_per_layer * 1e-3)
+    kv_append = measure_append(step, tens, slots, status, stream, dev)
 
     # ---- end to end: per-step inputs from pinned host memory, result back ----
     # Every step copies all of its inputs (q, new K/V rows of every layer and
@@ -601,8 +683,15 @@ def run_ours(args, rank, world, local_rank):
             rate, cores, desc = pool.rate(step, seconds_budget=15)
         finally:
             pool.close()
+        pool1 = OraclePool(workers=1)
+        try:
+            rate1, _, desc1 = pool1.rate(step, seconds_budget=6, seed=4242)
+        finally:
+            pool1.close()
         cpu = {"value": round(rate, 4), "unit": "GB/s", "cores": cores, "kind": "oracle",
-               "sample": desc}
+               "sample": desc,
+               "one_core": {"value": round(rate1, 4), "unit": "GB/s", "cores": 1,
+                            "sample": desc1}}
 
     line = {
         "metric": METRIC, "value": round(value, 1), "unit": "GB/s", "n_gpus": world,
@@ -612,11 +701,15 @@ def run_ours(args, rank, world, local_rank):
         "data": "synthetic (seeded N(0,1) q/K/V; seeded heavy-tailed lengths and block tables)",
         "config": workload_config(step, layers, name, args),
         "rows_per_s": round(rows_per_s, 1),
+        "tokens_per_s": round(tokens_per_s, 1),
+        "tokens_per_s_what": "T rows / (layers x (prologue: KV append + plan, work launch, "
+                             "combine) kernel ms per layer from the phase events)",
         "frac_of_hbm_peak": round(value / peak, 4),
         "frac_of_nominal_hbm": round(value / NOMINAL_HBM_GBS, 4),
         "bytes_per_step": step_bytes,
         "phase_ms_per_layer": {k: round(v, 4) for k, v in phase_ms.items()},
-        "roofline": roofline, "prefill_roofline": prefill, "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
+        "roofline": roofline, "prefill_roofline": prefill, "kv_append": kv_append,
+        "cpu_baseline": cpu, "e2e": e2e, "gpu_launches": int(launches),
         "clocks": clk,
     }
     return line
@@ -843,34 +936,65 @@ def run_gemm(args, rank, world, local_rank):
 # ---------------------------------------------------------------------------
 
 def run_reference(args):
-    from invariant_paged_kv_gb300 import workload as wl  # noqa: F401
+    from invariant_paged_kv_gb300 import workload as wl
     step, layers, name = make_step(args, 0)
-    total = max(1, args.steps + max(3, args.warmup))
+    W = max(3, args.warmup)
+    total = max(1, args.steps + W)
     per_step_s = max(0.5, 60.0 / total)  # whole run within a few minutes
-    rates = []
+    rates, walls = [], []
     desc = ""
     cores = 1
     pool = OraclePool()
     try:
         for k in range(total):
+            t0 = time.perf_counter()
             rate, cores, desc = pool.rate(step, seconds_budget=per_step_s, seed=777 + k)
-            if k >= max(3, args.warmup):
+            wall = time.perf_counter() - t0
+            if k >= W:
                 rates.append(rate)
+                walls.append(wall)
     finally:
         pool.close()
     value = statistics.mean(rates)
-    ms = wl.kv_bytes(step) * layers / (value * 1e9) * 1e3
+    ms = statistics.mean(walls) * 1e3
     return {
         "metric": METRIC, "value": round(value, 4), "unit": "GB/s", "n_gpus": 1,
-        "steps": args.steps, "warmup": max(3, args.warmup), "ms_per_step": round(ms, 1),
+        "steps": args.steps, "warmup": W, "ms_per_step": round(ms, 1),
         "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
         "data": "synthetic", "impl": "reference",
         "config": workload_config(step, layers, name, args),
+        "step_what": (f"each step runs the oracle on a bounded seeded sample of the workload's "
+                      f"lanes (about {per_step_s:.1f} s of compute on every worker); "
+                      f"ms_per_step is the wall time those steps took (input generation "
+                      f"included); value counts oracle compute time only"),
+        "full_step_ms_at_this_rate": round(wl.kv_bytes(step) * layers / (value * 1e9) * 1e3, 1),
         "cpu_baseline": {"value": round(value, 4), "unit": "GB/s", "cores": cores,
                          "kind": "oracle", "sample": desc + f"; {per_step_s:.1f} s budget per step"},
         "e2e": {"value": round(value, 4), "unit": "GB/s", "h2d_bytes_per_step": 0,
                 "d2h_bytes_per_step": 0},
     }
+
+
+SECONDARY_KEYS = ("value", "unit", "ms_per_step", "rows_per_s", "tokens_per_s",
+                  "frac_of_hbm_peak", "bytes_per_step", "phase_ms_per_layer", "roofline",
+                  "prefill_roofline", "kv_append", "gpu_launches", "clocks", "config")
+
+
+def run_secondary(args, rank, world, local_rank):
+    """The mixed ragged step (decode rows + tensor-core prefill chunks) and
+    the decode-only batch, each timed the same way as the headline workload
+    in the same run (K steps from one CUDA graph, phase events, clocks); no
+    end-to-end leg or CPU baseline."""
+    import torch
+    out = {}
+    for wname in ("mixed_step", "decode_batch"):
+        torch.cuda.empty_cache()
+        a2 = argparse.Namespace(**vars(args))
+        a2.workload, a2.layers, a2.no_e2e, a2.no_cpu_baseline = wname, None, True, True
+        l2 = run_ours(a2, rank, world, local_rank)
+        out[wname] = {k: l2[k] for k in SECONDARY_KEYS}
+    torch.cuda.empty_cache()
+    return out
 
 
 def main():
@@ -908,6 +1032,9 @@ def main():
         line = run_gemm(args, rank, world, local_rank)
     else:
         line = run_ours(args, rank, world, local_rank)
+        if args.workload == "long_tail" and not args.small and args.kv == "bf16" \
+                and args.mode == "batch":
+            line["secondary"] = run_secondary(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)
     if world > 1:
