@@ -63,7 +63,7 @@ def parse():
     ap.add_argument("--warmup", type=int, default=5)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
     ap.add_argument("--workload", choices=["long_tail", "decode_batch", "mixed_step",
-                                           "decode_gemm"],
+                                           "prefill_chunks", "decode_gemm"],
                     default="long_tail",
                     help="decode_gemm: the fixed-width decode linear layer (vocabulary head "
                          "248320 x 5120, T_pad 64), a second workload with its own metric")
@@ -103,6 +103,10 @@ def make_step(args, rank, free_bytes=None):
         layers = args.layers or 1
         step = wl.decode_batch(rank, lanes=16 if args.small else 64, dtype=args.kv)
         name = "decode_batch" + ("_e4m3_kv" if args.kv == "fp8" else "")
+    elif args.workload == "prefill_chunks":
+        layers = args.layers or 1
+        step = wl.prefill_chunks(rank)
+        name = "prefill_chunks"
     else:
         layers = args.layers or 1
         step = wl.mixed_step(rank)
@@ -676,6 +680,13 @@ def run_ours(args, rank, world, local_rank):
                    "peak_kind": tkind, "frac": round(ach / tpeak, 4),
                    "flops_per_launch": pf, "avg_launch_ms": round(dec_ms, 4)}
 
+    if prefill is not None and not (step.q_lens == 1).any():
+        # no decode rows: the launch is the tensor-core prefill alone
+        roofline = dict(prefill)
+        roofline["kernel"] = ("mixed_kernel, every CTA in the prefill role (tcgen05, "
+                              "bf16 -> fp32)" if mixed else prefill["kernel"])
+        roofline["traffic"] = None
+
     cpu = None
     if rank == 0 and world == 1 and not args.no_cpu_baseline:
         pool = OraclePool()
@@ -981,13 +992,14 @@ SECONDARY_KEYS = ("value", "unit", "ms_per_step", "rows_per_s", "tokens_per_s",
 
 
 def run_secondary(args, rank, world, local_rank):
-    """The mixed ragged step (decode rows + tensor-core prefill chunks) and
-    the decode-only batch, each timed the same way as the headline workload
-    in the same run (K steps from one CUDA graph, phase events, clocks); no
+    """The mixed ragged step (decode rows + tensor-core prefill chunks), its
+    prefill chunks alone (the tensor-core prefill on every SM) and the
+    decode-only batch, each timed the same way as the headline workload in
+    the same run (K steps from one CUDA graph, phase events, clocks); no
     end-to-end leg or CPU baseline."""
     import torch
     out = {}
-    for wname in ("mixed_step", "decode_batch"):
+    for wname in ("mixed_step", "prefill_chunks", "decode_batch"):
         torch.cuda.empty_cache()
         a2 = argparse.Namespace(**vars(args))
         a2.workload, a2.layers, a2.no_e2e, a2.no_cpu_baseline = wname, None, True, True

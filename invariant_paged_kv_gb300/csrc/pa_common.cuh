@@ -35,7 +35,7 @@ constexpr long long kWaitCycles = 2000000000LL;
 // Split plan, built on the device by the prologue kernel from cu_seqlens_q and
 // ctx_lens, stored in the workspace:
 //   header[0] = number of (row, split) pairs, header[1] = number of full pairs,
-//   header[2] = number of prefill q tiles, header[3] = number of prefill-row
+//   header[2] = number of prefill q-tile pairs, header[3] = number of prefill-row
 //   group records, header[4 + 2 c .. 5 + 2 c] = item counter c (64-bit,
 //   zeroed with the plan): c = 0 the split kernels, 1 the tensor-core
 //   prefill, 2 the prefill-row kernel; header[kHeaderSplitKeys],
@@ -46,8 +46,9 @@ constexpr long long kWaitCycles = 2000000000LL;
 //   pairs[capacity - 1 - (k - header[1])], see pair_slot)
 //   row_info[r] = {first full pair, tail pair or -1, number of splits, lane or -1}
 //   pairs[k]    = {row, split index, lane, key count of the row}
-//   ptiles[i]   = {lane, 128-row tile index, position of its last row, 0},
-//                 heaviest first (tensor-core prefill path)
+//   ptiles[i]   = {lane, index t of the pair of 128-row q tiles 2 t and
+//                 2 t + 1, position of the pair's last row, 0}, heaviest
+//                 first (tensor-core prefill path)
 // Full pairs (exactly kSplit keys) come first, lane-major; tail pairs after.
 // row_info.y holds the tail pair's slot itself.
 // Partial results of pair k: ml[k * H + h] = {m (log2 domain), l},

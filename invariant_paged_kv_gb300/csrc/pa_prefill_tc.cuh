@@ -4,9 +4,9 @@
 // continuous-batching sampler", Design, engine.py: prefill chunks and decode
 // tokens share one flat step; Evidence, mutant "prefill causal mask off by
 // one"): its row j sits at position ctx - q_len + j and attends keys
-// 0..position. Work item = (128-row q tile of one lane, a pair of query heads
-// that read the same kv head). Per item, key tiles of 128 keys go in
-// ascending order; for each head of the pair and each key tile:
+// 0..position. Work item = (query head, pair of consecutive 128-row q tiles
+// of one lane): two streams that read the same key tiles. Per item, key tiles
+// of 128 keys go in ascending order; for each stream s and key tile:
 //   S = Q K^T           tcgen05.mma, M = 128 rows, N = 128 keys, K = D, fp32 in TMEM
 //   m, p, l             one thread per row: running max, p = 2^(t - m) rounded
 //                       to bf16 and written back over S in TMEM, l += sum of
@@ -16,20 +16,27 @@
 // and finally out = O * (1 / l). The running max moves only when a tile's max
 // exceeds it by more than 8 (log2 units), so O is rescaled rarely. A row's
 // arithmetic depends on its q row, its keys and the fixed 128-key tiling from
-// key 0 -- never on other lanes. (N = 128 keys: a 128 x 128 x 16 product runs
-// at the tensor core's full rate, where a 128 x 64 x 16 one reaches ~70%.)
+// key 0 -- never on other lanes, other heads, or the other stream. (N = 128
+// keys: a 128 x 128 x 16 product runs at the tensor core's full rate, where
+// a 128 x 64 x 16 one reaches ~70%.) The second tile of a pair may need one
+// key tile more than the first (causal); the first stream skips it.
 //
-// Warp roles (320 threads): warps 0-3 and 4-7 are two softmax groups (one per
-// head of the pair; thread r of a group owns row r = TMEM lane r), warp 8
-// issues the MMAs (one elected thread), warp 9 streams Q / K / V in by TMA (K /
-// V through the block table, 16 keys per box) into 2-deep K and V rings shared
-// by both heads. TMEM per head slot (256 of the 512 columns): S / P (128), O
-// (128). Each head has one S / P buffer; the MMA warp serves the two heads in
-// turn -- P V of tile t for a head, then (once that P is consumed) its S of
-// tile t + 1 -- so one head's softmax runs while the tensor core works for the
-// other. Every wait is bounded (timeout -> PA_FLAG_TIMEOUT). No parity wait
-// ever meets a barrier more than one phase away from the awaited one, ahead
-// or behind (the P V barriers alternate by tile parity for that reason).
+// Warp roles (320 threads): warps 0-3 and 4-7 are the two streams' softmax
+// groups (thread r of a group owns row r = TMEM lane r), warp 8 issues the
+// MMAs (one elected lane of the converged warp), warp 9 streams Q / K / V in
+// by TMA (K / V through the block table, 16 keys per box) into 2-deep K and
+// V rings shared by both streams. TMEM per stream (256 of the 512 columns): S / P (128), O (128).
+// The issuing warp is stalled while the tensor pipe's queue is full, so its
+// order is the pipe's order: per key tile and stream, P V of tile t and then
+// S of tile t + 1 (which overwrites P of tile t in TMEM, so it waits for
+// that P V to finish); the streams alternate, so one stream's softmax runs
+// while the tensor core serves the other.
+//
+// Every wait is bounded (timeout -> PA_FLAG_TIMEOUT); before the CTA leaves,
+// the MMA warp waits for its products and the TMA warp for its copies. No
+// parity wait ever meets a barrier more than one phase away from the awaited
+// one, ahead or behind (the P V barriers alternate by tile parity for that
+// reason).
 //
 // The work is written as the code of one CTA (prefill_tc_cta): it runs as the
 // prefill role of the mixed-step kernel (pa_mixed.cu), which gives every CTA
@@ -42,7 +49,7 @@ namespace pa {
 namespace pftc {
 
 
-constexpr int kRows = 128;  // query rows per item (M)
+constexpr int kRows = 128;  // query rows per tile (M)
 constexpr int kKeys = 128;  // keys per tile (N of S, K of PV)
 constexpr int kStages = 2;  // depth of the K and V rings
 constexpr int kThreads = 320;
@@ -57,7 +64,7 @@ struct PfLayout {
   static constexpr int kQBytes = kHalves * kHalfBytes;   // one Q tile
   static constexpr int kKBytes = kHalves * kKHalfBytes;  // one K tile
   static constexpr int kVBytes = kHalves * kKHalfBytes;  // one V tile
-  static constexpr int kQ = 0;                           // Q of head A, then head B
+  static constexpr int kQ = 0;                           // Q of stream 0, then stream 1
   static constexpr int kK0 = kQ + 2 * kQBytes;
   static constexpr int kV0 = kK0 + kStages * kKBytes;
   static constexpr int kEnd = kV0 + kStages * kVBytes;
@@ -68,53 +75,60 @@ struct PfLayout {
 
 struct Bars {
   uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
-  uint64_t q, s[2], p[2], o[2][2];  // [head slot] ([tile parity] for o)
+  uint64_t q, qempty, vtail, fin, s[2], p[2], o[2][2];  // [stream] ([tile parity] for o)
 };
 
 struct ItemInfo {
-  int lane, tile, head0, has_b, cu0, q_len, ctx, nrows, p_first, nkt, kvh;
+  int lane, head, kvh, cu0, q_len, ctx, nst, nkt;
+  int row0[2], nrows[2], p_first[2], nkt_s[2];
 };
 
-__device__ __forceinline__ ItemInfo item_info(const StepParams& p, int item, int g) {
+// Item = (pair entry t, head): consecutive items share a pair and walk its
+// heads in order, so the g heads of a kv head follow each other.
+__device__ __forceinline__ ItemInfo item_info(const StepParams& p, int item) {
   ItemInfo it;
-  const int npair = (g + 1) / 2;
-  const int per_tile = p.Hkv * npair;
-  const int t = item / per_tile;
-  const int rem = item - t * per_tile;
-  it.kvh = rem / npair;
-  const int j = rem - it.kvh * npair;
-  it.head0 = it.kvh * g + 2 * j;
-  it.has_b = (2 * j + 1) < g;
+  const int t = item / p.H;
+  it.head = item - t * p.H;
+  it.kvh = it.head / (p.H / p.Hkv);
   const int4 e = p.plan.ptiles[t];
   it.lane = e.x;
-  it.tile = e.y;
   it.cu0 = p.cu_seqlens[it.lane];
   it.q_len = p.cu_seqlens[it.lane + 1] - it.cu0;
   it.ctx = p.ctx_lens[it.lane];
-  const int row0 = it.tile * kRows;
-  it.nrows = min(kRows, it.q_len - row0);
-  it.p_first = it.ctx - it.q_len + row0;
-  const int p_last = it.p_first + it.nrows - 1;
-  it.nkt = p_last / kKeys + 1;
+  it.nst = 0;
+  it.nkt = 0;
+#pragma unroll
+  for (int s = 0; s < 2; ++s) {
+    it.row0[s] = (2 * e.y + s) * kRows;
+    it.nrows[s] = min(kRows, it.q_len - it.row0[s]);
+    it.p_first[s] = it.ctx - it.q_len + it.row0[s];
+    it.nkt_s[s] = it.nrows[s] > 0 ? (it.p_first[s] + it.nrows[s] - 1) / kKeys + 1 : 0;
+    if (it.nrows[s] > 0) it.nst = s + 1;
+    it.nkt = max(it.nkt, it.nkt_s[s]);
+  }
   return it;
 }
 
-// Wait with the CTA-wide abort flag: returns false (and sets the flag) on timeout.
+// Wait with the CTA-wide abort flag: returns false (and sets the flag) on
+// timeout. The fast path is one try_wait: the flag lives in shared memory,
+// and a shared load waits behind the tensor core's operand reads (~140
+// cycles while products stream), so it is read only in the slow loop.
 __device__ __forceinline__ bool wait_or_abort_1(uint32_t bar, uint32_t parity,
                                                 volatile int* abort_flag, int* status,
                                                 long long limit) {
-  if (*abort_flag) return false;
   if (mbar_try_wait(bar, parity)) return true;
   const long long t0 = clock64();
-  while (!mbar_try_wait(bar, parity)) {
-    if (*abort_flag) return false;
-    if (clock64() - t0 > limit) {
-      *abort_flag = 1;
-      raise_flag(status, PA_FLAG_TIMEOUT);
-      return false;
+  for (uint32_t i = 0;; ++i) {
+    if (mbar_try_wait(bar, parity)) return true;
+    if ((i & 7) == 7) {
+      if (*abort_flag) return false;
+      if (clock64() - t0 > limit) {
+        *abort_flag = 1;
+        raise_flag(status, PA_FLAG_TIMEOUT);
+        return false;
+      }
     }
   }
-  return true;
 }
 
 // Every lane of the warp waits; the verdict is made warp-uniform.
@@ -125,24 +139,28 @@ __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
 }
 
 // The work of one CTA of kThreads threads (see the roles above); dsmem
-// holds PfLayout<D>::kSmemBytes bytes.
+// holds PfLayout<D>::kSmemBytes bytes. Each role runs its own loop over the
+// CTA's items (no CTA-wide barrier between items): the TMA warp takes item
+// indices from the prefill counter and publishes them through a 4-slot queue
+// (slot n % 4 for the CTA's n-th item, freed when all nine consumer warps
+// have read it), and the rings, the Q buffer and the TMEM regions carry the
+// handoffs from one item to the next.
 template <int D>
 __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtensorMap* tmQ,
                                                const CUtensorMap* tmK, const CUtensorMap* tmV,
                                                uint8_t* dsmem) {
   using L = PfLayout<D>;
+  constexpr int kSlots = 4;
   __shared__ __align__(8) Bars bars;
+  __shared__ __align__(8) uint64_t item_full[kSlots], item_free[kSlots];
   __shared__ uint32_t s_tmem;
   __shared__ volatile int s_abort;
-  // items are taken from the prefill item counter in list order (heaviest
-  // tiles first): thread 0 takes item n + 1 during item n into slot
-  // (n + 1) & 1, and the end-of-item barrier publishes it
-  __shared__ long long s_item[2];
+  __shared__ long long s_items[kSlots];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
   const uint32_t sQ = base + L::kQ, sK0 = base + L::kK0, sV0 = base + L::kV0;
-  const uint32_t bq = smem_u32(&bars.q);
+  const uint32_t bq = smem_u32(&bars.q), bqe = smem_u32(&bars.qempty), bvt = smem_u32(&bars.vtail);
   uint32_t bkf[kStages], bke[kStages], bvf[kStages], bve[kStages];
 #pragma unroll
   for (int i = 0; i < kStages; ++i) {
@@ -159,14 +177,20 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
       mbar_init(bve[i], 1);
     }
     mbar_init(bq, 1);
+    mbar_init(bqe, 1);
+    mbar_init(bvt, 1);
+    mbar_init(smem_u32(&bars.fin), 1);
     for (int h = 0; h < 2; ++h) {
       mbar_init(smem_u32(&bars.s[h]), 1);
       mbar_init(smem_u32(&bars.p[h]), kRows);
       mbar_init(smem_u32(&bars.o[h][0]), 1);
       mbar_init(smem_u32(&bars.o[h][1]), 1);
     }
+    for (int i = 0; i < kSlots; ++i) {
+      mbar_init(smem_u32(&item_full[i]), 1);
+      mbar_init(smem_u32(&item_free[i]), 9);  // 8 softmax warps + the MMA warp
+    }
     s_abort = 0;
-    s_item[0] = (long long)atomicAdd(item_counter(p.plan, kCounterPrefill), 1ull);
     fence_mbar_init();
   }
   if (warp == 9 && lane == 0) {
@@ -179,42 +203,63 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
   __syncthreads();
   tc_fence_after();
   const uint32_t tmem = s_tmem;
-  // head slot h: S / P at column 256 h, O at 256 h + 128
-  auto tS = [&](int h) -> uint32_t { return tmem + 256 * h; };
-  auto tO = [&](int h) -> uint32_t { return tmem + 256 * h + 128; };
-  auto bS = [&](int h) -> uint32_t { return smem_u32(&bars.s[h]); };
-  auto bP = [&](int h) -> uint32_t { return smem_u32(&bars.p[h]); };
-  // P V of tile t completes on o[head][t & 1]
-  auto bO = [&](int h, uint32_t t) -> uint32_t { return smem_u32(&bars.o[h][t & 1]); };
+  // stream s: S / P at column 256 s, O at 256 s + 128
+  auto tS = [&](int s) -> uint32_t { return tmem + 256 * s; };
+  auto tO = [&](int s) -> uint32_t { return tmem + 256 * s + 128; };
+  auto bS = [&](int s) -> uint32_t { return smem_u32(&bars.s[s]); };
+  auto bP = [&](int s) -> uint32_t { return smem_u32(&bars.p[s]); };
+  // P V of tile t completes on o[stream][t & 1]
+  auto bO = [&](int s, uint32_t t) -> uint32_t { return smem_u32(&bars.o[s][t & 1]); };
+  volatile int* ab = &s_abort;
+  const long long lim = p.wait_cycles;
+  // the CTA's n-th item, as the TMA warp published it (a consumer warp:
+  // wait for the slot, read it, free it); false on abort
+  auto read_item = [&](uint32_t n, long long& item) -> bool {
+    if (!wait_or_abort(smem_u32(&item_full[n % kSlots]), (n / kSlots) & 1, ab, p.status, lim))
+      return false;
+    item = s_items[n % kSlots];
+    __syncwarp();
+    if (lane == 0) mbar_arrive(smem_u32(&item_free[n % kSlots]));
+    return true;
+  };
 
-  const int g = p.H / p.Hkv;
-  const int n_items = p.plan.header[2] * p.Hkv * ((g + 1) / 2);
+  const int n_items = p.plan.header[2] * p.H;
   const float c2 = p.scale_log2;  // > 0 (validated on the host)
-  // running use counters, identical in every role: items, K/V ring fills,
-  // key tiles done by each head slot
-  uint32_t n_item = 0, n_kv = 0, n_t[2] = {0, 0};
+  // running use counters, identical in every role: K/V ring fills, key tiles
+  // of each stream, items with a tail key tile
+  uint32_t n_item = 0, n_kv = 0, n_t[2] = {0, 0}, n_tail = 0;
 
-  for (;;) {
-    const long long item = s_item[n_item & 1];
-    if (item >= n_items) break;
-    if (threadIdx.x == 0)
-      s_item[(n_item + 1) & 1] = (long long)atomicAdd(item_counter(p.plan, kCounterPrefill), 1ull);
-    const ItemInfo it = item_info(p, (int)item, g);
-    const int nh = 1 + it.has_b;
-
-    if (warp == 9) {
-      // ------------------------------ producer ------------------------------
-      // Q of this item's heads (the previous item's S products, which read
-      // this buffer, all finished before the item boundary)
+  if (warp == 9) {
+    // -------------------------------- producer ------------------------------
+    for (;; ++n_item) {
+      const uint32_t n = n_item;
+      // slot n % 4 is free once every consumer has read item n - 4
+      if (n >= kSlots &&
+          !wait_or_abort(smem_u32(&item_free[n % kSlots]), ((n / kSlots) - 1) & 1, ab, p.status, lim))
+        break;
+      long long item = 0;
       if (lane == 0) {
-        mbar_expect_tx(bq, nh * L::kQBytes);
-        for (int hb = 0; hb < nh; ++hb)
+        item = (long long)atomicAdd(item_counter(p.plan, kCounterPrefill), 1ull);
+        s_items[n % kSlots] = item;
+        mbar_arrive(smem_u32(&item_full[n % kSlots]));
+      }
+      item = __shfl_sync(0xffffffffu, item, 0);
+      if (item >= n_items) break;
+      const ItemInfo it = item_info(p, (int)item);
+      const bool tail = it.nkt * kKeys > it.ctx;  // only the last key tile can run past ctx
+      // Q of this item's streams, once every S product of the previous item
+      // (which read this buffer) has finished
+      if (n >= 1 && !wait_or_abort(bqe, (n - 1) & 1, ab, p.status, lim)) break;
+      if (lane == 0) {
+        mbar_expect_tx(bq, it.nst * L::kQBytes);
+        for (int s = 0; s < it.nst; ++s)
 #pragma unroll
           for (int h = 0; h < L::kHalves; ++h)
-            tma_load_3d(sQ + hb * L::kQBytes + h * L::kHalfBytes, tmQ, h * 64, it.head0 + hb,
-                        it.cu0 + it.tile * kRows, bq);
+            tma_load_3d(sQ + s * L::kQBytes + h * L::kHalfBytes, tmQ, h * 64, it.head,
+                        it.cu0 + it.row0[s], bq);
       }
-      for (int kt = 0; kt < it.nkt; ++kt) {
+      bool ok = true;
+      for (int kt = 0; ok && kt < it.nkt; ++kt) {
         const uint32_t f = n_kv + kt, st = f % kStages, use = f / kStages;
         const int key0 = kt * kKeys;
         const int nchunk = min(kKeys / kChunk, (it.ctx - key0 + kChunk - 1) / kChunk);
@@ -229,7 +274,8 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         const uint32_t bytes = (uint32_t)nchunk * L::kHalves * kChunk * 128;
         // lane c (< nchunk) copies chunk c: the boxes go out in parallel
         const int tok = blk * p.bs + (key0 + lane * kChunk) % p.bs;
-        if (use >= 1 && !wait_or_abort(bke[st], (use - 1) & 1, &s_abort, p.status, p.wait_cycles)) break;
+        ok = use < 1 || wait_or_abort(bke[st], (use - 1) & 1, ab, p.status, lim);
+        if (!ok) break;
         if (lane == 0) mbar_expect_tx(bkf[st], bytes);
         __syncwarp();
         if (lane < nchunk) {
@@ -238,7 +284,8 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
             tma_load_3d(sK0 + st * L::kKBytes + h * L::kKHalfBytes + lane * kChunk * 128, tmK,
                         h * 64, it.kvh, tok, bkf[st]);
         }
-        if (use >= 1 && !wait_or_abort(bve[st], (use - 1) & 1, &s_abort, p.status, p.wait_cycles)) break;
+        ok = use < 1 || wait_or_abort(bve[st], (use - 1) & 1, ab, p.status, lim);
+        if (!ok) break;
         if (lane == 0) mbar_expect_tx(bvf[st], bytes);
         __syncwarp();
         if (lane < nchunk) {
@@ -247,50 +294,13 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
             tma_load_3d(sV0 + st * L::kVBytes + h * L::kKHalfBytes + lane * kChunk * 128, tmV,
                         h * 64, it.kvh, tok, bvf[st]);
         }
-      }
-    } else if (warp == 8) {
-      // ------------------------------ MMA issuer ----------------------------
-      constexpr uint32_t idS = umma_idesc_bf16(kRows, kKeys, 0, 0);
-      constexpr uint32_t idPV = umma_idesc_bf16(kRows, D, 0, 1);
-      // S of key tile j for head slot hb: A = Q tile, B = K tile (both smem)
-      auto issue_s = [&](int hb, int j) {
-        const uint32_t st = (n_kv + j) % kStages;
-        if (lane == 0) {
-#pragma unroll
-          for (int kk = 0; kk < D / 16; ++kk) {
-            const uint32_t off_q = (kk >> 2) * L::kHalfBytes + (kk & 3) * 32;
-            const uint32_t off_k = (kk >> 2) * L::kKHalfBytes + (kk & 3) * 32;
-            const uint64_t ad = umma_desc_sw128(sQ + hb * L::kQBytes + off_q, 16, 1024);
-            const uint64_t bd = umma_desc_sw128(sK0 + st * L::kKBytes + off_k, 16, 1024);
-            umma_bf16(tS(hb), ad, bd, idS, kk > 0 ? 1u : 0u);
-          }
-          umma_commit(bS(hb));
-        }
-        __syncwarp();
-      };
-      bool ok = true;
-      // first S of the item, once Q is in TMEM and K tile 0 has landed
-      {
-        const uint32_t f = n_kv, st = f % kStages;
-        ok = wait_or_abort(bkf[st], (f / kStages) & 1, &s_abort, p.status, p.wait_cycles) &&
-             wait_or_abort(bq, n_item & 1, &s_abort, p.status, p.wait_cycles);
-        for (int hb = 0; ok && hb < nh; ++hb) {
-          tc_fence_after();
-          issue_s(hb, 0);
-        }
-        if (ok && lane == 0) umma_commit(bke[st]);
-        __syncwarp();
-      }
-      for (int kt = 0; ok && kt < it.nkt; ++kt) {
-        const uint32_t f = n_kv + kt, st = f % kStages;
-        const bool next = kt + 1 < it.nkt;
-        const uint32_t f1 = f + 1, st1 = f1 % kStages;
-        if (!wait_or_abort(bvf[st], (f / kStages) & 1, &s_abort, p.status, p.wait_cycles)) break;
-        const int key0 = kt * kKeys;
-        if (key0 + kKeys > it.ctx) {
-          // keys past the lane's end: zero their V rows (stale bytes must not
-          // meet p = 0 as 0 * NaN)
-          const int first = max(0, it.ctx - key0);
+        if (kt == it.nkt - 1 && tail) {
+          // keys past the lane's end: once the tile has landed, zero their V
+          // rows (stale bytes must not meet p = 0 as 0 * NaN); the MMA warp
+          // takes this tile from the vtail barrier
+          ok = wait_or_abort(bvf[st], use & 1, ab, p.status, lim);
+          if (!ok) break;
+          const int first = it.ctx - key0;
           const int n16 = (kKeys - first) * 8 * L::kHalves;
           for (int i = lane; i < n16; i += 32) {
             const int c16 = i & 7, rest = i >> 3;
@@ -300,77 +310,163 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
           }
           fence_proxy_async_smem();
           __syncwarp();
+          if (lane == 0) mbar_arrive(bvt);
         }
-        for (int hb = 0; hb < nh; ++hb) {
-          const uint32_t th = n_t[hb] + kt;
-          // P V of tile kt, once this head's softmax has written P
-          if (!wait_or_abort(bP(hb), th & 1, &s_abort, p.status, p.wait_cycles)) { ok = false; break; }
-          tc_fence_after();
-          if (lane == 0) {
+      }
+      if (!ok) break;
+      n_kv += it.nkt;
+      n_tail += tail ? 1 : 0;
+    }
+  } else if (warp == 8) {
+    // -------------------------------- MMA issuer ----------------------------
+    // the whole warp runs the loop with warp-uniform operands; one elected
+    // lane issues each product and commit. Descriptors of each operand tile
+    // are built once and stepped by constant offsets (14-bit address field,
+    // in 16-byte units).
+    constexpr uint32_t idS = umma_idesc_bf16(kRows, kKeys, 0, 0);
+    constexpr uint32_t idPV = umma_idesc_bf16(kRows, D, 0, 1);
+    const uint64_t dQ0 = umma_desc_sw128(sQ, 16, 1024);
+    const uint64_t dK0 = umma_desc_sw128(sK0, 16, 1024);
+    const uint64_t dV0 = umma_desc_sw128(sV0, L::kKHalfBytes, 1024);
+    // S of key tile j of the current item for stream s: A = Q tile, B = K tile
+    auto issue_s = [&](int s, int j) {
+      const uint32_t st = (n_kv + j) % kStages;
+      const uint64_t dq = dQ0 + (uint64_t)((s * L::kQBytes) >> 4);
+      const uint64_t dk = dK0 + (uint64_t)((st * L::kKBytes) >> 4);
 #pragma unroll
-            for (int k = 0; k < kKeys / 16; ++k) {
-              const uint64_t bd = umma_desc_sw128(sV0 + st * L::kVBytes + k * 16 * 128,
-                                                  L::kKHalfBytes, 1024);
-              umma_bf16_tmem_a(tO(hb), tS(hb) + k * 8, bd, idPV, (kt > 0 || k > 0) ? 1u : 0u);
-            }
-            umma_commit(bO(hb, th));
-          }
-          __syncwarp();
-          if (next) {
-            // S of tile kt + 1 needs its K tile, and it overwrites P of tile
-            // kt: wait for that P V
-            if (hb == 0 && !wait_or_abort(bkf[st1], (f1 / kStages) & 1, &s_abort, p.status, p.wait_cycles)) {
-              ok = false;
-              break;
-            }
-            if (!wait_or_abort(bO(hb, th), (th >> 1) & 1, &s_abort, p.status, p.wait_cycles)) { ok = false; break; }
-            tc_fence_after();
-            issue_s(hb, kt + 1);
-          }
+      for (int kk = 0; kk < D / 16; ++kk) {
+        const uint32_t oq = ((kk >> 2) * L::kHalfBytes + (kk & 3) * 32) >> 4;
+        const uint32_t ok = ((kk >> 2) * L::kKHalfBytes + (kk & 3) * 32) >> 4;
+        umma_bf16_w(tS(s), dq + oq, dk + ok, idS, kk > 0 ? 1u : 0u);
+      }
+      umma_commit_w(bS(s));
+    };
+    auto issue_pv = [&](int s, int j, uint32_t ts) {
+      const uint32_t st = (n_kv + j) % kStages;
+      const uint64_t dv = dV0 + (uint64_t)((st * L::kVBytes) >> 4);
+#pragma unroll
+      for (int k = 0; k < kKeys / 16; ++k)
+        umma_bf16_tmem_a_w(tO(s), tS(s) + k * 8, dv + (uint64_t)((k * 16 * 128) >> 4), idPV,
+                           (j > 0 || k > 0) ? 1u : 0u);
+      umma_commit_w(bO(s, ts));
+    };
+    for (;; ++n_item) {
+      long long item;
+      if (!read_item(n_item, item) || item >= n_items) break;
+      const ItemInfo it = item_info(p, (int)item);
+      const bool tail = it.nkt * kKeys > it.ctx;
+      bool ok = true;
+      // first S of the item for each stream, once Q and K tile 0 have landed
+      // and the stream's last P V (of an earlier item), which reads the P
+      // this S overwrites, has finished
+      {
+        const uint32_t f = n_kv, st = f % kStages;
+        ok = wait_or_abort(bkf[st], (f / kStages) & 1, ab, p.status, lim) &&
+             wait_or_abort(bq, n_item & 1, ab, p.status, lim);
+        for (int s = 0; ok && s < it.nst; ++s) {
+          if (n_t[s] > 0) ok = wait_or_abort(bO(s, n_t[s] - 1), ((n_t[s] - 1) >> 1) & 1, ab,
+                                             p.status, lim);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(s, 0);
         }
         if (!ok) break;
-        if (lane == 0) {
-          umma_commit(bve[st]);
-          if (next) umma_commit(bke[st1]);
-        }
-        __syncwarp();
+        umma_commit_w(bke[st]);
+        if (it.nkt == 1) umma_commit_w(bqe);  // every S of the item issued
       }
-    } else if (warp < 4 || it.has_b) {
-      // ------------------------------ softmax rows --------------------------
-      const int hb = warp >> 2;         // head slot of this group
-      const int r = threadIdx.x & 127;  // row within the tile == TMEM lane
-      const int pos = it.p_first + min(r, it.nrows - 1);
-      const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
-      const uint32_t tOr = tO(hb) + lane_off;
-      const uint32_t tSr = tS(hb) + lane_off;
+      for (int kt = 0; ok && kt < it.nkt; ++kt) {
+        const uint32_t f = n_kv + kt, st = f % kStages;
+        const bool next = kt + 1 < it.nkt;
+        const uint32_t f1 = f + 1, st1 = f1 % kStages;
+        // V of tile kt (the tail tile once its stale rows are zeroed)
+        ok = (kt == it.nkt - 1 && tail) ? wait_or_abort(bvt, n_tail & 1, ab, p.status, lim)
+                                        : wait_or_abort(bvf[st], (f / kStages) & 1, ab,
+                                                        p.status, lim);
+        if (!ok) break;
+        // per stream: P V of tile kt, once its softmax has written P, then S
+        // of tile kt + 1, which overwrites P of tile kt in TMEM and so waits
+        // for that P V to finish; the streams alternate, so one stream's
+        // softmax runs while the tensor core serves the other
+        bool k_ready = false;
+        for (int s = 0; ok && s < it.nst; ++s) {
+          if (kt >= it.nkt_s[s]) continue;
+          const uint32_t ts = n_t[s] + kt;
+          ok = wait_or_abort(bP(s), ts & 1, ab, p.status, lim);
+          if (!ok) break;
+          tc_fence_after();
+          issue_pv(s, kt, ts);
+          if (kt + 1 >= it.nkt_s[s]) continue;
+          if (!k_ready) {
+            ok = wait_or_abort(bkf[st1], (f1 / kStages) & 1, ab, p.status, lim);
+            k_ready = true;
+          }
+          ok = ok && wait_or_abort(bO(s, ts), (ts >> 1) & 1, ab, p.status, lim);
+          if (!ok) break;
+          tc_fence_after();
+          issue_s(s, kt + 1);
+        }
+        if (!ok) break;
+        // Q is free once the item's last S products finish (tile nkt - 1's)
+        if (kt + 2 == it.nkt) umma_commit_w(bqe);
+        umma_commit_w(bve[st]);
+        if (next) umma_commit_w(bke[st1]);
+      }
+      if (!ok) break;
+      n_kv += it.nkt;
+      n_t[0] += it.nkt_s[0];
+      n_t[1] += it.nkt_s[1];
+      n_tail += tail ? 1 : 0;
+    }
+  } else {
+    // -------------------------------- softmax rows --------------------------
+    const int s = warp >> 2;          // stream of this group
+    const int r = threadIdx.x & 127;  // row within the tile == TMEM lane
+    const uint32_t lane_off = (uint32_t)((warp & 3) * 32) << 16;
+    const uint32_t tOr = tO(s) + lane_off;
+    const uint32_t tSr = tS(s) + lane_off;
+    for (;; ++n_item) {
+      long long item;
+      if (!read_item(n_item, item) || item >= n_items) break;
+      const ItemInfo it = item_info(p, (int)item);
+      if (s >= it.nst) continue;  // the pair has no second tile
+      const int pos = it.p_first[s] + min(r, it.nrows[s] - 1);
       float m = -INFINITY, l = 0.f;
       bool ok = true;
 #pragma unroll 1
-      for (int kt = 0; kt < it.nkt; ++kt) {
-        const uint32_t th = n_t[hb] + kt;
-        if (!wait_or_abort(bS(hb), th & 1, &s_abort, p.status, p.wait_cycles)) { ok = false; break; }
+      for (int kt = 0; kt < it.nkt_s[s]; ++kt) {
+        const uint32_t th = n_t[s] + kt;
+        if (!wait_or_abort(bS(s), th & 1, ab, p.status, lim)) { ok = false; break; }
         tc_fence_after();
-        uint32_t sv[kKeys];
-#pragma unroll
-        for (int c = 0; c < kKeys / 32; ++c)
-          tmem_ld32(tSr + 32 * c, *reinterpret_cast<uint32_t(*)[32]>(&sv[32 * c]));
-        tmem_wait_ld();
-        const int lim = pos - kt * kKeys;  // columns c <= lim are visible to this row
-        const bool full = __all_sync(0xffffffffu, lim >= kKeys - 1);
-        // max of the visible raw scores (the scale is positive), eight
-        // independent running maxima folded by a fixed tree
+        const int lim_c = pos - kt * kKeys;  // columns c <= lim_c are visible to this row
+        const bool full = __all_sync(0xffffffffu, lim_c >= kKeys - 1);
+        // pass 1: max of the visible raw scores (the scale is positive), in
+        // 32-column chunks two at a time; eight independent running maxima
+        // folded by a fixed tree
         float m8[8];
 #pragma unroll
         for (int j = 0; j < 8; ++j) m8[j] = -INFINITY;
-        if (full) {
 #pragma unroll
-          for (int i = 0; i < kKeys; i += 2)
-            m8[(i >> 1) & 7] =
-                fmax3(m8[(i >> 1) & 7], __uint_as_float(sv[i]), __uint_as_float(sv[i + 1]));
-        } else {
+        for (int c2p = 0; c2p < kKeys / 64; ++c2p) {
+          uint32_t a[32], b[32];
+          tmem_ld32(tSr + 64 * c2p, a);
+          tmem_ld32(tSr + 64 * c2p + 32, b);
+          tmem_wait_ld();
+          if (full) {
 #pragma unroll
-          for (int i = 0; i < kKeys; ++i)
-            m8[i & 7] = fmaxf(m8[i & 7], i <= lim ? __uint_as_float(sv[i]) : -INFINITY);
+            for (int i = 0; i < 32; i += 2) {
+              m8[(i >> 1) & 3] = fmax3(m8[(i >> 1) & 3], __uint_as_float(a[i]), __uint_as_float(a[i + 1]));
+              m8[4 + ((i >> 1) & 3)] =
+                  fmax3(m8[4 + ((i >> 1) & 3)], __uint_as_float(b[i]), __uint_as_float(b[i + 1]));
+            }
+          } else {
+            const int c0 = 64 * c2p;
+#pragma unroll
+            for (int i = 0; i < 32; ++i) {
+              m8[i & 3] = fmaxf(m8[i & 3], c0 + i <= lim_c ? __uint_as_float(a[i]) : -INFINITY);
+              m8[4 + (i & 3)] =
+                  fmaxf(m8[4 + (i & 3)], c0 + 32 + i <= lim_c ? __uint_as_float(b[i]) : -INFINITY);
+            }
+          }
         }
 #pragma unroll
         for (int w = 4; w >= 1; w >>= 1)
@@ -382,35 +478,45 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         const float alpha = grow ? ex2_approx(m - mn) : 1.f;
         m = mn;
         const float neg = -mn;
-        // p = 2^(s c2 - m) rounded to bf16, written over S as P (two per
-        // column, 32 columns at a time); l adds the p before rounding, in
-        // four independent pairs of partial sums folded by a fixed tree.
-        // The scaling runs on packed fp32 pairs (lane by lane the same fmaf).
+        // pass 2: p = 2^(s c2 - m) rounded to bf16, written over S as P (two
+        // per column: chunk c of 32 scores becomes P columns 16 c .. 16 c + 15,
+        // all of them already read); the next chunk's scores are loaded while
+        // this one is computed. l adds the p before rounding, in four
+        // independent pairs of partial sums folded by a fixed tree. The
+        // scaling runs on packed fp32 pairs (lane by lane the same fmaf).
         const uint64_t c2x2 = f32x2(c2, c2), negx2 = f32x2(neg, neg);
         uint64_t r4[4];
 #pragma unroll
         for (int j = 0; j < 4; ++j) r4[j] = f32x2(0.f, 0.f);
+        uint32_t cur[32], nxt[32];
+        tmem_ld32(tSr, cur);
+        tmem_wait_ld();
 #pragma unroll
-        for (int hh = 0; hh < 2; ++hh) {
-          uint32_t pk[kKeys / 4];
+        for (int c = 0; c < kKeys / 32; ++c) {
+          if (c + 1 < kKeys / 32) tmem_ld32(tSr + 32 * (c + 1), nxt);
+          uint32_t pk[16];
 #pragma unroll
-          for (int i = 0; i < kKeys / 4; ++i) {
-            const int c0 = hh * (kKeys / 2) + 2 * i;
+          for (int i = 0; i < 16; ++i) {
+            const int col = 32 * c + 2 * i;
             float t0, t1;
-            f32x2_split(fma_f32x2(f32x2(__uint_as_float(sv[c0]), __uint_as_float(sv[c0 + 1])),
+            f32x2_split(fma_f32x2(f32x2(__uint_as_float(cur[2 * i]), __uint_as_float(cur[2 * i + 1])),
                                   c2x2, negx2),
                         t0, t1);
             float e0 = ex2_approx(t0);
             float e1 = ex2_approx(t1);
             if (!full) {
-              e0 = (c0 <= lim) ? e0 : 0.f;
-              e1 = (c0 + 1 <= lim) ? e1 : 0.f;
+              e0 = (col <= lim_c) ? e0 : 0.f;
+              e1 = (col + 1 <= lim_c) ? e1 : 0.f;
             }
             pk[i] = pack_bf16x2(e0, e1);
             r4[i & 3] = add_f32x2(r4[i & 3], f32x2(e0, e1));
           }
-          tmem_st16(tSr + hh * 32, *reinterpret_cast<uint32_t(*)[16]>(&pk[0]));
-          tmem_st16(tSr + hh * 32 + 16, *reinterpret_cast<uint32_t(*)[16]>(&pk[16]));
+          tmem_st16(tSr + 16 * c, pk);
+          if (c + 1 < kKeys / 32) {
+            tmem_wait_ld();
+#pragma unroll
+            for (int i = 0; i < 32; ++i) cur[i] = nxt[i];
+          }
         }
         r4[0] = add_f32x2(r4[0], r4[2]);
         r4[1] = add_f32x2(r4[1], r4[3]);
@@ -426,7 +532,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         // than one phase away from any wait on it even when tiles without a
         // rescale skip the wait.
         if (kt > 0 && __any_sync(0xffffffffu, alpha != 1.f)) {
-          if (!wait_or_abort(bO(hb, th - 1), ((th - 1) >> 1) & 1, &s_abort, p.status, p.wait_cycles)) {
+          if (!wait_or_abort(bO(s, th - 1), ((th - 1) >> 1) & 1, ab, p.status, lim)) {
             ok = false;
             break;
           }
@@ -443,41 +549,54 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
           tmem_wait_st();
         }
         tc_fence_before();
-        mbar_arrive(bP(hb));
+        mbar_arrive(bP(s));
       }
-      const uint32_t last = n_t[hb] + it.nkt - 1;
-      if (ok && wait_or_abort(bO(hb, last), (last >> 1) & 1, &s_abort, p.status, p.wait_cycles)) {
-        tc_fence_after();
-        const bool valid = r < it.nrows;
-        const float inv_l = 1.f / l;  // one division per row; out = O * (1 / l)
-        __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
-                             ((size_t)(it.cu0 + it.tile * kRows + r) * p.H + it.head0 + hb) * D;
+      if (!ok) break;
+      // the row's output once its last P V has finished; the next item's
+      // first P V (which restarts O) waits for this group's first P of that
+      // item, which comes after these reads
+      const uint32_t last = n_t[s] + it.nkt_s[s] - 1;
+      if (!wait_or_abort(bO(s, last), (last >> 1) & 1, ab, p.status, lim)) break;
+      tc_fence_after();
+      const bool valid = r < it.nrows[s];
+      const float inv_l = 1.f / l;  // one division per row; out = O * (1 / l)
+      __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
+                           ((size_t)(it.cu0 + it.row0[s] + r) * p.H + it.head) * D;
 #pragma unroll 1
-        for (int c = 0; c < D / 32; ++c) {
-          uint32_t ov[32];
-          tmem_ld32(tOr + c * 32, ov);
-          tmem_wait_ld();
-          if (valid) {
+      for (int c = 0; c < D / 32; ++c) {
+        uint32_t ov[32];
+        tmem_ld32(tOr + c * 32, ov);
+        tmem_wait_ld();
+        if (valid) {
 #pragma unroll
-            for (int i = 0; i < 32; i += 8) {
-              uint4 v;
-              v.x = pack_bf16x2(__uint_as_float(ov[i]) * inv_l, __uint_as_float(ov[i + 1]) * inv_l);
-              v.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv_l, __uint_as_float(ov[i + 3]) * inv_l);
-              v.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv_l, __uint_as_float(ov[i + 5]) * inv_l);
-              v.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv_l, __uint_as_float(ov[i + 7]) * inv_l);
-              *reinterpret_cast<uint4*>(out + c * 32 + i) = v;
-            }
+          for (int i = 0; i < 32; i += 8) {
+            uint4 v;
+            v.x = pack_bf16x2(__uint_as_float(ov[i]) * inv_l, __uint_as_float(ov[i + 1]) * inv_l);
+            v.y = pack_bf16x2(__uint_as_float(ov[i + 2]) * inv_l, __uint_as_float(ov[i + 3]) * inv_l);
+            v.z = pack_bf16x2(__uint_as_float(ov[i + 4]) * inv_l, __uint_as_float(ov[i + 5]) * inv_l);
+            v.w = pack_bf16x2(__uint_as_float(ov[i + 6]) * inv_l, __uint_as_float(ov[i + 7]) * inv_l);
+            *reinterpret_cast<uint4*>(out + c * 32 + i) = v;
           }
         }
-        tc_fence_before();
       }
+      tc_fence_before();
+      n_t[s] += it.nkt_s[s];
     }
-    n_kv += it.nkt;
-    n_t[0] += it.nkt;
-    if (it.has_b) n_t[1] += it.nkt;
-    ++n_item;
-    __syncthreads();
-    if (s_abort) break;
+  }
+  // before TMEM is released and the CTA leaves: every product the MMA warp
+  // issued has completed (a commit tracks all of them), and every copy the
+  // TMA warp issued has landed (on an abort some may still be in flight; on
+  // a normal exit the waits return at once)
+  if (warp == 8) {
+    umma_commit_w(smem_u32(&bars.fin));
+    mbar_wait_bounded(smem_u32(&bars.fin), 0, lim);
+  }
+  if (warp == 9 && lane == 0) {
+    if (n_item > 0) mbar_wait_bounded(bq, (n_item - 1) & 1, lim);
+    for (uint32_t f = n_kv > kStages ? n_kv - kStages : 0; f < n_kv; ++f) {
+      mbar_wait_bounded(bkf[f % kStages], (f / kStages) & 1, lim);
+      mbar_wait_bounded(bvf[f % kStages], (f / kStages) & 1, lim);
+    }
   }
   __syncthreads();
   if (warp == 8) {

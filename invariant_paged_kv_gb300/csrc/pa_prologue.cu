@@ -219,7 +219,8 @@ __device__ bool row_counts(const StepParams& p, const LaneCache* lc, int u, int&
     cnt[rp.sl > kSplit ? 0 : 1] = max(0, min(rp.i1, rp.nf) - rp.i0);
     cnt[2] = (rp.n > rp.nf && rp.n - 1 >= rp.i0 && rp.n - 1 < rp.i1);
   }
-  if (rp.tiles && rp.j == 0) cnt[3] = (rp.q + kPrefillRows - 1) / kPrefillRows;
+  // tensor-core prefill items pair two consecutive 128-row q tiles of a lane
+  if (rp.tiles && rp.j == 0) cnt[3] = (rp.q + 2 * kPrefillRows - 1) / (2 * kPrefillRows);
   return true;
 }
 
@@ -227,7 +228,7 @@ __device__ bool row_counts(const StepParams& p, const LaneCache* lc, int u, int&
 // that balances the two roles' times, from the step's work totals and per-SM
 // rates measured on this part with the roles running side by side -- the
 // decode role streams ~66 GB/s per SM up to ~6760 GB/s in all; the prefill
-// role runs pf_rate flop/s per SM (~4.0 TFLOP/s for the tensor-core prefill,
+// role runs pf_rate flop/s per SM (~5.3 TFLOP/s for the tensor-core prefill,
 // ~1.0 TFLOP/s for the row-invariant mode's prefill rows on mma.sync). fp32
 // (the part's fp64 rate is low); it decides only where work runs, never its
 // result.
@@ -369,8 +370,8 @@ __device__ void build_plan(const StepParams& p) {
       }
       if (ok && rp.tiles && rp.j == 0) {
         const long long t0 = carry[3] + ex[3];
-        for (int t = 0; t < cnt[3]; ++t) {
-          const int last = min(rp.q, (t + 1) * kPrefillRows) - 1;
+        for (int t = 0; t < cnt[3]; ++t) {  // tiles 2 t and 2 t + 1
+          const int last = min(rp.q, (2 * t + 2) * kPrefillRows) - 1;
           pl.ptiles_tmp[t0 + t] = make_int4(rp.b, t, rp.c - rp.q + last, 0);
         }
       }
@@ -380,8 +381,8 @@ __device__ void build_plan(const StepParams& p) {
   }
   const int n = (overflow || p.partials_mode || p.group_rows) ? 0 : (int)total[3];
   __syncthreads();
-  // prefill tiles heaviest first (position of the tile's last row; ties by
-  // list order) when there are at most blockDim of them: the order only
+  // prefill tile pairs heaviest first (position of the pair's last row; ties
+  // by list order) when there are at most blockDim of them: the order only
   // decides which CTA takes a tile first
   if (n <= nth) {
     if (tid < n) s_work[tid] = pl.ptiles_tmp[tid].z;
@@ -406,14 +407,12 @@ __device__ void build_plan(const StepParams& p) {
     for (int c = 0; c < kItemCounters; ++c) *item_counter(pl, c) = 0ull;
     *header_total(pl, kHeaderSplitKeys) = overflow ? 0 : s_mix[0];
     *header_total(pl, kHeaderPrefillWork) = overflow ? 0 : s_mix[1];
-    const int g = p.H / p.Hkv;
     pl.header[kHeaderPrefillCtas] =
         (overflow || !mixed) ? 0
         : p.group_rows ? prefill_role_ctas(p, s_mix[0], s_mix[1], total[4] * p.Hkv, 1.0e12f,
                                            p.sm_count)
-                       : prefill_role_ctas(p, s_mix[0], s_mix[1],
-                                           (long long)n * p.Hkv * ((g + 1) / 2), 4.0e12f,
-                                           p.sm_count);
+                       : prefill_role_ctas(p, s_mix[0], s_mix[1], (long long)n * p.H,
+                                           5.3e12f, p.sm_count);
   }
 }
 

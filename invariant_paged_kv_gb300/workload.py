@@ -284,6 +284,18 @@ def mixed_step(sample: int = 0, chunks: int = 8, chunk_len: int = 512,
     return build_step(geom, q, ctx, _pool_for(ctx, 16), rng)
 
 
+def prefill_chunks(sample: int = 0) -> Step:
+    """The prefill chunks of ``mixed_step`` alone (the same seeded offsets,
+    8 chunks of 512 rows, H40/Hkv8/D128/bs16 bf16): a step whose every row
+    takes the tensor-core prefill path, for measuring that path on its own."""
+    rng = np.random.default_rng(1000 * 3 + sample)
+    geom = Geometry(40, 8, 128, 16, "bf16")
+    rng.standard_normal(120)  # the mixed step's decode lengths, drawn first
+    offs = rng.integers(0, 4096, size=8, endpoint=True)
+    ctx = list(offs + 512)
+    return build_step(geom, [512] * 8, ctx, _pool_for(ctx, 16), rng)
+
+
 INVARIANCE_TARGET_CTX = 4096
 INVARIANCE_SIBLINGS = 7
 
