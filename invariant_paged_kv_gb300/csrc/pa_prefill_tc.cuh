@@ -75,7 +75,10 @@ struct PfLayout {
 
 struct Bars {
   uint64_t kfull[kStages], kempty[kStages], vfull[kStages], vempty[kStages];
-  uint64_t q, qempty, vtail, fin, s[2], p[2], o[2][2];  // [stream] ([tile parity] for o)
+  // vtail[stage]: a tail tile (keys past ctx) in that V stage is zeroed; one
+  // barrier per stage, so a fill can never complete a second phase of it
+  // before the first is consumed (the stage's next fill waits for that)
+  uint64_t q, qempty, vtail[kStages], fin, s[2], p[2], o[2][2];  // [stream] ([tile parity] for o)
 };
 
 struct ItemInfo {
@@ -160,7 +163,8 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const uint32_t base = (smem_u32(dsmem) + 1023u) & ~1023u;
   const uint32_t sQ = base + L::kQ, sK0 = base + L::kK0, sV0 = base + L::kV0;
-  const uint32_t bq = smem_u32(&bars.q), bqe = smem_u32(&bars.qempty), bvt = smem_u32(&bars.vtail);
+  const uint32_t bq = smem_u32(&bars.q), bqe = smem_u32(&bars.qempty);
+  auto bvt = [&](uint32_t st) -> uint32_t { return smem_u32(&bars.vtail[st]); };
   uint32_t bkf[kStages], bke[kStages], bvf[kStages], bve[kStages];
 #pragma unroll
   for (int i = 0; i < kStages; ++i) {
@@ -178,7 +182,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
     }
     mbar_init(bq, 1);
     mbar_init(bqe, 1);
-    mbar_init(bvt, 1);
+    for (int i = 0; i < kStages; ++i) mbar_init(bvt(i), 1);
     mbar_init(smem_u32(&bars.fin), 1);
     for (int h = 0; h < 2; ++h) {
       mbar_init(smem_u32(&bars.s[h]), 1);
@@ -227,7 +231,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
   const float c2 = p.scale_log2;  // > 0 (validated on the host)
   // running use counters, identical in every role: K/V ring fills, key tiles
   // of each stream, items with a tail key tile
-  uint32_t n_item = 0, n_kv = 0, n_t[2] = {0, 0}, n_tail = 0;
+  uint32_t n_item = 0, n_kv = 0, n_t[2] = {0, 0}, n_tail[kStages] = {0, 0};
 
   if (warp == 9) {
     // -------------------------------- producer ------------------------------
@@ -310,12 +314,11 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
           }
           fence_proxy_async_smem();
           __syncwarp();
-          if (lane == 0) mbar_arrive(bvt);
+          if (lane == 0) mbar_arrive(bvt(st));
         }
       }
       if (!ok) break;
       n_kv += it.nkt;
-      n_tail += tail ? 1 : 0;
     }
   } else if (warp == 8) {
     // -------------------------------- MMA issuer ----------------------------
@@ -379,7 +382,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         const bool next = kt + 1 < it.nkt;
         const uint32_t f1 = f + 1, st1 = f1 % kStages;
         // V of tile kt (the tail tile once its stale rows are zeroed)
-        ok = (kt == it.nkt - 1 && tail) ? wait_or_abort(bvt, n_tail & 1, ab, p.status, lim)
+        ok = (kt == it.nkt - 1 && tail) ? wait_or_abort(bvt(st), n_tail[st]++ & 1, ab, p.status, lim)
                                         : wait_or_abort(bvf[st], (f / kStages) & 1, ab,
                                                         p.status, lim);
         if (!ok) break;
@@ -415,7 +418,6 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
       n_kv += it.nkt;
       n_t[0] += it.nkt_s[0];
       n_t[1] += it.nkt_s[1];
-      n_tail += tail ? 1 : 0;
     }
   } else {
     // -------------------------------- softmax rows --------------------------
