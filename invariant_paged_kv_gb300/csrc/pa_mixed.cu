@@ -14,8 +14,10 @@
 // dependency latency) -- and row_mixed_kernel pairs those two the same way.
 //
 // The number of prefill CTAs, which balances the two roles' times, comes
-// from the plan builder (prefill_role_ctas); it decides only where work runs,
-// never its result.
+// from the plan builder (prefill_role_ctas); a prefill CTA that runs out of
+// prefill items then takes decode items, so the launch ends close to the
+// point where both kinds of work are done even when that estimate is off.
+// Neither decides any result.
 #include "pa_decode_bf16.cuh"
 #include "pa_prefill_tc.cuh"
 #include "pa_rows_bf16.cuh"
@@ -33,6 +35,9 @@ __global__ void __launch_bounds__(pftc::kThreads, 1)
   extern __shared__ uint8_t dsmem[];
   if ((int)blockIdx.x < p.plan.header[kHeaderPrefillCtas]) {
     pftc::prefill_tc_cta<D>(p, &tmQ, &tmK, &tmV, dsmem);
+    // out of prefill items (its copies landed, its products finished, its
+    // TMEM released): help with whatever decode items are left
+    if (threadIdx.x < kDecWarps * 32) decode_bf16_warps<D, NT, false, kDecWarps>(p, &tmK, &tmV, dsmem);
   } else if (threadIdx.x < kDecWarps * 32) {
     decode_bf16_warps<D, NT, false, kDecWarps>(p, &tmK, &tmV, dsmem);
   }

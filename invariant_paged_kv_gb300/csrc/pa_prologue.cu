@@ -228,7 +228,7 @@ __device__ bool row_counts(const StepParams& p, const LaneCache* lc, int u, int&
 // that balances the two roles' times, from the step's work totals and per-SM
 // rates measured on this part with the roles running side by side -- the
 // decode role streams ~66 GB/s per SM up to ~6760 GB/s in all; the prefill
-// role runs pf_rate flop/s per SM (~5.3 TFLOP/s for the tensor-core prefill,
+// role runs pf_rate flop/s per SM (~6.0 TFLOP/s for the tensor-core prefill,
 // ~1.0 TFLOP/s for the row-invariant mode's prefill rows on mma.sync). fp32
 // (the part's fp64 rate is low); it decides only where work runs, never its
 // result.
@@ -412,7 +412,7 @@ __device__ void build_plan(const StepParams& p) {
         : p.group_rows ? prefill_role_ctas(p, s_mix[0], s_mix[1], total[4] * p.Hkv, 1.0e12f,
                                            p.sm_count)
                        : prefill_role_ctas(p, s_mix[0], s_mix[1], (long long)n * p.H,
-                                           5.3e12f, p.sm_count);
+                                           6.0e12f, p.sm_count);
   }
 }
 
