@@ -26,13 +26,9 @@ constexpr int kWarps = 8;  // heads per CTA (one warp per (row, head))
 // before their fold so the memory system sees many requests at once; the fold
 // itself runs strictly in split order, so kAhead changes no bit.
 template <int D, int kAhead>
-__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p) {
+__device__ __forceinline__ void fold_row_head(const StepParams& p, int row, int h, int lane) {
   constexpr int VPL = D / 32;  // values per lane
   using Vec = typename std::conditional<VPL == 4, float4, float2>::type;
-  const int row = blockIdx.x;
-  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
-  const int h = blockIdx.y * kWarps + warp;
-  if (h >= p.H) return;
   const int4 info = p.plan.row_info[row];
   if (info.w < 0) return;                                  // not on the split path
   if (p.partials_mode != 2 && info.z <= 1) return;         // written directly
@@ -49,6 +45,18 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p
     return w;
   };
 
+  if (p.partials_mode != 2 && n > 16 && n > kAhead) {
+    // a long row: ask L2 for the partials of its later splits now, so the
+    // batches after the first find them there (the fold order is unchanged)
+    for (int i = kAhead + lane; i < n; i += 32) {
+      const int pair = i < nfull ? info.x + i : info.y;
+      const size_t e = (size_t)pair * p.H + h;
+      asm volatile("cp.async.bulk.prefetch.L2.global [%0], %1;" ::"l"(p.plan.acc + e * D),
+                   "r"((uint32_t)(D * sizeof(float)))
+                   : "memory");
+      asm volatile("prefetch.global.L2 [%0];" ::"l"(p.plan.ml + e) : "memory");
+    }
+  }
   Fold f;
   float A[VPL];
 #pragma unroll
@@ -109,6 +117,41 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p
   }
 }
 
+// One CTA per (row of the plan's combine list, group of kWarps heads); CTAs
+// past the list's length (the host sizes the grid by an upper bound) return
+// at once, and the hardware hands out CTAs as SMs free up. kRowMajor: a 1-D
+// grid ordered row by row over the list sorted by split count -- the head
+// groups of a row are adjacent, so every long row starts in the first wave.
+// Otherwise (prefill rows of a few splits each on the split path) a 2-D
+// grid over the flat rows themselves, x the row and y the head group, which
+// measured faster there.
+template <int D, int kAhead, bool kRowMajor>
+__global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p) {
+  const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
+  if (kRowMajor) {
+    const int hg_n = (p.H + kWarps - 1) / kWarps;
+    const int k = blockIdx.x / hg_n, hg = blockIdx.x - k * hg_n;
+    if (k >= p.plan.header[kHeaderCombineRows]) return;
+    const int h = hg * kWarps + warp;
+    if (h < p.H) fold_row_head<D, kAhead>(p, p.plan.crows[k], h, lane);
+  } else {
+    // every flat row in order (no list: one dependent load less per CTA;
+    // rows that need no fold return in fold_row_head)
+    const int h = blockIdx.y * kWarps + warp;
+    if (h < p.H) fold_row_head<D, kAhead>(p, blockIdx.x, h, lane);
+  }
+}
+
+template <int D, int kAhead>
+void launch_c(const StepParams& p, long long max_rows, bool row_order, cudaStream_t s) {
+  const int hg_n = (p.H + kWarps - 1) / kWarps;
+  if (max_rows <= 0) return;
+  if (row_order)
+    combine_kernel<D, kAhead, false><<<dim3((unsigned)max_rows, hg_n), kWarps * 32, 0, s>>>(p);
+  else
+    combine_kernel<D, kAhead, true><<<(unsigned)(max_rows * hg_n), kWarps * 32, 0, s>>>(p);
+}
+
 }  // namespace
 
 // Load depth per warp against resident warps: decode rows with long split
@@ -116,20 +159,24 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p
 // path (the row-invariant mode), most folded rows have a few splits and a
 // depth of 2 goes faster: 32 registers a thread admit 8 CTAs per SM where
 // depth 8 admits 3.
+// Rows that can need a fold: when only decode lanes take the split path, at
+// most one row per lane; otherwise every row. When prefill rows take the
+// split path the grid walks the flat rows, else the plan's sorted list.
 cudaError_t launch_combine(const StepParams& p, cudaStream_t s) {
   if (p.T <= 0) return cudaSuccess;
-  dim3 grid(p.T, (p.H + kWarps - 1) / kWarps);
+  const long long max_rows = (p.split_all_rows || p.partials_mode) ? p.T : (p.B < p.T ? p.B : p.T);
+  const bool row_order = p.split_all_rows && p.max_q_len >= 2 && !p.partials_mode;
   const bool shallow = p.split_all_rows && p.max_q_len >= 2;
   if (p.D == 128) {
     if (shallow)
-      combine_kernel<128, 2><<<grid, kWarps * 32, 0, s>>>(p);
+      launch_c<128, 2>(p, max_rows, row_order, s);
     else
-      combine_kernel<128, 8><<<grid, kWarps * 32, 0, s>>>(p);
+      launch_c<128, 8>(p, max_rows, row_order, s);
   } else {
     if (shallow)
-      combine_kernel<64, 2><<<grid, kWarps * 32, 0, s>>>(p);
+      launch_c<64, 2>(p, max_rows, row_order, s);
     else
-      combine_kernel<64, 8><<<grid, kWarps * 32, 0, s>>>(p);
+      launch_c<64, 8>(p, max_rows, row_order, s);
   }
   return cudaGetLastError();
 }

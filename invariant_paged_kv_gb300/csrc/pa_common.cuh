@@ -46,6 +46,10 @@ constexpr long long kWaitCycles = 2000000000LL;
 //   pairs[capacity - 1 - (k - header[1])], see pair_slot)
 //   row_info[r] = {first full pair, tail pair or -1, number of splits, lane or -1}
 //   pairs[k]    = {row, split index, lane, key count of the row}
+//   crows[k]    = the k-th row the combine folds (rows with 2 or more
+//                 splits -- every split row when merging KV-parallel
+//                 owners), most splits first; header[kHeaderCombineRows] of
+//                 them (not kept when prefill rows take the split path)
 //   ptiles[i]   = {lane, index t of the pair of 128-row q tiles 2 t and
 //                 2 t + 1, position of the pair's last row, 0}, heaviest
 //                 first (tensor-core prefill path)
@@ -60,6 +64,7 @@ struct SplitPlan {
   int4* ptiles;
   int4* ptiles_tmp;  // unsorted list, scratch of the plan
   int4* pairs;
+  int* crows;  // flat rows whose splits the combine folds, most splits first
   float2* ml;
   float* acc;
   int capacity;        // pairs the workspace holds
@@ -77,6 +82,8 @@ constexpr int kHeaderSplitKeys = 4 + 2 * kItemCounters;
 constexpr int kHeaderPrefillWork = kHeaderSplitKeys + 2;
 // prefill-role CTAs of the mixed-step kernel, chosen by the plan builder
 constexpr int kHeaderPrefillCtas = kHeaderPrefillWork + 2;
+// rows the combine folds (the length of crows)
+constexpr int kHeaderCombineRows = kHeaderPrefillCtas + 1;
 __device__ __forceinline__ long long* header_total(const SplitPlan& pl, int at) {
   return reinterpret_cast<long long*>(pl.header + at);
 }

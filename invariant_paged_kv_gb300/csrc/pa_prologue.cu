@@ -399,7 +399,75 @@ __device__ void build_plan(const StepParams& p) {
   } else {
     for (int i = tid; i < n; i += nth) pl.ptiles[i] = pl.ptiles_tmp[i];
   }
+  // rows the combine folds, the most splits first (decode rows: the
+  // batch-invariant mode, e4m3 and fp32 decode steps, KV-parallel merges), by
+  // a counting sort over the split counts, so every long row's fold starts in
+  // the combine's first wave. (When prefill rows take the split path the
+  // combine walks the flat rows instead and no list is kept.) The order
+  // decides only when a fold runs, never its bits: each (row, head) is folded
+  // by one warp in split order.
+  __shared__ int s_bucket[kMaxSplits + 1];
+  __shared__ int s_ncomb;
+  const int min_n = p.partials_mode == 2 ? 1 : 2;  // merging owners folds every split row
+  // when only decode lanes take the split path, a lane's one candidate is
+  // its row 0 (if q_len == 1): walk lanes instead of rows
+  const bool by_lane = !p.split_all_rows && !p.partials_mode;
+  const int nunits = by_lane ? p.B : p.T;
+  auto row_of = [&](int u) -> int {
+    if (!by_lane) return u;
+    if (lc && !lc->ok[u]) return -1;
+    const int c0 = lc ? lc->cu[u] : p.cu_seqlens[u];
+    const int c1 = lc ? lc->cu[u + 1] : p.cu_seqlens[u + 1];
+    return (c1 - c0 == 1 && c0 >= 0 && c0 < p.T) ? c0 : -1;
+  };
+  auto bucket_of = [&](int r) -> int {
+    if (r < 0) return -1;
+    const int4 ri = pl.row_info[r];
+    return (!overflow && ri.w >= 0 && ri.z >= min_n) ? min(ri.z, kMaxSplits) : -1;
+  };
+  const bool listed = !(p.split_all_rows && p.max_q_len >= 2 && !p.partials_mode);
+  if (listed) {  // (uniform across the CTA)
+    for (int i = tid; i <= kMaxSplits; i += nth) s_bucket[i] = 0;
+    __syncthreads();  // (also orders every row_info write above before the reads below)
+    for (int u = tid; u < nunits; u += nth) {
+      const int b = bucket_of(row_of(u));
+      if (b >= 0) atomicAdd(&s_bucket[b], 1);
+    }
+    __syncthreads();
+    if (tid < 32) {
+      // exclusive scan over the buckets in descending order: lane l holds
+      // positions 5 l .. 5 l + 4 of that order (bucket kMaxSplits - position)
+      constexpr int kPer = (kMaxSplits + 1 + 31) / 32;
+      int v[kPer], sum = 0;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int pos = tid * kPer + j;
+        v[j] = pos <= kMaxSplits ? s_bucket[kMaxSplits - pos] : 0;
+        sum += v[j];
+      }
+      int inc = sum;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const int x = __shfl_up_sync(0xffffffffu, inc, o);
+        if (tid >= o) inc += x;
+      }
+      int run = inc - sum;
+#pragma unroll
+      for (int j = 0; j < kPer; ++j) {
+        const int pos = tid * kPer + j;
+        if (pos <= kMaxSplits) s_bucket[kMaxSplits - pos] = run;
+        run += v[j];
+      }
+      if (tid == 31) s_ncomb = inc;
+    }
+    __syncthreads();
+    for (int u = tid; u < nunits; u += nth) {
+      const int r = row_of(u), b = bucket_of(r);
+      if (b >= 0) pl.crows[atomicAdd(&s_bucket[b], 1)] = r;
+    }
+  }
   if (tid == 0) {
+    pl.header[kHeaderCombineRows] = listed ? s_ncomb : 0;
     pl.header[0] = overflow ? 0 : (int)(nfull + total[2]);
     pl.header[1] = overflow ? 0 : (int)nfull;
     pl.header[2] = n;
