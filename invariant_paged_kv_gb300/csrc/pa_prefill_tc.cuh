@@ -165,20 +165,21 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
   const uint32_t sQ = base + L::kQ, sK0 = base + L::kK0, sV0 = base + L::kV0;
   const uint32_t bq = smem_u32(&bars.q), bqe = smem_u32(&bars.qempty);
   auto bvt = [&](uint32_t st) -> uint32_t { return smem_u32(&bars.vtail[st]); };
-  uint32_t bkf[kStages], bke[kStages], bvf[kStages], bve[kStages];
-#pragma unroll
-  for (int i = 0; i < kStages; ++i) {
-    bkf[i] = smem_u32(&bars.kfull[i]);
-    bke[i] = smem_u32(&bars.kempty[i]);
-    bvf[i] = smem_u32(&bars.vfull[i]);
-    bve[i] = smem_u32(&bars.vempty[i]);
-  }
+  // ring barriers by stage: address arithmetic, not arrays (an array
+  // indexed by a run-time stage lives in local memory, and every local load
+  // waits ~150 cycles behind the tensor core's shared-memory reads)
+  const uint32_t bkf0 = smem_u32(&bars.kfull[0]), bke0 = smem_u32(&bars.kempty[0]);
+  const uint32_t bvf0 = smem_u32(&bars.vfull[0]), bve0 = smem_u32(&bars.vempty[0]);
+  auto bkf = [&](uint32_t i) -> uint32_t { return bkf0 + 8u * i; };
+  auto bke = [&](uint32_t i) -> uint32_t { return bke0 + 8u * i; };
+  auto bvf = [&](uint32_t i) -> uint32_t { return bvf0 + 8u * i; };
+  auto bve = [&](uint32_t i) -> uint32_t { return bve0 + 8u * i; };
   if (threadIdx.x == 0) {
     for (int i = 0; i < kStages; ++i) {
-      mbar_init(bkf[i], 1);
-      mbar_init(bke[i], 1);
-      mbar_init(bvf[i], 1);
-      mbar_init(bve[i], 1);
+      mbar_init(bkf(i), 1);
+      mbar_init(bke(i), 1);
+      mbar_init(bvf(i), 1);
+      mbar_init(bve(i), 1);
     }
     mbar_init(bq, 1);
     mbar_init(bqe, 1);
@@ -231,7 +232,9 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
   const float c2 = p.scale_log2;  // > 0 (validated on the host)
   // running use counters, identical in every role: K/V ring fills, key tiles
   // of each stream, items with a tail key tile
-  uint32_t n_item = 0, n_kv = 0, n_t[2] = {0, 0}, n_tail[kStages] = {0, 0};
+  // (n_t0 / n_t1: key tiles of stream 0 / 1; tail_par: bit st = parity of
+  // the next tail use of V stage st)
+  uint32_t n_item = 0, n_kv = 0, n_t0 = 0, n_t1 = 0, tail_par = 0;
 
   if (warp == 9) {
     // -------------------------------- producer ------------------------------
@@ -256,11 +259,14 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
       if (n >= 1 && !wait_or_abort(bqe, (n - 1) & 1, ab, p.status, lim)) break;
       if (lane == 0) {
         mbar_expect_tx(bq, it.nst * L::kQBytes);
-        for (int s = 0; s < it.nst; ++s)
 #pragma unroll
-          for (int h = 0; h < L::kHalves; ++h)
-            tma_load_3d(sQ + s * L::kQBytes + h * L::kHalfBytes, tmQ, h * 64, it.head,
-                        it.cu0 + it.row0[s], bq);
+        for (int s = 0; s < 2; ++s)
+          if (s < it.nst) {
+#pragma unroll
+            for (int h = 0; h < L::kHalves; ++h)
+              tma_load_3d(sQ + s * L::kQBytes + h * L::kHalfBytes, tmQ, h * 64, it.head,
+                          it.cu0 + it.row0[s], bq);
+          }
       }
       bool ok = true;
       for (int kt = 0; ok && kt < it.nkt; ++kt) {
@@ -278,31 +284,31 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         const uint32_t bytes = (uint32_t)nchunk * L::kHalves * kChunk * 128;
         // lane c (< nchunk) copies chunk c: the boxes go out in parallel
         const int tok = blk * p.bs + (key0 + lane * kChunk) % p.bs;
-        ok = use < 1 || wait_or_abort(bke[st], (use - 1) & 1, ab, p.status, lim);
+        ok = use < 1 || wait_or_abort(bke(st), (use - 1) & 1, ab, p.status, lim);
         if (!ok) break;
-        if (lane == 0) mbar_expect_tx(bkf[st], bytes);
+        if (lane == 0) mbar_expect_tx(bkf(st), bytes);
         __syncwarp();
         if (lane < nchunk) {
 #pragma unroll
           for (int h = 0; h < L::kHalves; ++h)
             tma_load_3d(sK0 + st * L::kKBytes + h * L::kKHalfBytes + lane * kChunk * 128, tmK,
-                        h * 64, it.kvh, tok, bkf[st]);
+                        h * 64, it.kvh, tok, bkf(st));
         }
-        ok = use < 1 || wait_or_abort(bve[st], (use - 1) & 1, ab, p.status, lim);
+        ok = use < 1 || wait_or_abort(bve(st), (use - 1) & 1, ab, p.status, lim);
         if (!ok) break;
-        if (lane == 0) mbar_expect_tx(bvf[st], bytes);
+        if (lane == 0) mbar_expect_tx(bvf(st), bytes);
         __syncwarp();
         if (lane < nchunk) {
 #pragma unroll
           for (int h = 0; h < L::kHalves; ++h)
             tma_load_3d(sV0 + st * L::kVBytes + h * L::kKHalfBytes + lane * kChunk * 128, tmV,
-                        h * 64, it.kvh, tok, bvf[st]);
+                        h * 64, it.kvh, tok, bvf(st));
         }
         if (kt == it.nkt - 1 && tail) {
           // keys past the lane's end: once the tile has landed, zero their V
           // rows (stale bytes must not meet p = 0 as 0 * NaN); the MMA warp
           // takes this tile from the vtail barrier
-          ok = wait_or_abort(bvf[st], use & 1, ab, p.status, lim);
+          ok = wait_or_abort(bvf(st), use & 1, ab, p.status, lim);
           if (!ok) break;
           const int first = it.ctx - key0;
           const int n16 = (kKeys - first) * 8 * L::kHalves;
@@ -364,17 +370,19 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
       // this S overwrites, has finished
       {
         const uint32_t f = n_kv, st = f % kStages;
-        ok = wait_or_abort(bkf[st], (f / kStages) & 1, ab, p.status, lim) &&
+        ok = wait_or_abort(bkf(st), (f / kStages) & 1, ab, p.status, lim) &&
              wait_or_abort(bq, n_item & 1, ab, p.status, lim);
-        for (int s = 0; ok && s < it.nst; ++s) {
-          if (n_t[s] > 0) ok = wait_or_abort(bO(s, n_t[s] - 1), ((n_t[s] - 1) >> 1) & 1, ab,
-                                             p.status, lim);
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (!ok || s >= it.nst) break;
+          const uint32_t nts = s ? n_t1 : n_t0;
+          if (nts > 0) ok = wait_or_abort(bO(s, nts - 1), ((nts - 1) >> 1) & 1, ab, p.status, lim);
           if (!ok) break;
           tc_fence_after();
           issue_s(s, 0);
         }
         if (!ok) break;
-        umma_commit_w(bke[st]);
+        umma_commit_w(bke(st));
         if (it.nkt == 1) umma_commit_w(bqe);  // every S of the item issued
       }
       for (int kt = 0; ok && kt < it.nkt; ++kt) {
@@ -382,25 +390,30 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         const bool next = kt + 1 < it.nkt;
         const uint32_t f1 = f + 1, st1 = f1 % kStages;
         // V of tile kt (the tail tile once its stale rows are zeroed)
-        ok = (kt == it.nkt - 1 && tail) ? wait_or_abort(bvt(st), n_tail[st]++ & 1, ab, p.status, lim)
-                                        : wait_or_abort(bvf[st], (f / kStages) & 1, ab,
-                                                        p.status, lim);
+        if (kt == it.nkt - 1 && tail) {
+          ok = wait_or_abort(bvt(st), (tail_par >> st) & 1, ab, p.status, lim);
+          tail_par ^= 1u << st;
+        } else {
+          ok = wait_or_abort(bvf(st), (f / kStages) & 1, ab, p.status, lim);
+        }
         if (!ok) break;
         // per stream: P V of tile kt, once its softmax has written P, then S
         // of tile kt + 1, which overwrites P of tile kt in TMEM and so waits
         // for that P V to finish; the streams alternate, so one stream's
         // softmax runs while the tensor core serves the other
         bool k_ready = false;
-        for (int s = 0; ok && s < it.nst; ++s) {
+#pragma unroll
+        for (int s = 0; s < 2; ++s) {
+          if (!ok || s >= it.nst) break;
           if (kt >= it.nkt_s[s]) continue;
-          const uint32_t ts = n_t[s] + kt;
+          const uint32_t ts = (s ? n_t1 : n_t0) + kt;
           ok = wait_or_abort(bP(s), ts & 1, ab, p.status, lim);
           if (!ok) break;
           tc_fence_after();
           issue_pv(s, kt, ts);
           if (kt + 1 >= it.nkt_s[s]) continue;
           if (!k_ready) {
-            ok = wait_or_abort(bkf[st1], (f1 / kStages) & 1, ab, p.status, lim);
+            ok = wait_or_abort(bkf(st1), (f1 / kStages) & 1, ab, p.status, lim);
             k_ready = true;
           }
           ok = ok && wait_or_abort(bO(s, ts), (ts >> 1) & 1, ab, p.status, lim);
@@ -411,13 +424,13 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         if (!ok) break;
         // Q is free once the item's last S products finish (tile nkt - 1's)
         if (kt + 2 == it.nkt) umma_commit_w(bqe);
-        umma_commit_w(bve[st]);
-        if (next) umma_commit_w(bke[st1]);
+        umma_commit_w(bve(st));
+        if (next) umma_commit_w(bke(st1));
       }
       if (!ok) break;
       n_kv += it.nkt;
-      n_t[0] += it.nkt_s[0];
-      n_t[1] += it.nkt_s[1];
+      n_t0 += it.nkt_s[0];
+      n_t1 += it.nkt_s[1];
     }
   } else {
     // -------------------------------- softmax rows --------------------------
@@ -431,12 +444,17 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
       if (!read_item(n_item, item) || item >= n_items) break;
       const ItemInfo it = item_info(p, (int)item);
       if (s >= it.nst) continue;  // the pair has no second tile
-      const int pos = it.p_first[s] + min(r, it.nrows[s] - 1);
+      // this stream's values as scalars (selects, not a run-time index)
+      const int nkt_s = s ? it.nkt_s[1] : it.nkt_s[0];
+      const int nrows = s ? it.nrows[1] : it.nrows[0];
+      const int row0 = s ? it.row0[1] : it.row0[0];
+      const uint32_t nts = s ? n_t1 : n_t0;
+      const int pos = (s ? it.p_first[1] : it.p_first[0]) + min(r, nrows - 1);
       float m = -INFINITY, l = 0.f;
       bool ok = true;
 #pragma unroll 1
-      for (int kt = 0; kt < it.nkt_s[s]; ++kt) {
-        const uint32_t th = n_t[s] + kt;
+      for (int kt = 0; kt < nkt_s; ++kt) {
+        const uint32_t th = nts + kt;
         if (!wait_or_abort(bS(s), th & 1, ab, p.status, lim)) { ok = false; break; }
         tc_fence_after();
         const int lim_c = pos - kt * kKeys;  // columns c <= lim_c are visible to this row
@@ -557,13 +575,13 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
       // the row's output once its last P V has finished; the next item's
       // first P V (which restarts O) waits for this group's first P of that
       // item, which comes after these reads
-      const uint32_t last = n_t[s] + it.nkt_s[s] - 1;
+      const uint32_t last = nts + nkt_s - 1;
       if (!wait_or_abort(bO(s, last), (last >> 1) & 1, ab, p.status, lim)) break;
       tc_fence_after();
-      const bool valid = r < it.nrows[s];
+      const bool valid = r < nrows;
       const float inv_l = 1.f / l;  // one division per row; out = O * (1 / l)
       __nv_bfloat16* out = static_cast<__nv_bfloat16*>(p.out) +
-                           ((size_t)(it.cu0 + it.row0[s] + r) * p.H + it.head) * D;
+                           ((size_t)(it.cu0 + row0 + r) * p.H + it.head) * D;
 #pragma unroll 1
       for (int c = 0; c < D / 32; ++c) {
         uint32_t ov[32];
@@ -582,7 +600,7 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         }
       }
       tc_fence_before();
-      n_t[s] += it.nkt_s[s];
+      if (s) n_t1 += nkt_s; else n_t0 += nkt_s;
     }
   }
   // before TMEM is released and the CTA leaves: every product the MMA warp
@@ -596,8 +614,8 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
   if (warp == 9 && lane == 0) {
     if (n_item > 0) mbar_wait_bounded(bq, (n_item - 1) & 1, lim);
     for (uint32_t f = n_kv > kStages ? n_kv - kStages : 0; f < n_kv; ++f) {
-      mbar_wait_bounded(bkf[f % kStages], (f / kStages) & 1, lim);
-      mbar_wait_bounded(bvf[f % kStages], (f / kStages) & 1, lim);
+      mbar_wait_bounded(bkf(f % kStages), (f / kStages) & 1, lim);
+      mbar_wait_bounded(bvf(f % kStages), (f / kStages) & 1, lim);
     }
   }
   __syncthreads();
