@@ -254,6 +254,15 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
       if (item >= n_items) break;
       const ItemInfo it = item_info(p, (int)item);
       const bool tail = it.nkt * kKeys > it.ctx;  // only the last key tile can run past ctx
+      // block ids of key tile kt (lane c < 8: chunk c), loaded one tile ahead
+      // so the global load's latency passes while the ring waits and copies
+      auto load_blk = [&](int kt) -> int {
+        const int key0 = kt * kKeys;
+        const int nch = min(kKeys / kChunk, (it.ctx - key0 + kChunk - 1) / kChunk);
+        return lane < nch ? p.block_tables[(size_t)it.lane * p.max_blocks + (key0 + lane * kChunk) / p.bs]
+                          : 0;
+      };
+      int blk_next = load_blk(0);
       // Q of this item's streams, once every S product of the previous item
       // (which read this buffer) has finished
       if (n >= 1 && !wait_or_abort(bqe, (n - 1) & 1, ab, p.status, lim)) break;
@@ -273,13 +282,11 @@ __device__ __forceinline__ void prefill_tc_cta(const StepParams& p, const CUtens
         const uint32_t f = n_kv + kt, st = f % kStages, use = f / kStages;
         const int key0 = kt * kKeys;
         const int nchunk = min(kKeys / kChunk, (it.ctx - key0 + kChunk - 1) / kChunk);
-        int blk = 0;  // block id of chunk `lane` (lanes 0..7)
-        if (lane < nchunk) {
-          blk = p.block_tables[(size_t)it.lane * p.max_blocks + (key0 + lane * kChunk) / p.bs];
-          if (blk < 0 || blk >= p.NB) {
-            raise_flag(p.status, PA_FLAG_BLOCK_RANGE);
-            blk = 0;
-          }
+        int blk = blk_next;  // block id of chunk `lane` (lanes 0..7)
+        if (kt + 1 < it.nkt) blk_next = load_blk(kt + 1);
+        if (lane < nchunk && (blk < 0 || blk >= p.NB)) {
+          raise_flag(p.status, PA_FLAG_BLOCK_RANGE);
+          blk = 0;
         }
         const uint32_t bytes = (uint32_t)nchunk * L::kHalves * kChunk * 128;
         // lane c (< nchunk) copies chunk c: the boxes go out in parallel
