@@ -107,7 +107,7 @@ Layout layout_for(int32_t B, int32_t T, int32_t H, int32_t D) {
   L.ptiles = L.row_info + align_up((size_t)T * sizeof(int4));
   L.ptiles_tmp = L.ptiles + align_up((size_t)L.ptile_capacity * sizeof(int4));
   L.crows = L.ptiles_tmp + align_up((size_t)L.ptile_capacity * sizeof(int4));
-  L.pairs = L.crows + align_up((size_t)T * sizeof(int));
+  L.pairs = L.crows + align_up((size_t)T * sizeof(int4));
   L.fixed = L.pairs;
   L.per_pair = sizeof(int4) + (size_t)H * sizeof(float2) + (size_t)H * D * sizeof(float);
   return L;
@@ -155,7 +155,7 @@ SplitPlan carve(void* ws, int cap, int32_t B, int32_t T, int32_t H, int32_t D) {
   pl.ptiles = reinterpret_cast<int4*>(b + L.ptiles);
   pl.ptiles_tmp = reinterpret_cast<int4*>(b + L.ptiles_tmp);
   pl.ptile_capacity = L.ptile_capacity;
-  pl.crows = reinterpret_cast<int*>(b + L.crows);
+  pl.crows = reinterpret_cast<int4*>(b + L.crows);
   size_t off = L.pairs;
   pl.pairs = reinterpret_cast<int4*>(b + off);
   off += align_up((size_t)cap * sizeof(int4));
@@ -200,7 +200,7 @@ SplitPlan carve_partials(void* ws, size_t ws_bytes, void* partials, int32_t B, i
   pl.ptiles = reinterpret_cast<int4*>(b + L.ptiles);
   pl.ptiles_tmp = reinterpret_cast<int4*>(b + L.ptiles_tmp);
   pl.ptile_capacity = L.ptile_capacity;
-  pl.crows = reinterpret_cast<int*>(b + L.crows);
+  pl.crows = reinterpret_cast<int4*>(b + L.crows);
   pl.pairs = reinterpret_cast<int4*>(b + L.pairs);
   long long cap = ws_bytes > L.fixed ? (long long)((ws_bytes - L.fixed) / sizeof(int4)) : 0;
   pl.capacity = (int)(cap > 0x7fffffffLL ? 0x7fffffffLL : cap);

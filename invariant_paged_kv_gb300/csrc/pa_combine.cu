@@ -25,11 +25,12 @@ constexpr int kWarps = 8;  // heads per CTA (one warp per (row, head))
 // (D = 128) or 2l .. 2l+1 (D = 64). The loads of kAhead splits are issued
 // before their fold so the memory system sees many requests at once; the fold
 // itself runs strictly in split order, so kAhead changes no bit.
+// info: the row's row_info (its lane is read only when merging owners).
 template <int D, int kAhead>
-__device__ __forceinline__ void fold_row_head(const StepParams& p, int row, int h, int lane) {
+__device__ __forceinline__ void fold_row_head(const StepParams& p, int row, int4 info, int h,
+                                              int lane) {
   constexpr int VPL = D / 32;  // values per lane
   using Vec = typename std::conditional<VPL == 4, float4, float2>::type;
-  const int4 info = p.plan.row_info[row];
   if (info.w < 0) return;                                  // not on the split path
   if (p.partials_mode != 2 && info.z <= 1) return;         // written directly
   const int n = info.z;
@@ -131,14 +132,20 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p
   if (kRowMajor) {
     const int hg_n = (p.H + kWarps - 1) / kWarps;
     const int k = blockIdx.x / hg_n, hg = blockIdx.x - k * hg_n;
+    // the entry is read before the list's length is known (k < the grid's
+    // row bound <= T entries, so in bounds; used only if k is listed): the
+    // two loads travel together
+    const int4 c = p.plan.crows[k];
     if (k >= p.plan.header[kHeaderCombineRows]) return;
     const int h = hg * kWarps + warp;
-    if (h < p.H) fold_row_head<D, kAhead>(p, p.plan.crows[k], h, lane);
+    if (h >= p.H) return;
+    const int w = p.partials_mode == 2 ? p.plan.row_info[c.x].w : 0;
+    fold_row_head<D, kAhead>(p, c.x, make_int4(c.y, c.z, c.w, w), h, lane);
   } else {
     // every flat row in order (no list: one dependent load less per CTA;
     // rows that need no fold return in fold_row_head)
     const int h = blockIdx.y * kWarps + warp;
-    if (h < p.H) fold_row_head<D, kAhead>(p, blockIdx.x, h, lane);
+    if (h < p.H) fold_row_head<D, kAhead>(p, blockIdx.x, p.plan.row_info[blockIdx.x], h, lane);
   }
 }
 

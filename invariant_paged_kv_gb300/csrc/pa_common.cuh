@@ -46,10 +46,13 @@ constexpr long long kWaitCycles = 2000000000LL;
 //   pairs[capacity - 1 - (k - header[1])], see pair_slot)
 //   row_info[r] = {first full pair, tail pair or -1, number of splits, lane or -1}
 //   pairs[k]    = {row, split index, lane, key count of the row}
-//   crows[k]    = the k-th row the combine folds (rows with 2 or more
+//   crows[k]    = {row, first full pair, tail pair or -1, number of splits}
+//                 of the k-th row the combine folds (rows with 2 or more
 //                 splits -- every split row when merging KV-parallel
 //                 owners), most splits first; header[kHeaderCombineRows] of
-//                 them (not kept when prefill rows take the split path)
+//                 them (not kept when prefill rows take the split path).
+//                 The entry repeats the row's row_info so a combine warp
+//                 reaches its partials with one dependent load less.
 //   ptiles[i]   = {lane, index t of the pair of 128-row q tiles 2 t and
 //                 2 t + 1, position of the pair's last row, 0}, heaviest
 //                 first (tensor-core prefill path)
@@ -64,7 +67,7 @@ struct SplitPlan {
   int4* ptiles;
   int4* ptiles_tmp;  // unsorted list, scratch of the plan
   int4* pairs;
-  int* crows;  // flat rows whose splits the combine folds, most splits first
+  int4* crows;  // rows whose splits the combine folds, most splits first
   float2* ml;
   float* acc;
   int capacity;        // pairs the workspace holds

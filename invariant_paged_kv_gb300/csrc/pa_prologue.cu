@@ -463,7 +463,10 @@ __device__ void build_plan(const StepParams& p) {
     __syncthreads();
     for (int u = tid; u < nunits; u += nth) {
       const int r = row_of(u), b = bucket_of(r);
-      if (b >= 0) pl.crows[atomicAdd(&s_bucket[b], 1)] = r;
+      if (b >= 0) {
+        const int4 ri = pl.row_info[r];
+        pl.crows[atomicAdd(&s_bucket[b], 1)] = make_int4(r, ri.x, ri.y, ri.z);
+      }
     }
   }
   if (tid == 0) {
