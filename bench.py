@@ -73,6 +73,11 @@ def parse():
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-e2e", action="store_true")
     ap.add_argument("--no-clocks", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="skip the secondary workloads of the default run")
+    ap.add_argument("--no-plan-reuse", action="store_true",
+                    help="build the split plan in every layer's call instead of the first "
+                         "layer's only (PA_MODE_REUSE_PLAN for layers 2..)")
     ap.add_argument("--no-graph", action="store_true",
                     help="launch the timed steps eagerly instead of replaying a CUDA graph")
     ap.add_argument("--kv", choices=["bf16", "fp8"], default="bf16",
@@ -125,6 +130,8 @@ def workload_config(step, layers, name, args):
         "l2": "no flush: each layer's keys exceed the 129 MB L2",
         "small": bool(args.small),
         "cuda_graph": not getattr(args, "no_graph", True),
+        "plan": ("built in every layer's call" if getattr(args, "no_plan_reuse", False)
+                 else "built by the first layer's call of a step, reused by the others"),
         "invariance_mode": getattr(args, "mode", "batch"),
         "kv_cache": ("e4m3 codes, per-tensor scales k %g / v %g; f16 products, fp32 accumulate"
                      % (wl_scales()[0], wl_scales()[1])) if g.dtype == "fp8" else g.dtype,
@@ -449,7 +456,8 @@ def run_ours(args, rank, world, local_rank):
                          workspace=ws, slot_mapping=dslots if dslots is not None else slots,
                          k_new=(kn or tens["k_new"])[l], v_new=(vn or tens["v_new"])[l],
                          status=status, events=None if events is None else events[l],
-                         mode=args.mode, k_scale=wl.FP8_K_SCALE, v_scale=wl.FP8_V_SCALE)
+                         mode=args.mode, k_scale=wl.FP8_K_SCALE, v_scale=wl.FP8_V_SCALE,
+                         reuse_plan=l > 0 and not args.no_plan_reuse)
 
     def barrier():
         if world > 1:
@@ -588,7 +596,8 @@ def run_ours(args, rank, world, local_rank):
                                  O[l], max_q_len=step.max_q_len, max_ctx_len=step.max_ctx_len,
                                  scale=scale, workspace=ws, slot_mapping=dsl,
                                  k_new=B["kn"][l], v_new=B["vn"][l], status=status,
-                                 mode=args.mode, k_scale=wl.FP8_K_SCALE, v_scale=wl.FP8_V_SCALE)
+                                 mode=args.mode, k_scale=wl.FP8_K_SCALE, v_scale=wl.FP8_V_SCALE,
+                                 reuse_plan=l > 0 and not args.no_plan_reuse)
                     ev_comp[b][l].record(stream)
                     with torch.cuda.stream(ds):
                         ds.wait_event(ev_comp[b][l])
@@ -1045,7 +1054,7 @@ def main():
     else:
         line = run_ours(args, rank, world, local_rank)
         if args.workload == "long_tail" and not args.small and args.kv == "bf16" \
-                and args.mode == "batch":
+                and args.mode == "batch" and not args.no_secondary:
             line["secondary"] = run_secondary(args, rank, world, local_rank)
     if rank == 0:
         print(json.dumps(line), flush=True)

@@ -96,7 +96,36 @@ typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
  *                            chunk sizes 1, 2 and 64). fp32 and e4m3 steps
  *                            always behave this way.
  */
-typedef enum { PA_MODE_BATCH_INVARIANT = 0, PA_MODE_ROW_INVARIANT = 1 } pa_mode;
+/*
+ *   PA_MODE_REUSE_PLAN       a bit OR-ed into either mode (pass
+ *                            (pa_mode)(PA_MODE_... | PA_MODE_REUSE_PLAN)):
+ *                            the workspace already holds the split plan a
+ *                            previous pa_attention_ex call on the same
+ *                            stream built for this step -- the same B, T, H,
+ *                            Hkv, D, block size, dtype, mode, max_q_len,
+ *                            max_ctx_len and workspace size, and the same
+ *                            cu_seqlens_q and ctx_lens contents -- so the
+ *                            call does not build it again: the layers of one
+ *                            step attend over the same lanes, and only the
+ *                            first layer's call needs to plan ("P3: native
+ *                            paged-KV continuous-batching sampler", Design:
+ *                            one flat step description serves the whole
+ *                            forward pass). Everything else (the write of
+ *                            the new rows, q, the caches, block tables, out)
+ *                            is this call's own. The library checks the
+ *                            sizes on the device: on a mismatch it raises
+ *                            PA_FLAG_PLAN_MISMATCH and writes no output (the
+ *                            write of new rows still happens). Changed
+ *                            contents of cu_seqlens_q / ctx_lens are not
+ *                            detected: the caller must then plan again
+ *                            (a call without the bit). Output bits are the
+ *                            same with or without the bit.
+ */
+typedef enum {
+  PA_MODE_BATCH_INVARIANT = 0,
+  PA_MODE_ROW_INVARIANT = 1,
+  PA_MODE_REUSE_PLAN = 0x100
+} pa_mode;
 
 /* Device status word bits. */
 #define PA_FLAG_SLOT_RANGE   0x01  /* slot >= num_blocks * block_size: write skipped      */
@@ -110,6 +139,8 @@ typedef enum { PA_MODE_BATCH_INVARIANT = 0, PA_MODE_ROW_INVARIANT = 1 } pa_mode;
 #define PA_FLAG_TIMEOUT      0x80  /* a bounded wait inside a kernel gave up              */
 #define PA_FLAG_OWNER_RANGE  0x100 /* KV-parallel key ranges not split-aligned / not a
                                       partition of the lane's keys: lane skipped          */
+#define PA_FLAG_PLAN_MISMATCH 0x200 /* PA_MODE_REUSE_PLAN, but the workspace's plan was
+                                      built for other sizes: no output written            */
 
 /*
  * pa_write_kv -- scatter T new K/V rows into the caches.
@@ -170,8 +201,9 @@ size_t pa_attention_workspace_bytes(int32_t B, int32_t T, int32_t max_q_len,
  * pa_attention_workspace_bytes_ex -- the same for an invariance mode
  * (pa_attention_workspace_bytes is this with PA_MODE_BATCH_INVARIANT). In
  * PA_MODE_ROW_INVARIANT every row holds split partials, so the bound is
- * T * ceil(max_ctx_len / 512) (row, split) pairs. Returns 0 for unsupported
- * arguments or an unknown mode.
+ * T * ceil(max_ctx_len / 512) (row, split) pairs. The PA_MODE_REUSE_PLAN bit
+ * changes nothing here. Returns 0 for unsupported arguments or an unknown
+ * mode.
  */
 size_t pa_attention_workspace_bytes_ex(int32_t B, int32_t T, int32_t max_q_len,
                                        int32_t max_ctx_len, int64_t total_ctx, int32_t H,
@@ -239,9 +271,10 @@ pa_status pa_attention(const void* q, const void* k_cache, const void* v_cache,
  *             take the split path for every row (as fp32 steps do), so they
  *             are row invariant in either mode; scores use
  *             scale * k_scale and every output is multiplied by v_scale.
- *   mode      see pa_mode; an unknown value returns PA_ERR_INVALID_ARG. The
- *             workspace must hold what pa_attention_workspace_bytes_ex
- *             returns for the same mode.
+ *   mode      see pa_mode: an invariance mode, optionally with the
+ *             PA_MODE_REUSE_PLAN bit; any other value returns
+ *             PA_ERR_INVALID_ARG. The workspace must hold what
+ *             pa_attention_workspace_bytes_ex returns for the same mode.
  *   events    array of n_events cudaEvent_t handles (may be NULL / 0). They
  *             are recorded on `stream` in this order, as far as n_events
  *             reaches: [0] before the first launch, [1] after the write +

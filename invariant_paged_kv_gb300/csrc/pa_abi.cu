@@ -12,7 +12,7 @@
 
 namespace pa {
 
-cudaError_t launch_prologue(const StepParams& p, bool plan, bool write, cudaStream_t s);
+cudaError_t launch_prologue(const StepParams& p, int plan_mode, bool write, cudaStream_t s);
 cudaError_t launch_decode_bf16(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
                                long long max_items, cudaStream_t s);
 cudaError_t launch_decode_fp8(const StepParams& p, const CUtensorMap& k, const CUtensorMap& v,
@@ -87,8 +87,16 @@ bool split_all_rows(pa_dtype dtype, pa_mode mode) {
   return dtype != PA_BF16 || mode == PA_MODE_ROW_INVARIANT;
 }
 
+// The invariance mode of a pa_mode value (the PA_MODE_REUSE_PLAN bit taken off).
+pa_mode invariance_of(pa_mode mode) {
+  return static_cast<pa_mode>(static_cast<int>(mode) & ~static_cast<int>(PA_MODE_REUSE_PLAN));
+}
+bool reuses_plan(pa_mode mode) {
+  return (static_cast<int>(mode) & static_cast<int>(PA_MODE_REUSE_PLAN)) != 0;
+}
 bool mode_known(pa_mode mode) {
-  return mode == PA_MODE_BATCH_INVARIANT || mode == PA_MODE_ROW_INVARIANT;
+  const pa_mode m = invariance_of(mode);
+  return m == PA_MODE_BATCH_INVARIANT || m == PA_MODE_ROW_INVARIANT;
 }
 
 // Prefill tiles a step can hold: sum over lanes of ceil(q_len / 128).
@@ -371,7 +379,7 @@ pa_status pa_write_kv_scaled(const void* k_new, const void* v_new, void* k_cache
   p.kv_fp8 = fp8 ? 1 : 0;
   p.k_scale = fp8 ? k_scale : 1.f;
   p.v_scale = fp8 ? v_scale : 1.f;
-  cudaError_t e = launch_prologue(p, false, true, static_cast<cudaStream_t>(stream));
+  cudaError_t e = launch_prologue(p, 0, true, static_cast<cudaStream_t>(stream));
   if (e != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
   return PA_OK;
@@ -382,6 +390,7 @@ size_t pa_attention_workspace_bytes_ex(int32_t B, int32_t T, int32_t max_q_len,
                                        int32_t Hkv, int32_t D, int32_t block_size,
                                        pa_dtype dtype, pa_mode mode) {
   if (B < 0 || T < 0 || max_q_len < 0 || max_ctx_len < 0 || !mode_known(mode)) return 0;
+  mode = invariance_of(mode);
   if (check_geometry(H, Hkv, D, block_size, dtype) != PA_OK) return 0;
   const long long pairs = max_pairs(B, T, max_ctx_len, total_ctx, dtype, mode);
   return bytes_for_pairs(B, T, H, D, pairs > 0 ? pairs : 1);
@@ -409,6 +418,8 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
   if (B < 0 || T < 0 || num_blocks <= 0 || max_q_len < 0 || max_ctx_len < 0 || n_events < 0 ||
       !mode_known(mode))
     return PA_ERR_INVALID_ARG;
+  const bool reuse = reuses_plan(mode);
+  mode = invariance_of(mode);
   pa_status g = check_geometry(H, Hkv, D, block_size, dtype);
   if (g != PA_OK) return g;
   if (!std::isfinite(scale) || !(scale > 0.f)) return PA_ERR_INVALID_ARG;
@@ -493,7 +504,7 @@ pa_status pa_attention_ex(const void* q, const void* k_cache, const void* v_cach
   items *= Hkv;
 
   if (record(events, n_events, 0, s) != PA_OK) return PA_ERR_CUDA;
-  if (launch_prologue(p, true, with_write, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_prologue(p, reuse ? 2 : 1, with_write, s) != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
   if (record(events, n_events, 1, s) != PA_OK) return PA_ERR_CUDA;
   // steps with prefill chunks on the tensor cores run decode and prefill in
@@ -619,7 +630,7 @@ pa_status pa_attention_partials(const void* q, const void* k_cache, const void* 
   if (items > p.plan.capacity) items = p.plan.capacity;
   items *= Hkv;
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_prologue(p, true, false, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_prologue(p, 1, false, s) != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
   cudaError_t e = fp8 ? launch_decode_fp8(p, tmK, tmV, items, s)
                       : dtype == PA_BF16 ? launch_decode_bf16(p, tmK, tmV, items, s)
@@ -677,7 +688,7 @@ pa_status pa_merge_partials(const void* partials, size_t partials_bytes, int32_t
   p.plan = carve_partials(workspace, workspace_bytes, const_cast<void*>(partials), B, T, H,
                           max_ctx_len);
   cudaStream_t s = static_cast<cudaStream_t>(stream);
-  if (launch_prologue(p, true, false, s) != cudaSuccess) return PA_ERR_CUDA;
+  if (launch_prologue(p, 1, false, s) != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);
   if (launch_combine(p, s) != cudaSuccess) return PA_ERR_CUDA;
   count_launches(1);

@@ -128,6 +128,7 @@ __device__ __forceinline__ void fold_row_head(const StepParams& p, int row, int4
 // measured faster there.
 template <int D, int kAhead, bool kRowMajor>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p) {
+  if (!plan_ok(p)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (kRowMajor) {
     const int hg_n = (p.H + kWarps - 1) / kWarps;

@@ -87,6 +87,14 @@ constexpr int kHeaderPrefillWork = kHeaderSplitKeys + 2;
 constexpr int kHeaderPrefillCtas = kHeaderPrefillWork + 2;
 // rows the combine folds (the length of crows)
 constexpr int kHeaderCombineRows = kHeaderPrefillCtas + 1;
+// 1 when the plan in the workspace was built for this call's sizes (the
+// builder sets it; a call that reuses the plan sets it from the fingerprint
+// check); every kernel after the prologue does nothing when it is 0
+constexpr int kHeaderPlanOk = kHeaderCombineRows + 1;
+// the sizes the plan was built for (plan_fingerprint), compared by calls
+// that reuse it
+constexpr int kHeaderFingerprint = kHeaderPlanOk + 1;
+constexpr int kFingerprintInts = 14;
 __device__ __forceinline__ long long* header_total(const SplitPlan& pl, int at) {
   return reinterpret_cast<long long*>(pl.header + at);
 }
@@ -157,6 +165,34 @@ struct StepParams {
   long long owner_stride;       // bytes between owners' buffers
   SplitPlan plan;
 };
+
+// Whether the plan in the workspace belongs to this call (see kHeaderPlanOk);
+// uniform across the grid, so a kernel tests it once at entry.
+__device__ __forceinline__ bool plan_ok(const StepParams& p) {
+  return p.plan.header[kHeaderPlanOk] != 0;
+}
+
+// Entry i < kFingerprintInts of the sizes a split plan depends on (besides
+// the contents of cu_seqlens_q and ctx_lens, which a caller that reuses the
+// plan vouches for).
+__device__ __forceinline__ int plan_fingerprint(const StepParams& p, int i) {
+  switch (i) {
+    case 0: return p.B;
+    case 1: return p.T;
+    case 2: return p.H;
+    case 3: return p.Hkv;
+    case 4: return p.D;
+    case 5: return p.bs;
+    case 6: return p.elem_bytes;
+    case 7: return p.split_all_rows;
+    case 8: return p.group_rows;
+    case 9: return p.max_q_len;
+    case 10: return p.max_ctx_len;
+    case 11: return p.plan.capacity;
+    case 12: return p.sm_count;
+    default: return p.partials_mode * 4 + p.kv_fp8;
+  }
+}
 
 // Canonical partial entry of (row, split) in the KV-parallel modes, else the
 // pair's own slot.

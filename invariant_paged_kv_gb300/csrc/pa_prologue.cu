@@ -469,7 +469,9 @@ __device__ void build_plan(const StepParams& p) {
       }
     }
   }
+  if (tid < kFingerprintInts) pl.header[kHeaderFingerprint + tid] = plan_fingerprint(p, tid);
   if (tid == 0) {
+    pl.header[kHeaderPlanOk] = 1;
     pl.header[kHeaderCombineRows] = listed ? s_ncomb : 0;
     pl.header[0] = overflow ? 0 : (int)(nfull + total[2]);
     pl.header[1] = overflow ? 0 : (int)nfull;
@@ -551,12 +553,34 @@ __device__ void write_rows(const StepParams& p, int cta, int ncta) {
   }
 }
 
-__global__ void __launch_bounds__(1024) prologue_kernel(const StepParams p, int do_plan) {
-  if (do_plan && blockIdx.x == 0) {
-    build_plan(p);
+// A call that reuses the plan already in the workspace: the plan is valid
+// for it when the sizes it was built for match this call's; then only the
+// item counters, which the kernels consume, are reset. On a mismatch the
+// kernels after the prologue do nothing and PA_FLAG_PLAN_MISMATCH is raised.
+__device__ void check_plan(const StepParams& p) {
+  const SplitPlan& pl = p.plan;
+  const int tid = threadIdx.x;
+  const bool same = tid >= kFingerprintInts ||
+                    pl.header[kHeaderFingerprint + tid] == plan_fingerprint(p, tid);
+  const int ok = __syncthreads_and(same ? 1 : 0);
+  if (tid == 0) {
+    pl.header[kHeaderPlanOk] = ok;
+    if (!ok) raise_flag(p.status, PA_FLAG_PLAN_MISMATCH);
+    for (int c = 0; c < kItemCounters; ++c) *item_counter(pl, c) = 0ull;
+  }
+}
+
+// plan_mode: 0 no plan (the write alone), 1 build it, 2 check the one in
+// the workspace (CTA 0 in modes 1 and 2; the other CTAs write the new rows)
+__global__ void __launch_bounds__(1024) prologue_kernel(const StepParams p, int plan_mode) {
+  if (plan_mode && blockIdx.x == 0) {
+    if (plan_mode == 1)
+      build_plan(p);
+    else
+      check_plan(p);
     return;
   }
-  const int first = do_plan ? 1 : 0;
+  const int first = plan_mode ? 1 : 0;
   write_rows(p, blockIdx.x - first, gridDim.x - first);
 }
 
@@ -564,7 +588,7 @@ __global__ void __launch_bounds__(1024) prologue_kernel(const StepParams p, int 
 
 int num_sms();
 
-cudaError_t launch_prologue(const StepParams& p, bool plan, bool write, cudaStream_t s) {
+cudaError_t launch_prologue(const StepParams& p, int plan_mode, bool write, cudaStream_t s) {
   int write_ctas = 0;
   if (write && p.T > 0) {
     const long long vecs = (long long)p.T * (p.Hkv * p.D * p.elem_bytes / 16);  // 16-byte loads
@@ -572,9 +596,9 @@ cudaError_t launch_prologue(const StepParams& p, bool plan, bool write, cudaStre
     const long long cap = 4LL * num_sms();
     write_ctas = (int)(want < cap ? want : cap);
   }
-  const int grid = (plan ? 1 : 0) + write_ctas;
+  const int grid = (plan_mode ? 1 : 0) + write_ctas;
   if (grid == 0) return cudaSuccess;
-  prologue_kernel<<<grid, 1024, 0, s>>>(p, plan ? 1 : 0);
+  prologue_kernel<<<grid, 1024, 0, s>>>(p, plan_mode);
   return cudaGetLastError();
 }
 

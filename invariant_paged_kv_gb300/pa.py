@@ -19,12 +19,13 @@ _LIB_PATH = os.path.join(os.path.dirname(os.path.abspath(__file__)), "_lib", "li
 PA_F32, PA_BF16, PA_FP8_E4M3 = 0, 1, 2
 FP8_CACHE_DTYPES = (torch.uint8, torch.float8_e4m3fn)  # e4m3 code caches
 MODES = {"batch": 0, "row": 1}  # pa_mode: PA_MODE_BATCH_INVARIANT, PA_MODE_ROW_INVARIANT
+REUSE_PLAN = 0x100  # PA_MODE_REUSE_PLAN, OR-ed into a mode
 STATUS_NAMES = {0: "PA_OK", 1: "PA_ERR_INVALID_ARG", 2: "PA_ERR_UNSUPPORTED",
                 3: "PA_ERR_WORKSPACE", 4: "PA_ERR_CUDA"}
 FLAGS = {
     "SLOT_RANGE": 0x01, "BLOCK_RANGE": 0x02, "CTX_RANGE": 0x04, "QLEN_RANGE": 0x08,
     "CU_SEQLENS": 0x10, "WORKSPACE": 0x20, "HOST_BOUND": 0x40, "TIMEOUT": 0x80,
-    "OWNER_RANGE": 0x100,
+    "OWNER_RANGE": 0x100, "PLAN_MISMATCH": 0x200,
 }
 
 EXPORTS = ("pa_write_kv", "pa_write_kv_scaled", "pa_attention_workspace_bytes",
@@ -209,13 +210,16 @@ def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,
               max_q_len: int, max_ctx_len: int, scale: float, workspace: torch.Tensor,
               slot_mapping=None, k_new=None, v_new=None, status=None, stream=None,
               events: Optional[Sequence[torch.cuda.Event]] = None, mode: str = "batch",
-              k_scale: float = 1.0, v_scale: float = 1.0):
-    """pa_attention, or pa_attention_ex when ``events``, mode="row" or e4m3
-    caches (uint8 / float8_e4m3fn, with k_scale and v_scale) are given.
+              k_scale: float = 1.0, v_scale: float = 1.0, reuse_plan: bool = False):
+    """pa_attention, or pa_attention_ex when ``events``, mode="row", e4m3
+    caches (uint8 / float8_e4m3fn, with k_scale and v_scale) or
+    ``reuse_plan`` are given.
 
     mode "batch": a row's bits depend only on its own lane. mode "row": also
     not on its lane's q_len (every row takes the split-KV path); the
     workspace must then be sized with ``workspace_bytes(..., mode="row")``.
+    reuse_plan: the workspace holds the plan an earlier call built for this
+    very step (PA_MODE_REUSE_PLAN) -- the later layers of a step.
     """
     T, H, D = q.shape
     NB, bs, Hkv, _ = k_cache.shape
@@ -232,7 +236,7 @@ def attention(q, k_cache, v_cache, block_tables, cu_seqlens_q, ctx_lens, out, *,
             _cache_code(k_cache, q.dtype), _ptr(workspace), workspace.numel(), _ptr(status),
             _stream(stream)]
     L = load()
-    code = _mode_code(mode)
+    code = _mode_code(mode) | (REUSE_PLAN if reuse_plan else 0)
     if events is None and code == 0 and k_cache.dtype not in FP8_CACHE_DTYPES:
         _check(L.pa_attention(*args), "pa_attention")
         return

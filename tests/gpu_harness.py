@@ -32,7 +32,7 @@ def workspace_for(step: wl.Step, mode="batch"):
 
 
 def run_attention(step: wl.Step, t: dict, layer=0, write=True, scale=None, status=None,
-                  out=None, dev=None, workspace=None, mode="batch"):
+                  out=None, dev=None, workspace=None, mode="batch", reuse_plan=False):
     """One pa_attention call; returns out (device) and the status flags."""
     g = step.geom
     dev = dev or device_step(step)
@@ -49,7 +49,7 @@ def run_attention(step: wl.Step, t: dict, layer=0, write=True, scale=None, statu
                  dev["cu_seqlens_q"], dev["ctx_lens"], out,
                  max_q_len=step.max_q_len, max_ctx_len=step.max_ctx_len,
                  scale=opa.default_scale(g.D) if scale is None else scale,
-                 workspace=ws, status=st, mode=mode, **SCALES, **kw)
+                 workspace=ws, status=st, mode=mode, reuse_plan=reuse_plan, **SCALES, **kw)
     flags = pa.read_status(st)
     return out, flags
 

@@ -138,6 +138,9 @@ def test_workspace_bytes_ex_modes(lib):
     f32 = args[:-1] + (0,)
     assert f(*f32, 0) == f(*f32, 1)
     assert f(*args, 2) == 0 and f(*args, -1) == 0  # unknown mode
+    # the reuse-plan bit sizes nothing; other bits are unknown
+    assert f(*args, 0x100) == batch and f(*args, 0x101) == row
+    assert f(*args, 0x200) == 0 and f(*args, 0x102) == 0 and f(*args, 0x300) == 0
 
 
 def test_attention_ex_refuses_unknown_mode(lib):
@@ -146,6 +149,8 @@ def test_attention_ex_refuses_unknown_mode(lib):
     before = lib.pa_kernel_launches()
     assert lib.pa_attention_ex(*a, 1.0, 1.0, 2, None, 0) == 1
     assert lib.pa_attention_ex(*a, 1.0, 1.0, -1, None, 0) == 1
+    for bad in (0x200, 0x102, 0x301):  # only an invariance mode and the reuse bit are known
+        assert lib.pa_attention_ex(*a, 1.0, 1.0, bad, None, 0) == 1
     assert lib.pa_attention_ex(*(a[:15] + [96] + a[16:]), 1.0, 1.0, 1, None, 0) == 2
     assert lib.pa_kernel_launches() == before
 
