@@ -66,6 +66,11 @@ __global__ void __launch_bounds__(rows::kRThreads, 1)
   if (!plan_ok(p)) return;
   if ((int)blockIdx.x < p.plan.header[kHeaderPrefillCtas]) {
     rows::rows_bf16_cta<D>(p, &tmK, &tmV, dsmem);
+    // out of prefill-row items: once every copy of that role has landed
+    // (its TMA warp waits for them before it returns), its shared memory
+    // serves decode items
+    __syncthreads();
+    if (threadIdx.x < kDecWarps * 32) decode_bf16_warps<D, NT, false, kDecWarps>(p, &tmK, &tmV, dsmem);
   } else if (threadIdx.x < kDecWarps * 32) {
     decode_bf16_warps<D, NT, false, kDecWarps>(p, &tmK, &tmV, dsmem);
   }

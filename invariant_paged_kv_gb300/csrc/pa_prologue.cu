@@ -228,8 +228,11 @@ __device__ bool row_counts(const StepParams& p, const LaneCache* lc, int u, int&
 // that balances the two roles' times, from the step's work totals and per-SM
 // rates measured on this part with the roles running side by side -- the
 // decode role streams ~66 GB/s per SM up to ~6760 GB/s in all; the prefill
-// role runs pf_rate flop/s per SM (~6.0 TFLOP/s for the tensor-core prefill,
-// ~1.0 TFLOP/s for the row-invariant mode's prefill rows on mma.sync). fp32
+// role runs pf_rate flop/s per SM (6.5 TFLOP/s for the tensor-core prefill,
+// 0.8 TFLOP/s for the row-invariant mode's prefill rows on mma.sync: the
+// values that gave the shortest launch in sweeps on the mixed step, a little
+// under the roles' own rates because a prefill CTA that runs out of work
+// takes decode items while a decode CTA cannot help the prefill). fp32
 // (the part's fp64 rate is low); it decides only where work runs, never its
 // result.
 __device__ int prefill_role_ctas(const StepParams& p, long long split_keys, long long pf_work,
@@ -482,10 +485,10 @@ __device__ void build_plan(const StepParams& p) {
     *header_total(pl, kHeaderPrefillWork) = overflow ? 0 : s_mix[1];
     pl.header[kHeaderPrefillCtas] =
         (overflow || !mixed) ? 0
-        : p.group_rows ? prefill_role_ctas(p, s_mix[0], s_mix[1], total[4] * p.Hkv, 1.0e12f,
+        : p.group_rows ? prefill_role_ctas(p, s_mix[0], s_mix[1], total[4] * p.Hkv, 0.8e12f,
                                            p.sm_count)
                        : prefill_role_ctas(p, s_mix[0], s_mix[1], (long long)n * p.H,
-                                           6.0e12f, p.sm_count);
+                                           6.5e12f, p.sm_count);
   }
 }
 
