@@ -114,8 +114,11 @@ typedef enum { PA_F32 = 0, PA_BF16 = 1, PA_FP8_E4M3 = 2 } pa_dtype;
  *                            the new rows, q, the caches, block tables, out)
  *                            is this call's own. The library checks the
  *                            sizes on the device: on a mismatch it raises
- *                            PA_FLAG_PLAN_MISMATCH and writes no output (the
- *                            write of new rows still happens). Changed
+ *                            PA_FLAG_PLAN_MISMATCH, writes no output (the
+ *                            write of new rows still happens) and discards
+ *                            the stored plan, so later reusing calls are
+ *                            refused too until a call without the bit plans
+ *                            again. Changed
  *                            contents of cu_seqlens_q / ctx_lens are not
  *                            detected: the caller must then plan again
  *                            (a call without the bit). Output bits are the

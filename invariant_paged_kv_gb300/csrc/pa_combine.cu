@@ -128,7 +128,6 @@ __device__ __forceinline__ void fold_row_head(const StepParams& p, int row, int4
 // measured faster there.
 template <int D, int kAhead, bool kRowMajor>
 __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p) {
-  if (!plan_ok(p)) return;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   if (kRowMajor) {
     const int hg_n = (p.H + kWarps - 1) / kWarps;
@@ -144,7 +143,10 @@ __global__ void __launch_bounds__(kWarps * 32) combine_kernel(const StepParams p
     fold_row_head<D, kAhead>(p, c.x, make_int4(c.y, c.z, c.w, w), h, lane);
   } else {
     // every flat row in order (no list: one dependent load less per CTA;
-    // rows that need no fold return in fold_row_head)
+    // rows that need no fold return in fold_row_head); row_info is only
+    // this call's when the plan is (the listed path needs no such test:
+    // a refused plan lists no rows)
+    if (!plan_ok(p)) return;
     const int h = blockIdx.y * kWarps + warp;
     if (h < p.H) fold_row_head<D, kAhead>(p, blockIdx.x, p.plan.row_info[blockIdx.x], h, lane);
   }

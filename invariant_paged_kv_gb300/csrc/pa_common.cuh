@@ -89,7 +89,8 @@ constexpr int kHeaderPrefillCtas = kHeaderPrefillWork + 2;
 constexpr int kHeaderCombineRows = kHeaderPrefillCtas + 1;
 // 1 when the plan in the workspace was built for this call's sizes (the
 // builder sets it; a call that reuses the plan sets it from the fingerprint
-// check); every kernel after the prologue does nothing when it is 0
+// check, and on a mismatch also empties the plan's item counts and combine
+// list, so the kernels after the prologue find no work)
 constexpr int kHeaderPlanOk = kHeaderCombineRows + 1;
 // the sizes the plan was built for (plan_fingerprint), compared by calls
 // that reuse it

@@ -13,7 +13,6 @@ __global__ void __launch_bounds__(kWarps * 32, 2)
     decode_bf16_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
                        const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t dsmem[];
-  if (!plan_ok(p)) return;
   decode_bf16_warps<D, NT, kOwner, kWarps>(p, &tmK, &tmV, dsmem);
 }
 

@@ -60,7 +60,6 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
   constexpr int SEG = D / 64;  // 16-byte K runs a thread reads per key row
   extern __shared__ uint8_t dsmem[];
   __shared__ __align__(8) uint64_t bars[kWarps][kStages];
-  if (!plan_ok(p)) return;
   __shared__ long long s_items[kWarps][kItemSlots];
 
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;

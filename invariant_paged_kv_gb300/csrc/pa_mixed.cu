@@ -33,7 +33,6 @@ __global__ void __launch_bounds__(pftc::kThreads, 1)
     mixed_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmQ,
                  const __grid_constant__ CUtensorMap tmK, const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t dsmem[];
-  if (!plan_ok(p)) return;
   if ((int)blockIdx.x < p.plan.header[kHeaderPrefillCtas]) {
     pftc::prefill_tc_cta<D>(p, &tmQ, &tmK, &tmV, dsmem);
     // out of prefill items (its copies landed, its products finished, its
@@ -63,7 +62,6 @@ __global__ void __launch_bounds__(rows::kRThreads, 1)
     row_mixed_kernel(const StepParams p, const __grid_constant__ CUtensorMap tmK,
                      const __grid_constant__ CUtensorMap tmV) {
   extern __shared__ uint8_t dsmem[];
-  if (!plan_ok(p)) return;
   if ((int)blockIdx.x < p.plan.header[kHeaderPrefillCtas]) {
     rows::rows_bf16_cta<D>(p, &tmK, &tmV, dsmem);
     // out of prefill-row items: once every copy of that role has landed

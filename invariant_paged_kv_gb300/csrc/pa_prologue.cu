@@ -568,7 +568,19 @@ __device__ void check_plan(const StepParams& p) {
   const int ok = __syncthreads_and(same ? 1 : 0);
   if (tid == 0) {
     pl.header[kHeaderPlanOk] = ok;
-    if (!ok) raise_flag(p.status, PA_FLAG_PLAN_MISMATCH);
+    if (!ok) {
+      // a refused plan offers the kernels after the prologue no work: every
+      // item count and the combine list are emptied (the split, prefill and
+      // prefill-row kernels find nothing to take; the combine walking flat
+      // rows tests kHeaderPlanOk)
+      raise_flag(p.status, PA_FLAG_PLAN_MISMATCH);
+      for (int i = 0; i < 4; ++i) pl.header[i] = 0;
+      pl.header[kHeaderPrefillCtas] = 0;
+      pl.header[kHeaderCombineRows] = 0;
+      // and it matches no later call either (B >= 1 in every call that
+      // reaches the device) until a call without the reuse bit plans again
+      pl.header[kHeaderFingerprint] = -1;
+    }
     for (int c = 0; c < kItemCounters; ++c) *item_counter(pl, c) = 0ull;
   }
 }

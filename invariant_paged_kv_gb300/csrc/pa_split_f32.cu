@@ -17,7 +17,6 @@ constexpr int kWarps = 4;
 
 template <int D, int GMAX>
 __global__ void __launch_bounds__(kWarps * 32) split_f32_kernel(const StepParams p) {
-  if (!plan_ok(p)) return;
   constexpr int DPL = D / 32;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   const int g = p.H / p.Hkv;

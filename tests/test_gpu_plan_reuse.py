@@ -72,6 +72,10 @@ def test_plan_of_other_sizes_is_refused():
     out_b, fb = run_attention(b, tb, workspace=ws, write=False, reuse_plan=True)
     assert fb == pa.FLAGS["PLAN_MISMATCH"], f"flags {fb:#x}"
     assert torch.isnan(out_b.float()).all(), "a refused call wrote output"
+    # the refusal discarded a's plan: reusing it for a is refused as well
+    out_a, fa2 = run_attention(a, ta, workspace=ws, write=False, reuse_plan=True)
+    assert fa2 == pa.FLAGS["PLAN_MISMATCH"], f"flags {fa2:#x}"
+    assert torch.isnan(out_a.float()).all(), "a refused call wrote output"
     # the next ordinary call plans again and matches a fresh workspace
     got, f2 = run_attention(b, tb, workspace=ws, write=False)
     ref, f3 = run_attention(b, tb, write=False)
