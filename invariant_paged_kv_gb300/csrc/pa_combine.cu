@@ -11,6 +11,12 @@
 // instead of ranks. n depends only on the row's own key count, so the fold is
 // the same whatever else is in the step. The quotient is multiplied by
 // out_scale (the V scale of e4m3 caches; 1, an exact no-op, otherwise).
+//
+// The split kernels store the partials with an evict-last L2 policy and read
+// keys evict-first, so the partials are still in L2 here; once folded, an
+// ordinary step's partials are dead, and the fold discards their L2 lines so
+// they are never written back to HBM (the next step's split kernel then
+// streams its keys without those write-backs).
 #include <type_traits>
 
 #include "pa_common.cuh"
@@ -115,6 +121,18 @@ __device__ __forceinline__ void fold_row_head(const StepParams& p, int row, int4
     uint32_t* out = reinterpret_cast<uint32_t*>(static_cast<__nv_bfloat16*>(p.out) + o);
 #pragma unroll
     for (int j = 0; j < VPL; j += 2) out[j / 2] = pack_bf16x2(r[j], r[j + 1]);
+  }
+  // an ordinary step's partials are dead once folded: drop their L2 lines
+  // without writing them back (each (split, head) row of D floats is this
+  // warp's alone, and every lane has used its loads)
+  if (p.partials_mode == 0) {
+    __syncwarp();
+    constexpr int kLines = D * (int)sizeof(float) / 128;
+    for (int i = lane / kLines; i < n; i += 32 / kLines) {
+      const int pair = i < nfull ? info.x + i : info.y;
+      const float* line = p.plan.acc + ((size_t)pair * p.H + h) * D + (lane % kLines) * (128 / sizeof(float));
+      asm volatile("discard.global.L2 [%0], 128;" ::"l"(line) : "memory");
+    }
   }
 }
 

@@ -113,10 +113,13 @@ __device__ __forceinline__ void decode_bf16_warps(const StepParams& p, const CUt
       const uint32_t ks = wbase + stage * TL::kStageBytes;
       const uint32_t vs = ks + TL::kBytes;
       mbar_expect_tx(bar[stage], TL::kStageBytes);
+      // keys are read once: their L2 lines go first, so the split partials
+      // (stored evict-last) are still in L2 when the combine reads them
+      const uint64_t pol = l2_evict_first();
 #pragma unroll
       for (int h = 0; h < TL::kHalves; ++h) {
-        tma_load_3d(ks + h * TL::kHalfBytes, tmK, h * 64, pi.kvh, tok, bar[stage]);
-        tma_load_3d(vs + h * TL::kHalfBytes, tmV, h * 64, pi.kvh, tok, bar[stage]);
+        tma_load_3d_hint(ks + h * TL::kHalfBytes, tmK, h * 64, pi.kvh, tok, bar[stage], pol);
+        tma_load_3d_hint(vs + h * TL::kHalfBytes, tmV, h * 64, pi.kvh, tok, bar[stage], pol);
       }
     }
     ++issued;

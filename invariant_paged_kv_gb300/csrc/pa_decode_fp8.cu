@@ -391,7 +391,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
               const int d = TL::kBPT * gid + 2 * mt + (r >> 1);
-              p.plan.acc[(ph0 + hl) * D + d] = o[mt][nt][r];
+              st_hint(p.plan.acc + (ph0 + hl) * D + d, o[mt][nt][r], l2_evict_last());
             }
           }
         }
@@ -401,7 +401,7 @@ __global__ void __launch_bounds__(kWarps * 32, 3)
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int hl = nt * 8 + 2 * tig + e;
-            if (hl < g) p.plan.ml[ph0 + hl] = make_float2(m[nt][e], l[nt][e]);
+            if (hl < g) st_hint(p.plan.ml + ph0 + hl, make_float2(m[nt][e], l[nt][e]), l2_evict_last());
           }
       }
     }

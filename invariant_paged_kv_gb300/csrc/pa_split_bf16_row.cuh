@@ -139,7 +139,8 @@ struct RowAcc {
 #pragma unroll
             for (int mt = 0; mt < KS; ++mt) {
               const int d = mt * 16 + gid + (r >> 1) * 8;
-              p.plan.acc[(ph0 + hl) * D + d] = o[mt][nt][r];
+              // kept in L2 for the combine, which reads them soon after
+              st_hint(p.plan.acc + (ph0 + hl) * D + d, o[mt][nt][r], l2_evict_last());
             }
           }
         }
@@ -149,7 +150,7 @@ struct RowAcc {
 #pragma unroll
           for (int e = 0; e < 2; ++e) {
             const int hl = nt * 8 + 2 * tig + e;
-            if (hl < g) p.plan.ml[ph0 + hl] = make_float2(m[nt][e], l[nt][e]);
+            if (hl < g) st_hint(p.plan.ml + ph0 + hl, make_float2(m[nt][e], l[nt][e]), l2_evict_last());
           }
       }
     }

@@ -94,9 +94,9 @@ __global__ void __launch_bounds__(kWarps * 32) split_f32_kernel(const StepParams
           if (single)
             out[(head0 + h) * D + lane + 32 * i] = finish_div(acc[h][i], l[h]);
           else
-            p.plan.acc[(ph0 + h) * D + lane + 32 * i] = acc[h][i];
+            st_hint(p.plan.acc + (ph0 + h) * D + lane + 32 * i, acc[h][i], l2_evict_last());
         }
-        if (!single && lane == 0) p.plan.ml[ph0 + h] = make_float2(m[h], l[h]);
+        if (!single && lane == 0) st_hint(p.plan.ml + ph0 + h, make_float2(m[h], l[h]), l2_evict_last());
       }
     }
   }
