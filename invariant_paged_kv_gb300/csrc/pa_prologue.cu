@@ -228,7 +228,7 @@ __device__ bool row_counts(const StepParams& p, const LaneCache* lc, int u, int&
 // that balances the two roles' times, from the step's work totals and per-SM
 // rates measured on this part with the roles running side by side -- the
 // decode role streams ~66 GB/s per SM up to ~6760 GB/s in all; the prefill
-// role runs pf_rate flop/s per SM (6.5 TFLOP/s for the tensor-core prefill,
+// role runs pf_rate flop/s per SM (7.0 TFLOP/s for the tensor-core prefill,
 // 0.8 TFLOP/s for the row-invariant mode's prefill rows on mma.sync: the
 // values that gave the shortest launch in sweeps on the mixed step, a little
 // under the roles' own rates because a prefill CTA that runs out of work
@@ -488,7 +488,7 @@ __device__ void build_plan(const StepParams& p) {
         : p.group_rows ? prefill_role_ctas(p, s_mix[0], s_mix[1], total[4] * p.Hkv, 0.8e12f,
                                            p.sm_count)
                        : prefill_role_ctas(p, s_mix[0], s_mix[1], (long long)n * p.H,
-                                           6.5e12f, p.sm_count);
+                                           7.0e12f, p.sm_count);
   }
 }
 
