@@ -229,7 +229,7 @@ __device__ bool row_counts(const StepParams& p, const LaneCache* lc, int u, int&
 // rates measured on this part with the roles running side by side -- the
 // decode role streams ~66 GB/s per SM up to ~6760 GB/s in all; the prefill
 // role runs pf_rate flop/s per SM (7.0 TFLOP/s for the tensor-core prefill,
-// 0.8 TFLOP/s for the row-invariant mode's prefill rows on mma.sync: the
+// 0.9 TFLOP/s for the row-invariant mode's prefill rows on mma.sync: the
 // values that gave the shortest launch in sweeps on the mixed step, a little
 // under the roles' own rates because a prefill CTA that runs out of work
 // takes decode items while a decode CTA cannot help the prefill). fp32
@@ -485,7 +485,7 @@ __device__ void build_plan(const StepParams& p) {
     *header_total(pl, kHeaderPrefillWork) = overflow ? 0 : s_mix[1];
     pl.header[kHeaderPrefillCtas] =
         (overflow || !mixed) ? 0
-        : p.group_rows ? prefill_role_ctas(p, s_mix[0], s_mix[1], total[4] * p.Hkv, 0.8e12f,
+        : p.group_rows ? prefill_role_ctas(p, s_mix[0], s_mix[1], total[4] * p.Hkv, 0.9e12f,
                                            p.sm_count)
                        : prefill_role_ctas(p, s_mix[0], s_mix[1], (long long)n * p.H,
                                            7.0e12f, p.sm_count);
