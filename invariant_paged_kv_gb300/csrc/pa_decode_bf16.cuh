@@ -153,7 +153,7 @@ __device__ __forceinline__ void decode_bf16_warps(const StepParams& p, const CUt
     for (int ch = 0; ch < it.nchunks; ++ch) {
       const int stage = consumed % kStages;
       const uint32_t parity = (consumed / kStages) & 1u;
-      // every lane waits (so every lane sees the landed bytes); the verdict is
+      // every lane waits (so every lane sees the landed bytes); the outcome is
       // made warp-uniform before anyone acts on it
       const bool landed = __all_sync(0xffffffffu, mbar_wait_bounded(bar[stage], parity, p.wait_cycles));
       if (!landed) {

@@ -134,7 +134,7 @@ __device__ __forceinline__ bool wait_or_abort_1(uint32_t bar, uint32_t parity,
   }
 }
 
-// Every lane of the warp waits; the verdict is made warp-uniform.
+// Every lane of the warp waits; the outcome is made warp-uniform.
 __device__ __forceinline__ bool wait_or_abort(uint32_t bar, uint32_t parity,
                                               volatile int* abort_flag, int* status,
                                               long long limit) {

@@ -127,7 +127,7 @@ __device__ __forceinline__ void owned_splits(const StepParams& p, int b, int sl,
 }
 
 // Steps of up to kLaneCache lanes keep cu_seqlens_q, ctx_lens and each lane's
-// verdict in shared memory while the plan is built; larger ones read global
+// validity in shared memory while the plan is built; larger ones read global
 // memory.
 constexpr int kLaneCache = 1024;
 struct LaneCache {
