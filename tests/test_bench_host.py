@@ -87,3 +87,16 @@ def test_reference_arm_runs_on_rank_zero_only():
                        env=env, capture_output=True, text=True, timeout=120)
     assert r.returncode == 0, r.stderr
     assert r.stdout.strip() == ""
+
+
+def test_config_records_how_the_plan_is_built(monkeypatch):
+    """The line's config says whether layers 2.. of a step reuse the first
+    layer's split plan (the default) or plan in every call (--no-plan-reuse)."""
+    from invariant_paged_kv_gb300 import workload as wl
+    step = wl.decode_batch(0, lanes=4)
+    for argv, reused in ((["bench.py"], True), (["bench.py", "--no-plan-reuse"], False)):
+        monkeypatch.setattr(sys, "argv", argv)
+        args = bench.parse()
+        cfg = bench.workload_config(step, 4, "decode_batch", args)
+        assert ("reused" in cfg["plan"]) == reused, cfg["plan"]
+        assert args.no_secondary is False
